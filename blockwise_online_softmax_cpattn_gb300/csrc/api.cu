@@ -1,0 +1,339 @@
+// The C ABI of libcpattn: argument validation, dispatch to the kernels, the
+// per-device status word, tensor-map encoding and kernel timing.
+#include <math.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/cpattn.h"
+#include "kernels.h"
+
+// Device status word (one per device that loads the library): the first error a
+// kernel detects (a bounded wait that ran out) is latched here; cpattn_check
+// reads and clears it.
+static __device__ int g_cpattn_status;
+
+namespace cpattn {
+
+// ---------------------------------------------------------------------------
+// status word address per device
+// ---------------------------------------------------------------------------
+static std::mutex g_mu;
+static int* g_status_ptr[128];
+
+static int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_cpattn_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry point)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][inner], box [box_rows][box_inner], 128-byte swizzle.
+CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                             uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// ---------------------------------------------------------------------------
+// kernel timing
+// ---------------------------------------------------------------------------
+struct TimingEntry {
+  std::string name;
+  double total_ms = 0;
+  int64_t launches = 0;
+};
+struct PendingTiming {
+  int idx;
+  cudaEvent_t a, b;
+};
+static bool g_timing = false;
+static std::vector<TimingEntry> g_entries;
+static std::vector<PendingTiming> g_pending;
+static thread_local int t_open = -1;
+
+void timing_begin(const char* name, cudaStream_t st) {
+  if (!g_timing) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int idx = -1;
+  for (size_t i = 0; i < g_entries.size(); ++i)
+    if (g_entries[i].name == name) idx = (int)i;
+  if (idx < 0) {
+    g_entries.push_back(TimingEntry{name, 0.0, 0});
+    idx = (int)g_entries.size() - 1;
+  }
+  PendingTiming p{idx, nullptr, nullptr};
+  if (cudaEventCreate(&p.a) != cudaSuccess || cudaEventCreate(&p.b) != cudaSuccess) return;
+  cudaEventRecord(p.a, st);
+  g_pending.push_back(p);
+  t_open = (int)g_pending.size() - 1;
+}
+
+void timing_end(cudaStream_t st) {
+  if (!g_timing || t_open < 0) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (t_open < (int)g_pending.size()) cudaEventRecord(g_pending[t_open].b, st);
+  t_open = -1;
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+static bool aligned16(const void* p) { return p && ((uintptr_t)p % 16 == 0); }
+
+static cpattn_status validate(const cpattn_desc* d, Ring* R) {
+  if (!d) return CPATTN_ERR_INVALID_ARG;
+  if (d->B <= 0 || d->H_q <= 0 || d->H_kv <= 0 || d->T <= 0 || d->D <= 0 || d->cp <= 0 ||
+      d->a2a <= 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (d->H_q % d->H_kv || d->cp % d->a2a || d->H_q % d->a2a || d->H_kv % d->a2a)
+    return CPATTN_ERR_INVALID_ARG;
+  if (d->layout != CPATTN_CONTIGUOUS && d->layout != CPATTN_ZIGZAG) return CPATTN_ERR_INVALID_ARG;
+  if (d->dtype != CPATTN_F32 && d->dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  if (!(d->scale > 0.f) || !isfinite(d->scale)) return CPATTN_ERR_INVALID_ARG;
+  if (d->causal != 1) return CPATTN_ERR_UNSUPPORTED;
+  if (d->D > 128) return CPATTN_ERR_UNSUPPORTED;
+  const int p2p = d->cp / d->a2a;
+  if (d->T % p2p) return CPATTN_ERR_INVALID_ARG;
+  if (d->layout == CPATTN_ZIGZAG && d->T % (2 * p2p)) return CPATTN_ERR_INVALID_ARG;
+  const double elems = (double)d->B * d->H_q * d->T * d->D;
+  if (elems > 4.0e18 || d->T > (1 << 30)) return CPATTN_ERR_UNSUPPORTED;
+  if (R) {
+    R->B = d->B * d->a2a;
+    R->Hq = d->H_q / d->a2a;
+    R->Hkv = d->H_kv / d->a2a;
+    R->T = d->T;
+    R->D = d->D;
+    R->cp = p2p;
+    R->zz = d->layout == CPATTN_ZIGZAG;
+    R->scale = d->scale;
+    R->bf16 = d->dtype == CPATTN_BF16;
+    R->debug_fault = d->debug_fault;
+  }
+  return CPATTN_OK;
+}
+
+static cpattn_status from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" {
+
+cpattn_status cpattn_partial_fwd(const cpattn_desc* desc, int q_rank, int kv_rank,
+                                 const void* q, const void* k, const void* v, float* o_part,
+                                 float* lse_part, void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if (q_rank < 0 || q_rank >= R.cp || kv_rank < 0 || kv_rank >= R.cp)
+    return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) || !aligned16(lse_part))
+    return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  if (R.bf16 && tc_supported(R))
+    return from_cuda(launch_tc_fwd(R, q_rank, kv_rank, q, k, v, o_part, lse_part, status_ptr(), st));
+  return from_cuda(launch_simt_fwd(R, q_rank, kv_rank, q, k, v, o_part, lse_part, st));
+}
+
+cpattn_status cpattn_merge(int64_t rows, int D, const float* o_a, const float* lse_a,
+                           const float* o_b, const float* lse_b, float* o_out, float* lse_out,
+                           void* stream) {
+  if (rows < 0 || D <= 0) return CPATTN_ERR_INVALID_ARG;
+  if (rows == 0) return CPATTN_OK;
+  if (!aligned16(o_a) || !aligned16(lse_a) || !aligned16(o_b) || !aligned16(lse_b) ||
+      !aligned16(o_out) || !aligned16(lse_out))
+    return CPATTN_ERR_INVALID_ARG;
+  cudaGetLastError();
+  return from_cuda(launch_merge(rows, D, o_a, lse_a, o_b, lse_b, o_out, lse_out,
+                                (cudaStream_t)stream));
+}
+
+cpattn_status cpattn_ring_fwd(const cpattn_desc* desc, const void* q, const void* k,
+                              const void* v, void* o, float* lse, void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  if (R.bf16 && tc_supported(R))
+    return from_cuda(launch_tc_fwd(R, -1, -1, q, k, v, o, lse, status_ptr(), st));
+  return from_cuda(launch_simt_fwd(R, -1, -1, q, k, v, o, lse, st));
+}
+
+size_t cpattn_ring_bwd_workspace(const cpattn_desc* desc) {
+  if (validate(desc, nullptr) != CPATTN_OK) return 0;
+  const size_t rows = (size_t)desc->B * desc->H_q * desc->T;
+  return (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void* k,
+                              const void* v, const void* o, const float* lse, const void* dO,
+                              void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(workspace))
+    return CPATTN_ERR_INVALID_ARG;
+  if (ws_bytes < cpattn_ring_bwd_workspace(desc)) return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  float* delta = static_cast<float*>(workspace);
+  const int64_t rows = (int64_t)R.B * R.Hq * R.T;
+  cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, delta, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  if (R.bf16 && tc_supported(R))
+    return from_cuda(launch_tc_bwd(R, q, k, v, lse, delta, dO, dq, dk, dv, status_ptr(), st));
+  e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  return from_cuda(launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st));
+}
+
+cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* src, void* dst,
+                            int n_heads, void* stream) {
+  cpattn_status s = validate(desc, nullptr);
+  if (s != CPATTN_OK) return s;
+  if (permute < CPATTN_ZIGZAG_FWD || permute > CPATTN_A2A_INV || n_heads <= 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst) || src == dst) return CPATTN_ERR_INVALID_ARG;
+  PermuteArgs a;
+  a.kind = permute;
+  a.B = desc->B;
+  a.H = n_heads;
+  a.T = desc->T;
+  a.D = desc->D;
+  a.elt = desc->dtype == CPATTN_BF16 ? 2 : 4;
+  a.cp = desc->cp;
+  a.a2a = desc->a2a;
+  a.zz = desc->layout == CPATTN_ZIGZAG;
+  if (permute >= CPATTN_A2A_FWD) {
+    if (n_heads % desc->a2a || desc->T % desc->cp) return CPATTN_ERR_INVALID_ARG;
+    if (a.zz && desc->T % (2 * desc->cp)) return CPATTN_ERR_INVALID_ARG;
+  } else {
+    // zigzag permutes act on [B * n_heads] sequences of T tokens over the ring's ranks
+  }
+  cudaGetLastError();
+  return from_cuda(launch_permute(a, src, dst, (cudaStream_t)stream));
+}
+
+cpattn_status cpattn_check(void* stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CPATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_cpattn_status, sizeof(int)) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  if (v != 0) {
+    int zero = 0;
+    if (cudaMemcpyToSymbol(g_cpattn_status, &zero, sizeof(int)) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+  }
+  if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_CUDA;
+  return v == 0 ? CPATTN_OK : (cpattn_status)v;
+}
+
+const char* cpattn_status_string(cpattn_status status) {
+  switch (status) {
+    case CPATTN_OK: return "ok";
+    case CPATTN_ERR_INVALID_ARG: return "invalid argument";
+    case CPATTN_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case CPATTN_ERR_CUDA: return "CUDA error";
+    case CPATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+cpattn_status cpattn_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timing = on != 0;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_timing_collect(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  cpattn_status s = CPATTN_OK;
+  for (auto& p : g_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.b) == cudaSuccess && cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      g_entries[p.idx].total_ms += ms;
+      g_entries[p.idx].launches += 1;
+    } else {
+      s = CPATTN_ERR_CUDA;
+    }
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  g_pending.clear();
+  return s;
+}
+
+int cpattn_timing_count(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return (int)g_entries.size();
+}
+
+cpattn_status cpattn_timing_get(int index, const char** name, double* total_ms,
+                                int64_t* launches) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (index < 0 || index >= (int)g_entries.size()) return CPATTN_ERR_INVALID_ARG;
+  if (name) *name = g_entries[index].name.c_str();
+  if (total_ms) *total_ms = g_entries[index].total_ms;
+  if (launches) *launches = g_entries[index].launches;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_timing_reset(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& p : g_pending) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  g_pending.clear();
+  g_entries.clear();
+  return CPATTN_OK;
+}
+
+}  // extern "C"

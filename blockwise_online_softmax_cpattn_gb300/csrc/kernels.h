@@ -1,0 +1,66 @@
+// Host-side launchers of the library's kernels (internal to libcpattn).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace cpattn {
+
+// The ring problem one launch solves, after the a2a split of the hierarchical
+// mode has been folded into the batch (B = a2a * B_user, heads / a2a, cp / a2a).
+struct Ring {
+  int B, Hq, Hkv, T, D, cp, zz;
+  float scale;
+  int bf16;          // 1: bf16 tensors, 0: f32
+  int debug_fault;
+};
+
+// ---- layout.cu -------------------------------------------------------------
+enum PermuteKind { kZigzagFwd = 0, kZigzagInv = 1, kA2AFwd = 2, kA2AInv = 3 };
+struct PermuteArgs {
+  int kind;
+  int B, H, T, D, elt;     // elt = element bytes
+  int cp, a2a, zz;         // cp = ranks of the token shards; ring ranks = cp / a2a
+};
+cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cudaStream_t st);
+
+// ---- merge.cu --------------------------------------------------------------
+cudaError_t launch_merge(int64_t rows, int D, const float* oa, const float* la, const float* ob,
+                         const float* lb, float* oo, float* lo, cudaStream_t st);
+// delta[row] = sum_d dO[row, d] * O[row, d] (float32 accumulation)
+cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const void* dO,
+                         float* delta, cudaStream_t st);
+
+// ---- simt_attn.cu (exact float32 / any-D path) ------------------------------
+// partial: q_rank >= 0 selects one rank's queries against kv_rank's chunk and
+// writes float32 o/lse of c rows per (b, h); q_rank < 0 runs the whole ring and
+// writes o in the tensor dtype.
+cudaError_t launch_simt_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
+                            const void* v, void* o, float* lse, cudaStream_t st);
+cudaError_t launch_simt_bwd_dq(const Ring& R, const void* q, const void* k, const void* v,
+                               const float* lse, const float* delta, const void* dO, void* dq,
+                               cudaStream_t st);
+cudaError_t launch_simt_bwd_dkdv(const Ring& R, const void* q, const void* k, const void* v,
+                                 const float* lse, const float* delta, const void* dO, void* dk,
+                                 void* dv, cudaStream_t st);
+
+// ---- tc_fwd.cu / tc_bwd.cu (bf16 tcgen05 path, D in {64, 128}) --------------
+bool tc_supported(const Ring& R);
+cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
+                          const void* v, void* o, float* lse, int* status, cudaStream_t st);
+cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
+                          const float* lse, const float* delta, const void* dO, void* dq,
+                          void* dk, void* dv, int* status, cudaStream_t st);
+
+// ---- api.cu: kernel timing hooks -------------------------------------------
+void timing_begin(const char* name, cudaStream_t st);
+void timing_end(cudaStream_t st);
+
+// Tensor-map encoder (driver entry point fetched through the runtime).
+CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                             uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace cpattn

@@ -1,0 +1,114 @@
+// Layout permutes: the zigzag token map and the all-to-all head<->sequence
+// re-layout of the hierarchical mode, as row gathers with 16-byte vectors.
+//
+// Every destination row (D elements) is copied from one source row; threads
+// walk the destination in order, so stores are fully coalesced and each source
+// row is read as one contiguous run.  Pure copies: bit-exact by construction.
+#include "kernels.h"
+
+namespace cpattn {
+
+struct PermuteDev {
+  int kind, B, H, T, a2a, Hs, c_src;
+  SeqMap ring;   // layout map over the ring's ranks (zigzag permutes; a2a destination)
+  SeqMap shard;  // layout map over all cp ranks (a2a source shards)
+};
+
+// Source row of destination row `row`.
+__device__ __forceinline__ int64_t permute_src_row(const PermuteDev& p, int64_t row) {
+  switch (p.kind) {
+    case kZigzagFwd: {  // dst [b][h][slot] <- src [b][h][pos(slot)]
+      int64_t bh = row / p.T;
+      int t = (int)(row - bh * p.T);
+      return bh * p.T + p.ring.pos(t);
+    }
+    case kZigzagInv: {  // dst [b][h][pos] <- src [b][h][slot(pos)]
+      int64_t bh = row / p.T;
+      int t = (int)(row - bh * p.T);
+      return bh * p.T + p.ring.slot(t);
+    }
+    case kA2AFwd: {  // dst [j][b][hh][t] <- src [r][b][w][h]
+      int t = (int)(row % p.T);
+      int64_t rest = row / p.T;
+      int hh = (int)(rest % p.Hs);
+      rest /= p.Hs;
+      int b = (int)(rest % p.B);
+      int j = (int)(rest / p.B);
+      int pos = p.ring.pos(t);
+      int s = p.shard.slot(pos);
+      int r = s / p.c_src, w = s - r * p.c_src;
+      return (((int64_t)r * p.B + b) * p.c_src + w) * p.H + (j * p.Hs + hh);
+    }
+    default: {  // kA2AInv: dst [r][b][w][h] <- src [j][b][hh][t]
+      int h = (int)(row % p.H);
+      int64_t rest = row / p.H;
+      int w = (int)(rest % p.c_src);
+      rest /= p.c_src;
+      int b = (int)(rest % p.B);
+      int r = (int)(rest / p.B);
+      int pos = p.shard.pos(r * p.c_src + w);
+      int t = p.ring.slot(pos);
+      int j = h / p.Hs, hh = h - j * p.Hs;
+      return (((int64_t)j * p.B + b) * p.Hs + hh) * p.T + t;
+    }
+  }
+}
+
+template <typename V>
+__global__ void __launch_bounds__(256) permute_kernel(PermuteDev p, const V* __restrict__ src,
+                                                      V* __restrict__ dst, int64_t rows,
+                                                      int vpr) {
+  const int64_t total = rows * (int64_t)vpr;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t row = i / vpr;
+    int v = (int)(i - row * vpr);
+    int64_t s = permute_src_row(p, row);
+    dst[i] = __ldcs(src + s * vpr + v);
+  }
+}
+
+template <typename V>
+static cudaError_t run(const PermuteDev& p, const void* src, void* dst, int64_t rows, int vpr,
+                       cudaStream_t st) {
+  int64_t total = rows * vpr;
+  int64_t blocks = (total + 255) / 256;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t cap = (int64_t)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  permute_kernel<V><<<(unsigned)blocks, 256, 0, st>>>(p, (const V*)src, (V*)dst, rows, vpr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cudaStream_t st) {
+  PermuteDev p;
+  p.kind = a.kind;
+  p.B = a.B;
+  p.H = a.H;
+  p.T = a.T;
+  p.a2a = a.a2a;
+  p.Hs = a.H / a.a2a;
+  p.c_src = a.T / a.cp;
+  p.ring = SeqMap::make(a.T, a.cp / a.a2a, a.zz);
+  p.shard = SeqMap::make(a.T, a.cp, a.zz);
+  const int64_t rows = (int64_t)a.B * a.H * a.T;
+  const int row_bytes = a.D * a.elt;
+  const uintptr_t al = (uintptr_t)src | (uintptr_t)dst;
+  timing_begin(a.kind <= kZigzagInv ? "layout_zigzag" : "layout_a2a", st);
+  cudaError_t e;
+  if (row_bytes % 16 == 0 && al % 16 == 0)
+    e = run<int4>(p, src, dst, rows, row_bytes / 16, st);
+  else if (row_bytes % 8 == 0 && al % 8 == 0)
+    e = run<int2>(p, src, dst, rows, row_bytes / 8, st);
+  else if (row_bytes % 4 == 0 && al % 4 == 0)
+    e = run<int>(p, src, dst, rows, row_bytes / 4, st);
+  else
+    e = run<short>(p, src, dst, rows, row_bytes / 2, st);
+  timing_end(st);
+  return e;
+}
+
+}  // namespace cpattn

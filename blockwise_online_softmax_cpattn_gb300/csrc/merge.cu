@@ -1,0 +1,129 @@
+// (O, LSE) merge of two partial results, and the backward pre-pass
+// Delta = rowsum(dO * O).  Both are HBM-bound row kernels: one warp per row,
+// 16-byte vector accesses, float32 arithmetic.
+#include <math.h>
+
+#include "kernels.h"
+
+namespace cpattn {
+
+// Online-softmax merge (tutorial "上下文并行", section "朴素 Ring Attention": the
+// block order is free as long as the current output, max and sum are carried).
+// lse = m + ln(e^(la-m) + e^(lb-m)) with m = max(la, lb); an operand with
+// lse = -inf contributes nothing; two empty operands give (0, -inf).
+// All lanes read both LSEs before lane 0 overwrites lse_out (which may alias
+// lse_a or lse_b); o_out[i] depends only on o_a[i], o_b[i].
+template <bool VEC4>
+__global__ void __launch_bounds__(256) merge_kernel(int64_t rows, int D,
+                                                    const float* oa, const float* la,
+                                                    const float* ob, const float* lb,
+                                                    float* oo, float* lo) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const float a = la[row], b = lb[row];
+    const float m = fmaxf(a, b);
+    float wa = 0.f, wb = 0.f, lse = -INFINITY;
+    if (m != -INFINITY) {
+      const float ea = expf(a - m), eb = expf(b - m);
+      const float s = ea + eb;
+      wa = ea / s;
+      wb = eb / s;
+      lse = m + logf(s);
+    }
+    const int64_t base = row * (int64_t)D;
+    if (VEC4) {
+      const float4* pa = reinterpret_cast<const float4*>(oa + base);
+      const float4* pb = reinterpret_cast<const float4*>(ob + base);
+      float4* po = reinterpret_cast<float4*>(oo + base);
+      for (int i = lane; i < D / 4; i += 32) {
+        float4 x = pa[i], y = pb[i], z;
+        z.x = wa * x.x + wb * y.x;
+        z.y = wa * x.y + wb * y.y;
+        z.z = wa * x.z + wb * y.z;
+        z.w = wa * x.w + wb * y.w;
+        po[i] = z;
+      }
+    } else {
+      for (int i = lane; i < D; i += 32) oo[base + i] = wa * oa[base + i] + wb * ob[base + i];
+    }
+    __syncwarp();
+    if (lane == 0) lo[row] = lse;
+  }
+}
+
+cudaError_t launch_merge(int64_t rows, int D, const float* oa, const float* la, const float* ob,
+                         const float* lb, float* oo, float* lo, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+  timing_begin("merge", st);
+  if (D % 4 == 0)
+    merge_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(rows, D, oa, la, ob, lb, oo, lo);
+  else
+    merge_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(rows, D, oa, la, ob, lb, oo, lo);
+  cudaError_t e = cudaGetLastError();
+  timing_end(st);
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ld_f(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) delta_kernel(int64_t rows, int D, const T* __restrict__ o,
+                                                    const T* __restrict__ dO,
+                                                    float* __restrict__ delta) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const int64_t base = row * (int64_t)D;
+    float acc = 0.f;
+    constexpr int kVec = 16 / sizeof(T);
+    if (D % kVec == 0) {
+      for (int i = lane * kVec; i < D; i += 32 * kVec) {
+        int4 a = *reinterpret_cast<const int4*>(o + base + i);
+        int4 b = *reinterpret_cast<const int4*>(dO + base + i);
+        const T* pa = reinterpret_cast<const T*>(&a);
+        const T* pb = reinterpret_cast<const T*>(&b);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) acc += ld_f(pa, k) * ld_f(pb, k);
+      }
+    } else {
+      for (int i = lane; i < D; i += 32) acc += ld_f(o, base + i) * ld_f(dO, base + i);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) delta[row] = acc;
+  }
+}
+
+cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const void* dO,
+                         float* delta, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+  if (blocks < 1) blocks = 1;
+  timing_begin("bwd_delta", st);
+  if (bf16)
+    delta_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
+        rows, D, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, delta);
+  else
+    delta_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(rows, D, (const float*)o,
+                                                          (const float*)dO, delta);
+  cudaError_t e = cudaGetLastError();
+  timing_end(st);
+  return e;
+}
+
+}  // namespace cpattn

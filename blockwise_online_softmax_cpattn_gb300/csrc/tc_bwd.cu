@@ -1,0 +1,725 @@
+// Ring-attention backward on the 5th-generation tensor cores (sm_103a).
+//
+// The pull request "Feat: Context Parallel" #181 (mode "p2p") computes the ring
+// backward by recomputing the probabilities from the saved statistics and
+// sending each K/V chunk's gradient around the ring back to its owner.  On one
+// GPU the same sums are formed by two kernels, neither of which needs atomics:
+//
+//  dkdv_kernel  one CTA per 128-row K/V tile (K/V stationary in shared memory).
+//               It walks the query tiles that can see it, in the order the
+//               chunk's gradient travels the ring (ranks s, s+1, ..., s-1), for
+//               every query head of its group, so the grouped-query sum over the
+//               n_rep heads (the reverse of RepeatKVHeads) happens in the TMEM
+//               accumulators:
+//                 S^T = K Q^T, dP^T = V dO^T          (SS MMAs, M = keys)
+//                 P^T = 2^(S^T scale log2e - LSE log2e), masked from positions
+//                 dS^T = P^T (dP^T - Delta)
+//                 dV += P^T dO, dK += dS^T Q          (TS MMAs, P^T/dS^T in TMEM)
+//               TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
+//  dq_kernel    one CTA per 128-row query tile (Q, dO stationary), walking the
+//               K/V tiles in ring order like the forward:
+//                 S = Q K^T, dP = dO V^T, dS = P (dP - Delta), dQ += dS K.
+//               TMEM: S [0,128), dP double-buffered [128,384), dQ [384, 384+D).
+//
+// Delta = rowsum(dO * O) comes from the pre-pass kernel (merge.cu).  Compute
+// warps: 8, warp w handles TMEM lane quadrant w%4 and column half (w-4)/4.
+// Every mbarrier wait is bounded (see tc_fwd.cu for the abort protocol).
+#include <math.h>
+
+#include "kernels.h"
+
+namespace cpattn {
+namespace tcbwd {
+
+constexpr int kTile = 128;
+constexpr int kThreads = 384;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+enum : int { kEmpty = 0, kFull = 1, kDiag = 2 };
+
+struct Params {
+  int B, Hq, Hkv, T, n_rep;
+  SeqMap m;
+  float scale, scale_log2;
+  const float* lse;
+  const float* delta;
+  void* out0;  // dkdv: dK ; dq: dQ
+  void* out1;  // dkdv: dV
+  int* status;
+};
+
+__device__ __forceinline__ int classify(int qpos0, int kpos0) {
+  if (kpos0 + kTile - 1 <= qpos0) return kFull;
+  if (kpos0 > qpos0 + kTile - 1) return kEmpty;
+  return kDiag;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t par, volatile int* abort,
+                                          int* status) {
+  bool ok = mbar_wait(bar, par, abort, status, kTimeoutNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t par) {
+  int never = 0;
+  return mbar_wait(bar, par, &never, nullptr, kDrainTimeoutNs);
+}
+
+// Store 32 consecutive fp32 values (times `mul`) of one row as bf16.
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                                 float mul) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 w;
+    w.x = pack_bf16(__uint_as_float(v[8 * j + 0]) * mul, __uint_as_float(v[8 * j + 1]) * mul);
+    w.y = pack_bf16(__uint_as_float(v[8 * j + 2]) * mul, __uint_as_float(v[8 * j + 3]) * mul);
+    w.z = pack_bf16(__uint_as_float(v[8 * j + 4]) * mul, __uint_as_float(v[8 * j + 5]) * mul);
+    w.w = pack_bf16(__uint_as_float(v[8 * j + 6]) * mul, __uint_as_float(v[8 * j + 7]) * mul);
+    d4[j] = w;
+  }
+}
+
+// ===========================================================================
+// dK / dV
+// ===========================================================================
+template <int D>
+struct DkdvSmem {
+  static constexpr int kStages = 2;
+  static constexpr int kTB = kTile * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kTB;
+  static constexpr int kQ = 2 * kTB;
+  static constexpr int kDO = kQ + kStages * kTB;
+  static constexpr int kLse = kDO + kStages * kTB;
+  static constexpr int kDelta = kLse + kStages * 512;
+  static constexpr int kBar = kDelta + kStages * 512;
+  // kv_full, q_full[S], do_full[S], qdo_empty[S], s_full, dp_full, p_full,
+  // ds_full, dv_done, dk_done, final
+  static constexpr int kNumBars = 1 + 3 * kStages + 7;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const Params p) {
+  using L = DkdvSmem<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + L::kBar;
+  const uint32_t kv_full = bars;
+  auto q_full = [&](int s) { return bars + 8 * (1 + s); };
+  auto do_full = [&](int s) { return bars + 8 * (1 + S + s); };
+  auto qdo_empty = [&](int s) { return bars + 8 * (1 + 2 * S + s); };
+  const uint32_t s_full = bars + 8 * (1 + 3 * S);
+  const uint32_t dp_full = s_full + 8;
+  const uint32_t p_full = s_full + 16;
+  const uint32_t ds_full = s_full + 24;
+  const uint32_t dv_done = s_full + 32;
+  const uint32_t dk_done = s_full + 40;
+  const uint32_t final_bar = s_full + 48;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) {
+      const uint32_t b = bars + 8 * i;
+      mbar_init(b, (b == p_full || b == ds_full) ? 256 : 1);
+    }
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // work item: kv tiles with the earliest positions (the most queries) first
+  const int units = p.B * p.Hkv;
+  const int ti = blockIdx.x / units;
+  const int rem = blockIdx.x - ti * units;
+  const int b = rem / p.Hkv, g = rem - (rem / p.Hkv) * p.Hkv;
+  const int kpos0 = ti * kTile;
+  const int kslot0 = p.m.slot(kpos0);
+  const int s_own = kslot0 / p.m.c;
+  const int c_tiles = p.m.c / kTile;
+  const int n_walk = p.m.cp * p.n_rep * c_tiles;
+  // query tile n of the walk: ring distance i, head hh of the group, tile t
+  auto q_tile = [&](int n, int& h, int& qslot0) {
+    const int i = n / (p.n_rep * c_tiles);
+    const int r2 = n - i * (p.n_rep * c_tiles);
+    const int hh = r2 / c_tiles, t = r2 - hh * c_tiles;
+    const int r = (s_own + i) % p.m.cp;
+    h = g * p.n_rep + hh;
+    qslot0 = r * p.m.c + t * kTile;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const int krow = (b * p.Hkv + g) * p.T + kslot0;
+      mbar_expect_tx(kv_full, 2 * L::kTB);
+      for (int kb = 0; kb < D / 64; ++kb) {
+        tma_load_2d(sbase + L::kK + kb * (kTile * 128), &tm_k, kb * 64, krow, kv_full);
+        tma_load_2d(sbase + L::kV + kb * (kTile * 128), &tm_v, kb * 64, krow, kv_full);
+      }
+      int stage = 0, par = 0, issued[S], ipar[S];
+      for (int s = 0; s < S; ++s) issued[s] = 0, ipar[s] = 0;
+      for (int n = 0; n < n_walk; ++n) {
+        int h, qslot0;
+        q_tile(n, h, qslot0);
+        if (classify(p.m.pos(qslot0), kpos0) == kEmpty) continue;
+        if (!mbar_wait(qdo_empty(stage), par ^ 1, abort, p.status, kTimeoutNs)) break;
+        const int qrow = (b * p.Hq + h) * p.T + qslot0;
+        mbar_expect_tx(q_full(stage), L::kTB + 1024);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_2d(sbase + L::kQ + stage * L::kTB + kb * (kTile * 128), &tm_q, kb * 64, qrow,
+                      q_full(stage));
+        bulk_load(sbase + L::kLse + stage * 512, p.lse + qrow, 512, q_full(stage));
+        bulk_load(sbase + L::kDelta + stage * 512, p.delta + qrow, 512, q_full(stage));
+        mbar_expect_tx(do_full(stage), L::kTB);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_2d(sbase + L::kDO + stage * L::kTB + kb * (kTile * 128), &tm_do, kb * 64, qrow,
+                      do_full(stage));
+        issued[stage] = 1;
+        ipar[stage] = par;
+        if (++stage == S) stage = 0, par ^= 1;
+      }
+      drain_wait(kv_full, 0);
+      for (int s = 0; s < S; ++s)
+        if (issued[s]) {
+          drain_wait(q_full(s), ipar[s]);
+          drain_wait(do_full(s), ipar[s]);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
+      bool ok = mbar_wait(kv_full, 0, abort, p.status, kTimeoutNs);
+      tc_fence_after();
+      int stage = 0, par = 0, cnt = 0;
+      for (int n = 0; n < n_walk && ok; ++n) {
+        int h, qslot0;
+        q_tile(n, h, qslot0);
+        if (classify(p.m.pos(qslot0), kpos0) == kEmpty) continue;
+        const uint32_t qa = sbase + L::kQ + stage * L::kTB;
+        const uint32_t da = sbase + L::kDO + stage * L::kTB;
+        // S^T = K Q^T  (the S region is free once the previous dV has read P^T)
+        if (!(ok = mbar_wait(q_full(stage), par, abort, p.status, kTimeoutNs))) break;
+        if (cnt > 0 && !(ok = mbar_wait(dv_done, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem, sdesc_sw128(sbase + L::kK + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                 kIdSS, kk > 0);
+        }
+        mma_commit(s_full);
+        // dP^T = V dO^T  (the dP region is free once the previous dK has read dS^T)
+        if (!(ok = mbar_wait(do_full(stage), par, abort, p.status, kTimeoutNs))) break;
+        if (cnt > 0 && !(ok = mbar_wait(dk_done, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem + 128, sdesc_sw128(sbase + L::kV + off, 16, 1024),
+                 sdesc_sw128(da + off, 16, 1024), kIdSS, kk > 0);
+        }
+        mma_commit(dp_full);
+        // dV += P^T dO
+        if (!(ok = mbar_wait(p_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acol = (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tmem + 256, tmem + acol, sdesc_sw128(da + kk * 2048, kTile * 128, 1024), kIdTS,
+                 (cnt > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(dv_done);
+        // dK += dS^T Q
+        if (!(ok = mbar_wait(ds_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acol = 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tmem + 256 + D, tmem + acol, sdesc_sw128(qa + kk * 2048, kTile * 128, 1024), kIdTS,
+                 (cnt > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(dk_done);
+        mma_commit(qdo_empty(stage));
+        ++cnt;
+        if (++stage == S) stage = 0, par ^= 1;
+      }
+      mma_commit(final_bar);
+      drain_wait(final_bar, 0);
+    }
+  } else if (warp >= 4) {
+    const int quad = warp & 3, half = (warp - 4) >> 2;
+    const int row = quad * 32 + lane;  // key row of the tile
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + half * 64;
+    const uint32_t t_dp = tmem + lane_off + 128 + half * 64;
+    const float* lse_s = reinterpret_cast<const float*>(smem + L::kLse);
+    const float* del_s = reinterpret_cast<const float*>(smem + L::kDelta);
+    int stage = 0, par = 0, cnt = 0;
+    bool ok = true;
+    for (int n = 0; n < n_walk; ++n) {
+      int h, qslot0;
+      q_tile(n, h, qslot0);
+      const int qpos0 = p.m.pos(qslot0);
+      const int cls = classify(qpos0, kpos0);
+      if (cls == kEmpty) continue;
+      if (!(ok = warp_wait(q_full(stage), par, abort, p.status))) break;  // LSE, Delta landed
+      if (!(ok = warp_wait(s_full, cnt & 1, abort, p.status))) break;
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32(t_s, sr[0]);
+      tmem_ld32(t_s + 32, sr[1]);
+      tmem_wait_ld();
+      const float* lse_t = lse_s + stage * 128 + half * 64;
+      const float* del_t = del_s + stage * 128 + half * 64;
+      // query column j (of this half) sees this key row iff kpos0 + row <= qpos0 + 64*half + j
+      const int thr = kpos0 + row - qpos0 - half * 64;
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int j0 = c * 32 + j;
+          float p0 = ex2(fmaf(__uint_as_float(sr[c][j]), p.scale_log2, -lse_t[j0] * kLog2e));
+          float p1 = ex2(fmaf(__uint_as_float(sr[c][j + 1]), p.scale_log2, -lse_t[j0 + 1] * kLog2e));
+          if (cls == kDiag) {
+            if (j0 < thr) p0 = 0.f;
+            if (j0 + 1 < thr) p1 = 0.f;
+          }
+          pr[j0] = p0;
+          pr[j0 + 1] = p1;
+          pk[j >> 1] = pack_bf16(p0, p1);
+        }
+        tmem_st16(t_s + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      if (!(ok = warp_wait(dp_full, cnt & 1, abort, p.status))) break;
+      tc_fence_after();
+      tmem_ld32(t_dp, sr[0]);
+      tmem_ld32(t_dp + 32, sr[1]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int j0 = c * 32 + j;
+          const float d0 = pr[j0] * (__uint_as_float(sr[c][j]) - del_t[j0]);
+          const float d1 = pr[j0 + 1] * (__uint_as_float(sr[c][j + 1]) - del_t[j0 + 1]);
+          pk[j >> 1] = pack_bf16(d0, d1);
+        }
+        tmem_st16(t_dp + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+      ++cnt;
+      if (++stage == S) stage = 0, par ^= 1;
+    }
+    if (ok && cnt > 0) ok = warp_wait(dk_done, (cnt - 1) & 1, abort, p.status);
+    if (ok) {
+      tc_fence_after();
+      const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
+      __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(p.out0) + orow * D + half * (D / 2);
+      __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.out1) + orow * D + half * (D / 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v32[32];
+        if (cnt > 0) {
+          tmem_ld32(tmem + lane_off + 256 + half * (D / 2) + c * 32, v32);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v32[j] = 0u;
+        }
+        store_row32_bf16(dv + c * 32, v32, 1.f);
+        if (cnt > 0) {
+          tmem_ld32(tmem + lane_off + 256 + D + half * (D / 2) + c * 32, v32);
+          tmem_wait_ld();
+        }
+        store_row32_bf16(dk + c * 32, v32, p.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// dQ
+// ===========================================================================
+template <int D>
+struct DqSmem {
+  static constexpr int kStages = 2;
+  static constexpr int kTB = kTile * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kTB;
+  static constexpr int kK = 2 * kTB;
+  static constexpr int kV = kK + kStages * kTB;
+  static constexpr int kBar = kV + kStages * kTB;
+  // qdo_full, k_full[S], v_full[S], kv_empty[S], s_full, s_free, dp_full, ds_full,
+  // dq_done[2], final
+  static constexpr int kNumBars = 1 + 3 * kStages + 7;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const Params p) {
+  using L = DqSmem<D>;
+  constexpr int S = L::kStages;
+  constexpr int kDqCol = 384;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + L::kBar;
+  const uint32_t qdo_full = bars;
+  auto k_full = [&](int s) { return bars + 8 * (1 + s); };
+  auto v_full = [&](int s) { return bars + 8 * (1 + S + s); };
+  auto kv_empty = [&](int s) { return bars + 8 * (1 + 2 * S + s); };
+  const uint32_t s_full = bars + 8 * (1 + 3 * S);
+  const uint32_t s_free = s_full + 8;
+  const uint32_t dp_full = s_full + 16;
+  const uint32_t ds_full = s_full + 24;
+  auto dq_done = [&](int x) { return s_full + 32 + 8 * x; };
+  const uint32_t final_bar = s_full + 48;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumBars; ++i) {
+      const uint32_t b = bars + 8 * i;
+      mbar_init(b, (b == s_free || b == ds_full) ? 256 : 1);
+    }
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // work item: latest query positions (the most keys) first
+  const int units = p.B * p.Hq;
+  const int ti = blockIdx.x / units;
+  const int rem = blockIdx.x - ti * units;
+  const int b = rem / p.Hq, h = rem - (rem / p.Hq) * p.Hq, g = h / p.n_rep;
+  const int n_q_tiles = p.T / kTile;
+  const int qpos0 = (n_q_tiles - 1 - ti) * kTile;
+  const int qslot0 = p.m.slot(qpos0);
+  const int r_own = qslot0 / p.m.c;
+  const int c_tiles = p.m.c / kTile;
+  const int n_walk = p.m.cp * c_tiles;
+  auto kv_slot = [&](int n) {
+    const int step = n / c_tiles, t = n - step * c_tiles;
+    return ((r_own - step + p.m.cp) % p.m.cp) * p.m.c + t * kTile;
+  };
+  const int64_t qrow = ((int64_t)b * p.Hq + h) * p.T + qslot0;
+  const int kv_row_base = (b * p.Hkv + g) * p.T;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_expect_tx(qdo_full, 2 * L::kTB);
+      for (int kb = 0; kb < D / 64; ++kb) {
+        tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)qrow, qdo_full);
+        tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)qrow, qdo_full);
+      }
+      int stage = 0, par = 0, issued[S], ipar[S];
+      for (int s = 0; s < S; ++s) issued[s] = 0, ipar[s] = 0;
+      for (int n = 0; n < n_walk; ++n) {
+        const int ks = kv_slot(n);
+        if (classify(qpos0, p.m.pos(ks)) == kEmpty) continue;
+        if (!mbar_wait(kv_empty(stage), par ^ 1, abort, p.status, kTimeoutNs)) break;
+        const int row = kv_row_base + ks;
+        mbar_expect_tx(k_full(stage), L::kTB);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_2d(sbase + L::kK + stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64, row,
+                      k_full(stage));
+        mbar_expect_tx(v_full(stage), L::kTB);
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_2d(sbase + L::kV + stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64, row,
+                      v_full(stage));
+        issued[stage] = 1;
+        ipar[stage] = par;
+        if (++stage == S) stage = 0, par ^= 1;
+      }
+      drain_wait(qdo_full, 0);
+      for (int s = 0; s < S; ++s)
+        if (issued[s]) {
+          drain_wait(k_full(s), ipar[s]);
+          drain_wait(v_full(s), ipar[s]);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
+      bool ok = mbar_wait(qdo_full, 0, abort, p.status, kTimeoutNs);
+      tc_fence_after();
+      // visited tiles in order; S/dP of tile j+1 are issued before dQ of tile j
+      int n_next = 0;
+      auto next_visit = [&](int from) {
+        for (int n = from; n < n_walk; ++n)
+          if (classify(qpos0, p.m.pos(kv_slot(n))) != kEmpty) return n;
+        return n_walk;
+      };
+      int stage = 0, par = 0;
+      auto issue_s = [&](int st, int pr) -> bool {
+        if (!mbar_wait(k_full(st), pr, abort, p.status, kTimeoutNs)) return false;
+        tc_fence_after();
+        const uint32_t ka = sbase + L::kK + st * L::kTB;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem, sdesc_sw128(sbase + L::kQ + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                 kIdSS, kk > 0);
+        }
+        mma_commit(s_full);
+        return true;
+      };
+      auto issue_dp = [&](int st, int pr, int buf) -> bool {
+        if (!mbar_wait(v_full(st), pr, abort, p.status, kTimeoutNs)) return false;
+        tc_fence_after();
+        const uint32_t va = sbase + L::kV + st * L::kTB;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem + 128 + 128 * buf, sdesc_sw128(sbase + L::kDO + off, 16, 1024),
+                 sdesc_sw128(va + off, 16, 1024), kIdSS, kk > 0);
+        }
+        mma_commit(dp_full);
+        return true;
+      };
+      int j = 0;
+      n_next = next_visit(0);
+      if (ok && n_next < n_walk) ok = issue_s(stage, par) && issue_dp(stage, par, 0);
+      while (ok && n_next < n_walk) {
+        const int n_after = next_visit(n_next + 1);
+        const int cur_stage = stage, cur_buf = j & 1;
+        int nstage = stage + 1, npar = par;
+        if (nstage == S) nstage = 0, npar ^= 1;
+        // S of the next tile as soon as this tile's S has been read out
+        if (n_after < n_walk) {
+          if (!(ok = mbar_wait(s_free, j & 1, abort, p.status, kTimeoutNs))) break;
+          if (!(ok = issue_s(nstage, npar))) break;
+        }
+        // dQ += dS K
+        if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status, kTimeoutNs))) break;
+        tc_fence_after();
+        const uint32_t ka = sbase + L::kK + cur_stage * L::kTB;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acol = 128 + 128 * cur_buf + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tmem + kDqCol, tmem + acol, sdesc_sw128(ka + kk * 2048, kTile * 128, 1024), kIdTS,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(dq_done(cur_buf));
+        mma_commit(kv_empty(cur_stage));
+        // dP of the next tile into the other buffer, once dQ of tile j-1 has read it
+        if (n_after < n_walk) {
+          if (j >= 1 &&
+              !(ok = mbar_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status,
+                               kTimeoutNs)))
+            break;
+          tc_fence_after();
+          if (!(ok = issue_dp(nstage, npar, (j + 1) & 1))) break;
+        }
+        stage = nstage;
+        par = npar;
+        n_next = n_after;
+        ++j;
+      }
+      mma_commit(final_bar);
+      drain_wait(final_bar, 0);
+    }
+  } else if (warp >= 4) {
+    const int quad = warp & 3, half = (warp - 4) >> 2;
+    const int row = quad * 32 + lane;  // query row of the tile
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + half * 64;
+    const float lse2 = p.lse[qrow + row] * kLog2e;
+    const float dl = p.delta[qrow + row];
+    int j = 0;
+    bool ok = true;
+    for (int n = 0; n < n_walk; ++n) {
+      const int ks = kv_slot(n);
+      const int kpos0 = p.m.pos(ks);
+      const int cls = classify(qpos0, kpos0);
+      if (cls == kEmpty) continue;
+      if (!(ok = warp_wait(s_full, j & 1, abort, p.status))) break;
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32(t_s, sr[0]);
+      tmem_ld32(t_s + 32, sr[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free);
+      // key column j (of this half) is visible iff kpos0 + 64*half + j <= qpos0 + row
+      const int thr = qpos0 + row - kpos0 - half * 64;
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j0 = c * 32 + jj;
+          float pv = ex2(fmaf(__uint_as_float(sr[c][jj]), p.scale_log2, -lse2));
+          if (cls == kDiag && j0 > thr) pv = 0.f;
+          pr[j0] = pv;
+        }
+      if (!(ok = warp_wait(dp_full, j & 1, abort, p.status))) break;
+      tc_fence_after();
+      const uint32_t t_dp = tmem + lane_off + 128 + 128 * (j & 1) + half * 64;
+      tmem_ld32(t_dp, sr[0]);
+      tmem_ld32(t_dp + 32, sr[1]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 2) {
+          const int j0 = c * 32 + jj;
+          pk[jj >> 1] = pack_bf16(pr[j0] * (__uint_as_float(sr[c][jj]) - dl),
+                                  pr[j0 + 1] * (__uint_as_float(sr[c][jj + 1]) - dl));
+        }
+        tmem_st16(t_dp + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+      ++j;
+    }
+    if (ok && j > 0) ok = warp_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(p.out0) + (qrow + row) * D + half * (D / 2);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v32[32];
+        if (j > 0) {
+          tmem_ld32(tmem + lane_off + kDqCol + half * (D / 2) + c * 32, v32);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) v32[jj] = 0u;
+        }
+        store_row32_bf16(dq + c * 32, v32, p.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename K>
+static cudaError_t prep(K kern, int smem) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <int D>
+static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, const void* k,
+                           const void* v, const void* dO, void* dq, void* dk, void* dv,
+                           cudaStream_t st) {
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t qrows = (uint64_t)R.B * R.Hq * R.T, krows = (uint64_t)R.B * R.Hkv * R.T;
+  if (encode_tmap_2d_bf16(&tq, q, D, qrows, 64, kTile) != CUDA_SUCCESS ||
+      encode_tmap_2d_bf16(&tdo, dO, D, qrows, 64, kTile) != CUDA_SUCCESS ||
+      encode_tmap_2d_bf16(&tk, k, D, krows, 64, kTile) != CUDA_SUCCESS ||
+      encode_tmap_2d_bf16(&tv, v, D, krows, 64, kTile) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  Params pk = base;
+  pk.out0 = dk;
+  pk.out1 = dv;
+  cudaError_t e = prep(dkdv_kernel<D>, DkdvSmem<D>::kBytes);
+  if (e != cudaSuccess) return e;
+  const int kv_items = R.B * R.Hkv * (R.T / kTile);
+  timing_begin("tc_bwd_dkdv", st);
+  dkdv_kernel<D><<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pk);
+  e = cudaGetLastError();
+  timing_end(st);
+  if (e != cudaSuccess) return e;
+  Params pq = base;
+  pq.out0 = dq;
+  pq.out1 = nullptr;
+  e = prep(dq_kernel<D>, DqSmem<D>::kBytes);
+  if (e != cudaSuccess) return e;
+  const int q_items = R.B * R.Hq * (R.T / kTile);
+  timing_begin("tc_bwd_dq", st);
+  dq_kernel<D><<<q_items, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
+  e = cudaGetLastError();
+  timing_end(st);
+  return e;
+}
+
+}  // namespace tcbwd
+
+cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
+                          const float* lse, const float* delta, const void* dO, void* dq,
+                          void* dk, void* dv, int* status, cudaStream_t st) {
+  tcbwd::Params p;
+  p.B = R.B;
+  p.Hq = R.Hq;
+  p.Hkv = R.Hkv;
+  p.T = R.T;
+  p.n_rep = R.Hq / R.Hkv;
+  p.m = SeqMap::make(R.T, R.cp, R.zz);
+  p.scale = R.scale;
+  p.scale_log2 = R.scale * tcbwd::kLog2e;
+  p.lse = lse;
+  p.delta = delta;
+  p.status = status;
+  if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st);
+  return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st);
+}
+
+}  // namespace cpattn

@@ -1,0 +1,200 @@
+/*
+ * cpattn — causal blockwise ring attention for one GB300 (sm_103a), C ABI.
+ *
+ * The operation (tutorial "上下文并行", section "朴素 Ring Attention"; pull request
+ * "Feat: Context Parallel" #181, mode table row "p2p"): the sequence of T tokens
+ * is split over cp context-parallel ranks; each rank's query chunk attends to one
+ * key/value chunk per ring step (rank r holds the K/V of rank (r - i) mod cp at
+ * step i) with the causal mask taken from GLOBAL token positions, and the
+ * per-step partial results are merged by the single-pass online softmax
+ * (running max and sum, carried as (O, LSE)).  The backward pass recomputes the
+ * probabilities and returns dQ and, for every K/V chunk, the dK/dV its owner
+ * receives.  On one GPU the ranks are chunk indices inside one kernel launch;
+ * nothing is exchanged between GPUs.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors are row-major and contiguous, D fastest:
+ *   q, o, dq, dO : [B, H_q, T, D]        k, v, dk, dv : [B, H_kv, T, D]
+ *   lse          : [B, H_q, T] float32, natural logarithm
+ * The token axis T is in LAYOUT ORDER: rank r holds slots [r*c, (r+1)*c),
+ * c = T / cp.  With CPATTN_CONTIGUOUS, slot t is natural position t.  With
+ * CPATTN_ZIGZAG (tutorial, section "Zig-Zag Ring Attention") the sequence is cut
+ * into 2*cp chunks of c/2 tokens and rank r holds chunk r followed by chunk
+ * 2cp-1-r.  cpattn_layout converts between natural and layout order.
+ * Query head h uses key/value head h / (H_q / H_kv): the H_q heads form H_kv
+ * groups of n_rep = H_q / H_kv consecutive heads (the grouped-query view of the
+ * pull request's review thread on RepeatKVHeads, resolved here as an index map;
+ * no repeated K/V copy is made).  dK, dV sum over the heads of a group.
+ * With a2a > 1 (the hierarchical "a2a+p2p" mode) q/k/v/o/lse and the gradients
+ * are the head-sharded tensors that cpattn_layout(CPATTN_A2A_FWD) produces,
+ * [a2a][B][H/a2a][T][D], and the ring runs over p2p = cp / a2a ranks inside each
+ * of the a2a slices.
+ *
+ * dtype CPATTN_BF16: q/k/v/o/dO/dq/dk/dv are bfloat16, all accumulation is
+ * float32, probabilities are rounded to bf16 only as an MMA operand and O is
+ * rounded only after the division by the softmax sum.  dtype CPATTN_F32: every
+ * tensor is float32 and every step runs in float32.
+ *
+ * Ownership: the caller allocates and owns every buffer; the library allocates
+ * no device memory in any call.  Every call is asynchronous on `stream` (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream) and returns
+ * after enqueueing.  Pointers are device pointers unless stated otherwise and
+ * must be 16-byte aligned.
+ *
+ * Errors: invalid arguments are reported synchronously, before anything is
+ * enqueued (CPATTN_ERR_INVALID_ARG; CPATTN_ERR_UNSUPPORTED for shapes outside the
+ * implemented set).  Launch failures return CPATTN_ERR_CUDA.  Errors detected on
+ * the device (a bounded wait that ran out) are latched in a per-device status
+ * word and reported by cpattn_check.
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cpattn_status {
+  CPATTN_OK = 0,
+  CPATTN_ERR_INVALID_ARG = 1,
+  CPATTN_ERR_UNSUPPORTED = 2,
+  CPATTN_ERR_CUDA = 3,
+  CPATTN_ERR_TIMEOUT = 4
+} cpattn_status;
+
+typedef enum cpattn_dtype { CPATTN_F32 = 0, CPATTN_BF16 = 1 } cpattn_dtype;
+
+typedef enum cpattn_seq_layout { CPATTN_CONTIGUOUS = 0, CPATTN_ZIGZAG = 1 } cpattn_seq_layout;
+
+typedef enum cpattn_permute {
+  CPATTN_ZIGZAG_FWD = 0, /* natural order -> layout order (desc.layout over the ring's ranks) */
+  CPATTN_ZIGZAG_INV = 1, /* layout order -> natural order */
+  CPATTN_A2A_FWD = 2,    /* token-sharded [cp][B][T/cp][H][D] -> head-sharded [a2a][B][H/a2a][T][D] */
+  CPATTN_A2A_INV = 3     /* head-sharded -> token-sharded */
+} cpattn_permute;
+
+/* Problem descriptor.  Integers are int32; layout and dtype hold the enum values. */
+typedef struct cpattn_desc {
+  int32_t B;           /* batch */
+  int32_t H_q;         /* query heads (a multiple of H_kv) */
+  int32_t H_kv;        /* key/value heads */
+  int32_t T;           /* tokens per sequence */
+  int32_t D;           /* head dimension (<= 128; the bf16 tensor-core path takes 64 or 128) */
+  int32_t cp;          /* context-parallel ranks emulated in the launch */
+  int32_t a2a;         /* all-to-all group size of the hierarchical mode; 1 = plain ring */
+  int32_t layout;      /* cpattn_seq_layout */
+  int32_t dtype;       /* cpattn_dtype */
+  float scale;         /* softmax scale, > 0 (1/sqrt(D) for standard attention) */
+  int32_t causal;      /* must be 1: the pages define causal self-attention only */
+  int32_t debug_fault; /* 0.  Test hook: 1 makes the tensor-core forward withhold one
+                          load so that its bounded wait runs out (CPATTN_ERR_TIMEOUT
+                          via cpattn_check, within about 50 ms). */
+} cpattn_desc;
+
+/*
+ * One ring step's partial result: the queries of rank q_rank against the K/V
+ * chunk of rank kv_rank, causal mask from global positions (tutorial, section
+ * "朴素 Ring Attention": partial = Softmax(Q_i K^T / sqrt(d)) V for the block
+ * held at that step).
+ *   q, k, v   : full layout-order tensors (see above), dtype desc->dtype
+ *   o_part    : [B', H_q', c, D] float32, normalised within the chunk
+ *   lse_part  : [B', H_q', c] float32; a row that sees no key of the chunk gets
+ *               o = 0 and lse = -inf (the identity of cpattn_merge)
+ * (B' = a2a*B, H_q' = H_q/a2a, c = T/(cp/a2a); ranks index the p2p ring.)
+ * Errors: rank outside [0, cp/a2a) -> CPATTN_ERR_INVALID_ARG.
+ */
+cpattn_status cpattn_partial_fwd(const cpattn_desc* desc, int q_rank, int kv_rank,
+                                 const void* q, const void* k, const void* v,
+                                 float* o_part, float* lse_part, void* stream);
+
+/*
+ * Online-softmax merge of two partial results over disjoint key sets (tutorial,
+ * section "朴素 Ring Attention": the block order does not matter as long as the
+ * current O, max and sum are carried; section "Zig-Zag Ring Attention": the
+ * softmax_lse update).  For each of `rows` rows of D floats:
+ *   lse = ln(e^lse_a + e^lse_b),  o = e^(lse_a-lse) o_a + e^(lse_b-lse) o_b,
+ * evaluated max-shifted; an empty operand (lse = -inf) is the identity and two
+ * empty operands give (0, -inf), never NaN.  All buffers are float32;
+ * o_out/lse_out may alias o_a/lse_a (or o_b/lse_b) exactly.
+ */
+cpattn_status cpattn_merge(int64_t rows, int D, const float* o_a, const float* lse_a,
+                           const float* o_b, const float* lse_b, float* o_out,
+                           float* lse_out, void* stream);
+
+/*
+ * All cp ring steps of the forward pass, merged in ring order inside one launch:
+ * o = causal attention output (dtype desc->dtype), lse = its log-sum-exp.
+ * (Pull request #181, mode "p2p": the K/V travel the ring and the chunk results
+ * are merged with a single-pass online softmax.)
+ */
+cpattn_status cpattn_ring_fwd(const cpattn_desc* desc, const void* q, const void* k,
+                              const void* v, void* o, float* lse, void* stream);
+
+/* Bytes of device workspace cpattn_ring_bwd needs (float32 row statistics). */
+size_t cpattn_ring_bwd_workspace(const cpattn_desc* desc);
+
+/*
+ * Backward pass of cpattn_ring_fwd (pull request #181, mode "p2p": recompute the
+ * probabilities; the K/V gradients go back to their owner).  Inputs are the
+ * forward's q, k, v, o, lse and the upstream gradient dO (same dtype as q);
+ * outputs dq [B,H_q,T,D], dk and dv [B,H_kv,T,D] in layout order, so each rank's
+ * slice of dk/dv is what its owner receives.  `workspace` is device scratch of at
+ * least cpattn_ring_bwd_workspace(desc) bytes (ws_bytes smaller ->
+ * CPATTN_ERR_INVALID_ARG); its contents on entry do not matter.
+ */
+cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void* k,
+                              const void* v, const void* o, const float* lse,
+                              const void* dO, void* dq, void* dk, void* dv,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Permutes one tensor of n_heads heads (H_q or H_kv) between orders:
+ *  CPATTN_ZIGZAG_FWD / _INV : [B][n_heads][T][D] natural <-> layout order of
+ *      desc->layout over the ring's cp/a2a ranks (tutorial, section "Zig-Zag Ring
+ *      Attention": rank r holds chunks r and 2cp-1-r).
+ *  CPATTN_A2A_FWD / _INV : the all-to-all of the hierarchical mode (pull request
+ *      #181, mode "a2a+p2p"; tutorial, section "Ulysses CP").  Token-sharded
+ *      [cp][B][T/cp][n_heads][D] (rank r's tokens in desc->layout order over cp)
+ *      <-> head-sharded [a2a][B][n_heads/a2a][T][D]: the cp ranks form a2a groups
+ *      of consecutive ranks; slice j holds heads [j*n_heads/a2a, ...) of every
+ *      token, and its token axis is the layout order of the p2p = cp/a2a ring
+ *      whose rank k is a2a group k.
+ * Element size from desc->dtype.  A pure copy: bit-exact.  src and dst must not
+ * overlap.
+ */
+cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* src, void* dst,
+                            int n_heads, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns CPATTN_ERR_TIMEOUT if a kernel's bounded wait ran out
+ * since the last check, CPATTN_ERR_CUDA on a CUDA error, else CPATTN_OK.
+ */
+cpattn_status cpattn_check(void* stream);
+
+/* Static English text for a status code. */
+const char* cpattn_status_string(cpattn_status status);
+
+/*
+ * Kernel timing (instrumentation for measurement).  While enabled, every kernel
+ * the library enqueues is bracketed by CUDA events recorded on its stream.
+ * cpattn_timing_collect synchronises those events and adds their durations to
+ * per-kernel totals; cpattn_timing_get reads total milliseconds and launch count
+ * of entry `index` (0 <= index < cpattn_timing_count()).  Host-side only.
+ */
+cpattn_status cpattn_timing_enable(int on);
+cpattn_status cpattn_timing_collect(void);
+int cpattn_timing_count(void);
+cpattn_status cpattn_timing_get(int index, const char** name, double* total_ms,
+                                int64_t* launches);
+cpattn_status cpattn_timing_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */

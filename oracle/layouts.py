@@ -132,17 +132,18 @@ def a2a_groups(cp: int, a2a: int):
     return groups, rings
 
 
-def a2a_source_rows(B: int, H: int, T: int, cp: int, a2a: int) -> np.ndarray:
+def a2a_source_rows(B: int, H: int, T: int, cp: int, a2a: int,
+                    layout: str = "zigzag") -> np.ndarray:
     """Flat source row of every destination row of the a2a re-layout.
 
     Source (token-sharded, what each of the cp ranks holds before the
     all-to-all): [cp][B][T/cp][H] rows of D values, rank r's T/cp tokens being its
-    zigzag share over cp (chunks r and 2cp-1-r of length T/(2cp)).
+    share over cp in ``layout`` (zigzag: chunks r and 2cp-1-r of length T/(2cp)).
     Destination (head-sharded, after the all-to-all): [a2a][B][H/a2a][T] rows,
     where slice j holds heads [j*H/a2a, (j+1)*H/a2a) and its token axis is the
-    layout order of a zigzag ring over p2p = cp/a2a ranks: p2p rank k (a2a group
-    k) owns slots [k*T/p2p, (k+1)*T/p2p), i.e. the p2p zigzag chunks k and
-    2*p2p-1-k of length T/(2*p2p).
+    layout order of a ring over p2p = cp/a2a ranks in the same ``layout``: p2p
+    rank k (a2a group k) owns slots [k*T/p2p, (k+1)*T/p2p) (zigzag: the p2p
+    chunks k and 2*p2p-1-k of length T/(2*p2p)).
     Returns an int64 array of shape [a2a, B, H/a2a, T].
     """
     if H % a2a:
@@ -154,10 +155,10 @@ def a2a_source_rows(B: int, H: int, T: int, cp: int, a2a: int) -> np.ndarray:
     src_rank = np.empty(T, dtype=np.int64)
     src_slot = np.empty(T, dtype=np.int64)
     for r in range(cp):
-        pos_r = rank_positions(T, cp, "zigzag", r)
+        pos_r = rank_positions(T, cp, layout, r)
         src_rank[pos_r] = r
         src_slot[pos_r] = np.arange(c_src)
-    dst_pos = positions(T, p2p, "zigzag")      # natural position of each dst slot
+    dst_pos = positions(T, p2p, layout)        # natural position of each dst slot
     out = np.empty((a2a, B, Hs, T), dtype=np.int64)
     for j in range(a2a):
         for b in range(B):
@@ -169,29 +170,29 @@ def a2a_source_rows(B: int, H: int, T: int, cp: int, a2a: int) -> np.ndarray:
     return out
 
 
-def a2a_forward(src, B, H, T, cp, a2a):
+def a2a_forward(src, B, H, T, cp, a2a, layout="zigzag"):
     """Apply the re-layout to a source array of shape [cp, B, T/cp, H, D]."""
     D = src.shape[-1]
     flat = src.reshape(-1, D)
-    idx = a2a_source_rows(B, H, T, cp, a2a)
+    idx = a2a_source_rows(B, H, T, cp, a2a, layout)
     return flat[idx.reshape(-1)].reshape(a2a, B, H // a2a, T, D)
 
 
-def a2a_inverse(dst, B, H, T, cp, a2a):
+def a2a_inverse(dst, B, H, T, cp, a2a, layout="zigzag"):
     """Undo the re-layout: [a2a, B, H/a2a, T, D] -> [cp, B, T/cp, H, D]."""
     D = dst.shape[-1]
-    idx = a2a_source_rows(B, H, T, cp, a2a).reshape(-1)
+    idx = a2a_source_rows(B, H, T, cp, a2a, layout).reshape(-1)
     out = np.empty((cp * B * (T // cp) * H, D), dtype=dst.dtype)
     out[idx] = dst.reshape(-1, D)
     return out.reshape(cp, B, T // cp, H, D)
 
 
-def token_shards(x_natural_bhtd, cp):
-    """Natural [B, H, T, D] -> the cp ranks' zigzag token shards [cp, B, T/cp, H, D]."""
+def token_shards(x_natural_bhtd, cp, layout="zigzag"):
+    """Natural [B, H, T, D] -> the cp ranks' token shards [cp, B, T/cp, H, D]."""
     B, H, T, D = x_natural_bhtd.shape
     c = T // cp
     out = np.empty((cp, B, c, H, D), dtype=x_natural_bhtd.dtype)
     for r in range(cp):
-        pos_r = rank_positions(T, cp, "zigzag", r)
+        pos_r = rank_positions(T, cp, layout, r)
         out[r] = np.transpose(x_natural_bhtd[:, :, pos_r, :], (0, 2, 1, 3))
     return out

@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/cpattn.h declares, and rejects invalid arguments
+synchronously, before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def cp():
+    from blockwise_online_softmax_cpattn_gb300 import build_lib
+    build_lib.build()
+    import blockwise_online_softmax_cpattn_gb300 as mod
+    return mod
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "cpattn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpattn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(cp):
+    names = _declared_functions()
+    assert len(names) >= 13
+    lib = ctypes.CDLL(cp.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _desc(mod, **kw):
+    base = dict(B=1, H_q=4, H_kv=2, T=512, D=64, cp=2, layout="zigzag", dtype="bf16")
+    base.update(kw)
+    return mod.make_desc(**base)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H_q=3, H_kv=2), 1),
+    (dict(T=502), 1),                        # zigzag needs T % (2 cp) == 0
+    (dict(T=511, layout="contiguous"), 1),   # T % cp != 0
+    (dict(D=192), 2),
+    (dict(causal=0), 2),
+    (dict(scale=0.0), 1),
+    (dict(scale=-1.0), 1),
+    (dict(cp=0), 1),
+    (dict(a2a=3, cp=2), 1),                  # a2a must divide cp
+    (dict(a2a=2, cp=4, H_kv=1, H_q=4), 1),   # heads must split over a2a
+    (dict(layout=7), 1),
+    (dict(dtype=5), 1),
+    (dict(B=0), 1),
+])
+def test_invalid_descriptors_are_rejected(cp, kw, code):
+    d = _desc(cp, **kw)
+    assert cp.cpattn_ring_fwd(d, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == code
+    assert cp.cpattn_ring_bwd(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              1 << 30, 0) == code
+    assert cp.cpattn_partial_fwd(d, 0, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == code
+    assert cp.cpattn_ring_bwd_workspace(d) == 0
+
+
+def test_null_and_misaligned_pointers(cp):
+    d = _desc(cp)
+    assert cp.cpattn_ring_fwd(d, 0, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert cp.cpattn_ring_fwd(d, FAKE + 8, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert cp.cpattn_merge(10, 64, FAKE, FAKE, FAKE + 4, FAKE, FAKE, FAKE, 0) == 1
+    assert cp.cpattn_merge(-1, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert cp.cpattn_merge(0, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 0  # nothing to do
+    assert cp.cpattn_layout(0, d, FAKE, FAKE, 4, 0) == 1                    # src == dst
+    assert cp.cpattn_layout(9, d, FAKE, FAKE + 64, 4, 0) == 1
+    assert cp.cpattn_layout(2, _desc(cp, a2a=2, cp=4, T=512), FAKE, FAKE + 64, 3, 0) == 1
+
+
+def test_ranks_and_workspace_are_checked(cp):
+    d = _desc(cp)
+    assert cp.cpattn_partial_fwd(d, 2, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert cp.cpattn_partial_fwd(d, 0, -1, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    need = cp.cpattn_ring_bwd_workspace(d)
+    assert need >= 1 * 4 * 512 * 4 and need % 256 == 0
+    assert cp.cpattn_ring_bwd(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              need - 1, 0) == 1
+
+
+def test_status_strings(cp):
+    for code in range(5):
+        assert cp.cpattn_status_string(code)
+    assert cp.cpattn_status_string(99) == "unknown status"
+
+
+def test_timing_table_host_side(cp):
+    assert cp.cpattn_timing_reset() == 0
+    assert cp.cpattn_timing_enable(False) == 0
+    assert cp.cpattn_timing_collect() == 0
+    assert cp.cpattn_timing_table() == {}

@@ -101,27 +101,28 @@ def test_chunk_pair_flops_match_the_page():
 
 # ------------------------------------------------------------------ a2a ----
 
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 @pytest.mark.parametrize("B,H,T,cp,a2a", [(1, 8, 64, 8, 2), (2, 4, 32, 4, 2), (1, 6, 48, 6, 3),
                                           (1, 4, 16, 2, 2), (1, 4, 32, 4, 1)])
-def test_a2a_round_trip_and_structure(rng, B, H, T, cp, a2a):
+def test_a2a_round_trip_and_structure(rng, B, H, T, cp, a2a, layout):
     D = 3
     nat = rng.standard_normal((B, H, T, D))
-    src = L.token_shards(nat, cp)
-    dst = L.a2a_forward(src, B, H, T, cp, a2a)
-    assert np.array_equal(L.a2a_inverse(dst, B, H, T, cp, a2a), src)
+    src = L.token_shards(nat, cp, layout)
+    dst = L.a2a_forward(src, B, H, T, cp, a2a, layout)
+    assert np.array_equal(L.a2a_inverse(dst, B, H, T, cp, a2a, layout), src)
     p2p = cp // a2a
     Hs = H // a2a
     # slice j holds heads [j*Hs, (j+1)*Hs) of every token, token axis in the
     # layout order of a zigzag ring over p2p ranks
     for j in range(a2a):
-        want = L.to_layout(nat[:, j * Hs:(j + 1) * Hs], p2p, "zigzag")
+        want = L.to_layout(nat[:, j * Hs:(j + 1) * Hs], p2p, layout)
         assert np.array_equal(dst[j], want)
     # p2p rank k's slots hold exactly the tokens of a2a group k's cp ranks
     groups, rings = L.a2a_groups(cp, a2a)
     c_p = T // p2p
-    dst_pos = L.positions(T, p2p, "zigzag")
+    dst_pos = L.positions(T, p2p, layout)
     for k, grp in enumerate(groups):
-        held = np.concatenate([L.rank_positions(T, cp, "zigzag", r) for r in grp])
+        held = np.concatenate([L.rank_positions(T, cp, layout, r) for r in grp])
         assert np.array_equal(np.sort(dst_pos[k * c_p:(k + 1) * c_p]), np.sort(held))
     assert all(len(r_) == p2p for r_ in rings)
 
