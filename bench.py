@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark of causal ring attention (forward + backward) on GB300.
+
+One step = the whole hot path over one batch of synthetic input already in HBM:
+  layout permute of q, k, v, dO (natural -> zigzag layout order; the all-to-all
+  re-layout for the hierarchical a2a x p2p workload) -> cpattn_ring_fwd ->
+  cpattn_ring_bwd -> inverse permute of o, dq, dk, dv.
+FLOPs counted: 4*D per attended (q, k) pair forward, 10*D backward (attended
+pairs = B * H_q * T (T + 1) / 2; masked work inside diagonal tiles is not
+counted).  `value` is TFLOP/s over all GPUs; L2 is flushed (256 MiB write)
+before every timed step.
+
+--impl reference times the FP64 CPU oracle (the only reference there is) on the
+host cores, each step a bounded sample of the same workload.
+
+Launch: python bench.py [--gpus N --steps K --warmup W] [--impl cpattn|reference]
+        [--workload NAME]; for N > 1 under torch.distributed.run, one independent
+replica of the workload per GPU (no data exchange; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "causal ring-attention fwd+bwd TFLOP/s and % of BF16 tensor peak (1 GB300)"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = W.LLAMA.name
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cpattn", choices=["cpattn", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_of(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "T": w.T, "D": w.D,
+           "cp": w.cp, "a2a": w.a2a, "layout": w.layout, "causal": True, "seed": w.seed,
+           "inputs": f"i.i.d. N(0,1), seeded torch CPU generator, cast to {w.dtype}",
+           "flops_per_step": w.fwd_flops + w.bwd_flops}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.path = os.path.join("/tmp", f"cpattn_clocks_{os.getpid()}.csv")
+        self.proc = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(1.0)  # first samples come after nvidia-smi starts up
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        mhz, mx, reasons, n_all = [], None, set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                n_all += 1
+                if not (t0 - 0.06 <= ts <= t1 + 0.06):
+                    continue
+                try:
+                    mhz.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[4:8]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+def kernel_flops_or_bytes(name, w):
+    """Algorithmic work of one launch of a library kernel on this workload."""
+    pairs = w.attended_pairs
+    elt = 2 if w.dtype == "bf16" else 4
+    rows_q = w.B * w.H_q * w.T
+    rows_kv = w.B * w.H_kv * w.T
+    if name in ("tc_ring_fwd", "simt_ring_fwd"):
+        return "tensor", 4.0 * w.D * pairs
+    if name in ("tc_bwd_dkdv", "simt_bwd_dkdv"):     # S, dP recomputed + dV, dK products
+        return "tensor", 8.0 * w.D * pairs
+    if name in ("tc_bwd_dq", "simt_bwd_dq"):         # the dQ product only
+        return "tensor", 2.0 * w.D * pairs
+    if name == "bwd_delta":
+        return "hbm", 2.0 * rows_q * w.D * elt + 4.0 * rows_q
+    if name.startswith("layout"):                    # per launch: one tensor read + written
+        return "hbm", None
+    return "hbm", None
+
+
+def traffic_for(kernel, workload):
+    """dram bytes per launch from the committed ncu summary, if the kernel's
+    sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "blockwise_online_softmax_cpattn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload:
+                return float(parts[2]) if parts[3] == digest else None
+    return None
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank value over all ranks (the slowest replica sets the time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_cpattn(args, rank, world):
+    import torch
+    import blockwise_online_softmax_cpattn_gb300 as cp
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.ALL[args.workload]
+    stream = torch.cuda.current_stream()
+    desc = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, w.D, w.cp, w.layout, w.dtype, a2a=w.a2a)
+    dt = W.torch_dtype(w)
+    nat_host = [x.pin_memory() for x in W.draw_cast(w)]             # natural order
+    q, k, v, do = [x.to(dev) for x in nat_host]
+    H = [w.H_q, w.H_kv, w.H_kv, w.H_q]
+    if w.a2a > 1:
+        # inputs as the cp ranks' token shards [cp][B][T/cp][H][D]: prepared once,
+        # outside the timed region (zigzag over cp, then rank-major transpose)
+        d_cp = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, w.D, w.cp, w.layout, w.dtype)
+        shards = []
+        for x, h in zip((q, k, v, do), H):
+            y = torch.empty_like(x)
+            cp.check(cp.cpattn_layout(cp.ZIGZAG_FWD, d_cp, x, y, h))
+            shards.append(y.view(w.B, h, w.cp, w.T // w.cp, w.D).permute(2, 0, 3, 1, 4)
+                          .contiguous())
+        src = shards
+        fwd_perm, inv_perm = cp.A2A_FWD, cp.A2A_INV
+    else:
+        src = [q, k, v, do]
+        fwd_perm, inv_perm = cp.ZIGZAG_FWD, cp.ZIGZAG_INV
+    lay = [torch.empty(w.B, h, w.T, w.D, dtype=dt, device=dev) for h in H]
+    o = torch.empty_like(lay[0])
+    lse = torch.empty(w.B, w.H_q, w.T, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(lay[0]), torch.empty_like(lay[1]), torch.empty_like(lay[2])
+    outs = [torch.empty_like(s) for s in (src[0], src[1], src[2], src[0])]  # o, dk, dv, dq
+    ws = torch.empty(cp.cpattn_ring_bwd_workspace(desc), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        for s_, l_, h in zip(src, lay, H):
+            cp.check(cp.cpattn_layout(fwd_perm, desc, s_, l_, h))
+        cp.check(cp.cpattn_ring_fwd(desc, lay[0], lay[1], lay[2], o, lse))
+        cp.check(cp.cpattn_ring_bwd(desc, lay[0], lay[1], lay[2], o, lse, lay[3], dq, dk, dv, ws))
+        for x, y, h in zip((o, dk, dv, dq), outs, (w.H_q, w.H_kv, w.H_kv, w.H_q)):
+            cp.check(cp.cpattn_layout(inv_perm, desc, x, y, h))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cp.check(cp.cpattn_check())
+
+    # ---- device-resident timed region
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    cp.check(cp.cpattn_check())
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, dev)
+    flops = w.fwd_flops + w.bwd_flops
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # ---- per-kernel durations (events on the launch stream, same steps)
+    cp.cpattn_timing_reset()
+    cp.cpattn_timing_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    cp.check(cp.cpattn_timing_collect())
+    cp.cpattn_timing_enable(False)
+    table = cp.cpattn_timing_table()
+    cp.cpattn_timing_reset()
+    launches_per_step = sum(n for _, n in table.values()) / args.steps
+    kernels = {name: {"avg_ms": tot / n, "launches": n, "share": tot / sum(t for t, _ in table.values())}
+               for name, (tot, n) in table.items()}
+    dom = max(table, key=lambda n: table[n][0])
+    pk, src_pk = peaks()
+    bound, work = kernel_flops_or_bytes(dom, w)
+    avg_ms = table[dom][0] / table[dom][1]
+    if bound == "tensor":
+        achieved = work / (avg_ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{src_pk} bf16 dense burst (cuBLAS)",
+                "work_per_launch": work, "avg_launch_ms": avg_ms}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": None}
+    traffic = traffic_for(dom, w.name)
+    roof["traffic"] = traffic
+
+    # ---- end to end through the C ABI with host buffers
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in nat_host)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    src_dev = src if w.a2a == 1 else None
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_e2e)]
+    torch.cuda.synchronize()
+    for a, b in ev2:
+        flush.zero_()
+        a.record(stream)
+        if src_dev is not None:
+            for dst_, hsrc in zip(src_dev, nat_host):
+                dst_.copy_(hsrc, non_blocking=True)
+        else:
+            for dst_, hsrc in zip((q, k, v, do), nat_host):
+                dst_.copy_(hsrc, non_blocking=True)
+            # token shards are rebuilt from the natural-order upload
+            for x, y, h in zip((q, k, v, do), src, H):
+                tmp = torch.empty_like(x)
+                cp.check(cp.cpattn_layout(cp.ZIGZAG_FWD, d_cp, x, tmp, h))
+                y.copy_(tmp.view(w.B, h, w.cp, w.T // w.cp, w.D).permute(2, 0, 3, 1, 4))
+        step()
+        for hdst, dsrc in zip(host_out, outs):
+            hdst.copy_(dsrc, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(cp.cpattn_check())
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev2), world, dev)
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+           "config": config_of(w, {
+               "parallelism": "replicas" if world > 1 else "single GPU, cp ranks emulated in-kernel",
+               "l2": "flushed before every timed step (256 MiB device write, outside the events)",
+               "step": ("a2a permute" if w.a2a > 1 else "zigzag permute")
+               + " q,k,v,dO -> ring fwd -> ring bwd -> inverse permute o,dq,dk,dv",
+               "pct_of_bf16_peak": value / world / pk["bf16_tflops"],
+               "peak_source": src_pk}),
+           "roofline": roof, "gpu_launches": int(round(launches_per_step * args.steps)),
+           "clocks": clocks, "e2e": e2e, "kernels": kernels}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the oracle (CPU) legs
+# ---------------------------------------------------------------------------
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [x.get("num_threads") for x in threadpool_info() if x.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def oracle_head(w, nat, h, T_sample=None):
+    """Time the oracle's forward + backward of query head h (and its K/V head),
+    on the first T_sample tokens (a causal prefix is a self-contained problem)."""
+    from oracle import attention as OA
+    Ts = w.T if T_sample is None else T_sample
+    g = h // (w.H_q // w.H_kv)
+    q, k, v, do = (W.as_f64(x[:1, hh:hh + 1, :Ts]) for x, hh in
+                   ((nat[0], h), (nat[1], g), (nat[2], g), (nat[3], h)))
+    t0 = time.perf_counter()
+    OA.attention_fwd(q, k, v, w.scale)
+    OA.attention_bwd(q, k, v, do, w.scale)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * w.D * Ts * (Ts + 1) / 2
+    return flops, dt
+
+
+def cpu_baseline(w):
+    nat = W.draw_cast(w)
+    flops, dt, n = 0.0, 0.0, 0
+    for h in range(w.H_q):
+        f, t = oracle_head(w, nat, h)
+        flops += f
+        dt += t
+        n += 1
+        if dt > 10.0:
+            break
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{n} of {w.H_q} query heads (with their K/V heads), full T={w.T}, "
+                      f"fwd+bwd in float64 numpy, {dt:.1f} s",
+            "seconds": dt}
+
+
+def run_reference(args):
+    w = W.ALL[args.workload]
+    nat = W.draw_cast(w)
+    Ts = min(w.T, 1024)
+    for i in range(args.warmup):
+        oracle_head(w, nat, i % w.H_q, Ts)
+    flops, dt = 0.0, 0.0
+    for i in range(args.steps):
+        f, t = oracle_head(w, nat, i % w.H_q, Ts)
+        flops += f
+        dt += t
+    value = flops / dt / 1e12
+    ms = dt / args.steps * 1e3
+    sample = (f"per step: the first {Ts} tokens of one query head (cycling over the {w.H_q} heads) "
+              f"with its K/V head, fwd+bwd in float64 numpy")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, {"sample": sample}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    out = run_cpattn(args, rank, world)
+    if rank == 0:
+        w = W.ALL[args.workload]
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(w)
+        else:
+            out["cpu_baseline"] = None
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -12,8 +12,8 @@ from conftest import ROOT
 
 @pytest.fixture(scope="module")
 def cp():
-    from blockwise_online_softmax_cpattn_gb300 import build_lib
-    build_lib.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import blockwise_online_softmax_cpattn_gb300 as mod
     return mod
 
