@@ -146,8 +146,8 @@ def kernel_flops_or_bytes(name, w):
         return "tensor", 8.0 * w.D * pairs
     if name in ("tc_bwd_dq", "simt_bwd_dq"):         # the dQ product only
         return "tensor", 2.0 * w.D * pairs
-    if name == "bwd_delta":
-        return "hbm", 2.0 * rows_q * w.D * elt + 4.0 * rows_q
+    if name == "bwd_prepass":
+        return "hbm", 2.0 * rows_q * w.D * elt + 12.0 * rows_q
     if name.startswith("layout"):                    # per launch: one tensor read + written
         return "hbm", None
     return "hbm", None

@@ -203,10 +203,16 @@ cpattn_status cpattn_ring_fwd(const cpattn_desc* desc, const void* q, const void
   return from_cuda(launch_simt_fwd(R, -1, -1, q, k, v, o, lse, st));
 }
 
-size_t cpattn_ring_bwd_workspace(const cpattn_desc* desc) {
-  if (validate(desc, nullptr) != CPATTN_OK) return 0;
+// Workspace: Delta (float32 per query row), then the LSE in base 2 (float32 per
+// query row), each section 256-byte aligned.
+static size_t ws_section(const cpattn_desc* desc) {
   const size_t rows = (size_t)desc->B * desc->H_q * desc->T;
   return (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+size_t cpattn_ring_bwd_workspace(const cpattn_desc* desc) {
+  if (validate(desc, nullptr) != CPATTN_OK) return 0;
+  return 2 * ws_section(desc);
 }
 
 cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void* k,
@@ -224,11 +230,13 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
   float* delta = static_cast<float*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_section(desc));
   const int64_t rows = (int64_t)R.B * R.Hq * R.T;
-  cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, delta, st);
+  const bool tc = R.bf16 && tc_supported(R);
+  cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  if (R.bf16 && tc_supported(R))
-    return from_cuda(launch_tc_bwd(R, q, k, v, lse, delta, dO, dq, dk, dv, status_ptr(), st));
+  if (tc)
+    return from_cuda(launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st));
   e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   return from_cuda(launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st));

@@ -45,6 +45,50 @@ struct SeqMap {
   __host__ __device__ __forceinline__ int rank_of_slot(int s) const { return s / c; }
 };
 
+// Walk over the 128-token tiles of consecutive ring chunks without integer
+// divisions: `nchunks` chunks starting at `first`, stepping by `dir` (-1: the
+// order in which a rank receives K/V chunks, +1: the order in which a chunk's
+// gradient travels back), `reps` passes over each chunk's tiles (the query heads
+// of a K/V group), tiles of a chunk in slot order.
+struct TileWalk {
+  int cp, c, h, zz, tpc, reps, dir, nchunks;
+  int i, rep, t, s;
+  __device__ __forceinline__ void start(const SeqMap& m, int first, int n, int direction,
+                                        int repeats) {
+    cp = m.cp;
+    c = m.c;
+    h = m.h;
+    zz = m.zz;
+    tpc = m.c >> 7;
+    reps = repeats;
+    dir = direction;
+    nchunks = n;
+    i = 0;
+    rep = 0;
+    t = 0;
+    s = first;
+  }
+  __device__ __forceinline__ bool done() const { return i >= nchunks; }
+  __device__ __forceinline__ int slot() const { return s * c + (t << 7); }
+  __device__ __forceinline__ int pos() const {
+    const int w = t << 7;
+    if (!zz) return s * c + w;
+    return w < h ? s * h + w : (2 * cp - 1 - s) * h + (w - h);
+  }
+  __device__ __forceinline__ void next() {
+    if (++t == tpc) {
+      t = 0;
+      if (++rep == reps) {
+        rep = 0;
+        ++i;
+        s += dir;
+        if (s < 0) s += cp;
+        else if (s >= cp) s -= cp;
+      }
+    }
+  }
+};
+
 __device__ __forceinline__ void latch_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
@@ -276,6 +320,31 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA pipe, to take part of the exponentials off the special-
+// function unit.  Cody-Waite style split x = n + f with n = round(x) (via the
+// 1.5 * 2^23 rounding constant) and |f| <= 1/2; 2^f from a degree-3 polynomial
+// whose coefficients were fitted in this repository by the Remez exchange on
+// the relative error over [-1/2, 1/2]; 2^n is added to the exponent field.  Max
+// relative error 7.5e-5 for -125 <= x <= 127 (far below the 2^-9 rounding of a
+// bf16 probability); x < -126 (including -inf) returns exactly 0.
+__device__ __forceinline__ float ex2_poly(float x) {
+  const float t = x + 12582912.f;
+  const float n = t - 12582912.f;
+  const float f = x - n;
+  float q = fmaf(0.0551716685295105f, f, 0.2426111251115799f);
+  q = fmaf(q, f, 0.6932609677314758f);
+  q = fmaf(q, f, 0.9999280571937561f);
+  const float r = __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+  return x < -126.f ? 0.f : r;
+}
+
+// Exponential of column j of a row: columns with (j & 7) >= 6 (a quarter) go to
+// the FMA-pipe polynomial, the rest to the special-function unit.  j is a
+// constant in the fully unrolled loops that call this, so the choice folds away.
+__device__ __forceinline__ float ex2_mix(float x, int j) {
+  return (j & 7) >= 6 ? ex2_poly(x) : ex2(x);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

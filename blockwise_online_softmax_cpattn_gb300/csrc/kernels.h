@@ -30,9 +30,10 @@ cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cud
 // ---- merge.cu --------------------------------------------------------------
 cudaError_t launch_merge(int64_t rows, int D, const float* oa, const float* la, const float* ob,
                          const float* lb, float* oo, float* lo, cudaStream_t st);
-// delta[row] = sum_d dO[row, d] * O[row, d] (float32 accumulation)
+// delta[row] = sum_d dO[row, d] * O[row, d] (float32 accumulation); when lse2 is
+// not null also lse2[row] = lse[row] * log2(e).
 cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const void* dO,
-                         float* delta, cudaStream_t st);
+                         const float* lse, float* delta, float* lse2, cudaStream_t st);
 
 // ---- simt_attn.cu (exact float32 / any-D path) ------------------------------
 // partial: q_rank >= 0 selects one rank's queries against kv_rank's chunk and
@@ -52,7 +53,7 @@ bool tc_supported(const Ring& R);
 cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
                           const void* v, void* o, float* lse, int* status, cudaStream_t st);
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
-                          const float* lse, const float* delta, const void* dO, void* dq,
+                          const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st);
 
 // ---- api.cu: kernel timing hooks -------------------------------------------

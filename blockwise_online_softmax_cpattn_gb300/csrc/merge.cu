@@ -1,6 +1,7 @@
 // (O, LSE) merge of two partial results, and the backward pre-pass
-// Delta = rowsum(dO * O).  Both are HBM-bound row kernels: one warp per row,
-// 16-byte vector accesses, float32 arithmetic.
+// Delta = rowsum(dO * O) (plus the LSE rescaled to base 2 for the tensor-core
+// backward).  Both are HBM-bound row kernels: one warp per row, 16-byte vector
+// accesses, float32 arithmetic.
 #include <math.h>
 
 #include "kernels.h"
@@ -80,7 +81,9 @@ __device__ __forceinline__ float ld_f(const __nv_bfloat16* p, int64_t i) {
 template <typename T>
 __global__ void __launch_bounds__(256) delta_kernel(int64_t rows, int D, const T* __restrict__ o,
                                                     const T* __restrict__ dO,
-                                                    float* __restrict__ delta) {
+                                                    const float* __restrict__ lse,
+                                                    float* __restrict__ delta,
+                                                    float* __restrict__ lse2) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
@@ -102,25 +105,28 @@ __global__ void __launch_bounds__(256) delta_kernel(int64_t rows, int D, const T
     }
 #pragma unroll
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) delta[row] = acc;
+    if (lane == 0) {
+      delta[row] = acc;
+      if (lse2) lse2[row] = lse[row] * 1.44269504088896340736f;
+    }
   }
 }
 
 cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const void* dO,
-                         float* delta, cudaStream_t st) {
+                         const float* lse, float* delta, float* lse2, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int64_t blocks = (rows + 7) / 8;
   if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
   if (blocks < 1) blocks = 1;
-  timing_begin("bwd_delta", st);
+  timing_begin("bwd_prepass", st);
   if (bf16)
     delta_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
-        rows, D, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, delta);
+        rows, D, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, lse, delta, lse2);
   else
     delta_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(rows, D, (const float*)o,
-                                                          (const float*)dO, delta);
+                                                          (const float*)dO, lse, delta, lse2);
   cudaError_t e = cudaGetLastError();
   timing_end(st);
   return e;

@@ -43,7 +43,7 @@ struct Params {
   int B, Hq, Hkv, T, n_rep;
   SeqMap m;
   float scale, scale_log2;
-  const float* lse;
+  const float* lse2;   // LSE * log2(e), from the pre-pass
   const float* delta;
   void* out0;  // dkdv: dK ; dq: dQ
   void* out1;  // dkdv: dV
@@ -155,17 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kpos0 = ti * kTile;
   const int kslot0 = p.m.slot(kpos0);
   const int s_own = kslot0 / p.m.c;
-  const int c_tiles = p.m.c / kTile;
-  const int n_walk = p.m.cp * p.n_rep * c_tiles;
-  // query tile n of the walk: ring distance i, head hh of the group, tile t
-  auto q_tile = [&](int n, int& h, int& qslot0) {
-    const int i = n / (p.n_rep * c_tiles);
-    const int r2 = n - i * (p.n_rep * c_tiles);
-    const int hh = r2 / c_tiles, t = r2 - hh * c_tiles;
-    const int r = (s_own + i) % p.m.cp;
-    h = g * p.n_rep + hh;
-    qslot0 = r * p.m.c + t * kTile;
-  };
+  // query tiles in the order the chunk's gradient travels the ring back to its
+  // owner: ranks s, s+1, ..., s-1; every query head of the group per rank
+  auto walk_start = [&](TileWalk& w) { w.start(p.m, s_own, p.m.cp, +1, p.n_rep); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -179,33 +171,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sbase + L::kK + kb * (kTile * 128), &tm_k, kb * 64, krow, kv_full);
         tma_load_2d(sbase + L::kV + kb * (kTile * 128), &tm_v, kb * 64, krow, kv_full);
       }
-      int stage = 0, par = 0, issued[S], ipar[S];
-      for (int s = 0; s < S; ++s) issued[s] = 0, ipar[s] = 0;
-      for (int n = 0; n < n_walk; ++n) {
-        int h, qslot0;
-        q_tile(n, h, qslot0);
-        if (classify(p.m.pos(qslot0), kpos0) == kEmpty) continue;
+      int stage = 0, par = 0;
+      uint32_t issued = 0, ipar = 0;  // bit s: stage s loaded / its phase parity
+      TileWalk wk;
+      for (walk_start(wk); !wk.done(); wk.next()) {
+        if (classify(wk.pos(), kpos0) == kEmpty) continue;
         if (!mbar_wait(qdo_empty(stage), par ^ 1, abort, p.status, kTimeoutNs)) break;
-        const int qrow = (b * p.Hq + h) * p.T + qslot0;
+        const int qrow = (b * p.Hq + g * p.n_rep + wk.rep) * p.T + wk.slot();
         mbar_expect_tx(q_full(stage), L::kTB + 1024);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kQ + stage * L::kTB + kb * (kTile * 128), &tm_q, kb * 64, qrow,
                       q_full(stage));
-        bulk_load(sbase + L::kLse + stage * 512, p.lse + qrow, 512, q_full(stage));
+        bulk_load(sbase + L::kLse + stage * 512, p.lse2 + qrow, 512, q_full(stage));
         bulk_load(sbase + L::kDelta + stage * 512, p.delta + qrow, 512, q_full(stage));
         mbar_expect_tx(do_full(stage), L::kTB);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kDO + stage * L::kTB + kb * (kTile * 128), &tm_do, kb * 64, qrow,
                       do_full(stage));
-        issued[stage] = 1;
-        ipar[stage] = par;
+        issued |= 1u << stage;
+        ipar = (ipar & ~(1u << stage)) | ((uint32_t)par << stage);
         if (++stage == S) stage = 0, par ^= 1;
       }
       drain_wait(kv_full, 0);
       for (int s = 0; s < S; ++s)
-        if (issued[s]) {
-          drain_wait(q_full(s), ipar[s]);
-          drain_wait(do_full(s), ipar[s]);
+        if ((issued >> s) & 1u) {
+          drain_wait(q_full(s), (ipar >> s) & 1u);
+          drain_wait(do_full(s), (ipar >> s) & 1u);
         }
     }
   } else if (warp == 1) {
@@ -214,13 +205,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(kv_full, 0, abort, p.status, kTimeoutNs);
       tc_fence_after();
+      // descriptor bases (16-byte units); K-major for S^T/dP^T, MN-major for dV/dK
+      constexpr uint32_t kTD = L::kTB >> 4;
+      const uint64_t kd = sdesc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t vd = sdesc_sw128(sbase + L::kV, 16, 1024);
+      const uint64_t qd_k0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dod_k0 = sdesc_sw128(sbase + L::kDO, 16, 1024);
+      const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQ, kTile * 128, 1024);
+      const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
       int stage = 0, par = 0, cnt = 0;
-      for (int n = 0; n < n_walk && ok; ++n) {
-        int h, qslot0;
-        q_tile(n, h, qslot0);
-        if (classify(p.m.pos(qslot0), kpos0) == kEmpty) continue;
-        const uint32_t qa = sbase + L::kQ + stage * L::kTB;
-        const uint32_t da = sbase + L::kDO + stage * L::kTB;
+      TileWalk wk;
+      for (walk_start(wk); !wk.done() && ok; wk.next()) {
+        if (classify(wk.pos(), kpos0) == kEmpty) continue;
+        const uint64_t soff = (uint64_t)(stage * kTD);
         // S^T = K Q^T  (the S region is free once the previous dV has read P^T)
         if (!(ok = mbar_wait(q_full(stage), par, abort, p.status, kTimeoutNs))) break;
         if (cnt > 0 && !(ok = mbar_wait(dv_done, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
@@ -228,9 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_ss(tmem, sdesc_sw128(sbase + L::kK + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                 kIdSS, kk > 0);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+          mma_ss(tmem, kd + off, qd_k0 + soff + off, kIdSS, kk > 0);
         }
         mma_commit(s_full);
         // dP^T = V dO^T  (the dP region is free once the previous dK has read dS^T)
@@ -240,9 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_ss(tmem + 128, sdesc_sw128(sbase + L::kV + off, 16, 1024),
-                 sdesc_sw128(da + off, 16, 1024), kIdSS, kk > 0);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+          mma_ss(tmem + 128, vd + off, dod_k0 + soff + off, kIdSS, kk > 0);
         }
         mma_commit(dp_full);
         // dV += P^T dO
@@ -251,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t acol = (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + 256, tmem + acol, sdesc_sw128(da + kk * 2048, kTile * 128, 1024), kIdTS,
+          mma_ts(tmem + 256, tmem + acol, dod_mn0 + soff + kk * 128, kIdTS,
                  (cnt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(dv_done);
@@ -261,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t acol = 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + 256 + D, tmem + acol, sdesc_sw128(qa + kk * 2048, kTile * 128, 1024), kIdTS,
+          mma_ts(tmem + 256 + D, tmem + acol, qd_mn0 + soff + kk * 128, kIdTS,
                  (cnt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(dk_done);
@@ -282,10 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* del_s = reinterpret_cast<const float*>(smem + L::kDelta);
     int stage = 0, par = 0, cnt = 0;
     bool ok = true;
-    for (int n = 0; n < n_walk; ++n) {
-      int h, qslot0;
-      q_tile(n, h, qslot0);
-      const int qpos0 = p.m.pos(qslot0);
+    TileWalk wk;
+    for (walk_start(wk); !wk.done(); wk.next()) {
+      const int qpos0 = wk.pos();
       const int cls = classify(qpos0, kpos0);
       if (cls == kEmpty) continue;
       if (!(ok = warp_wait(q_full(stage), par, abort, p.status))) break;  // LSE, Delta landed
@@ -306,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const int j0 = c * 32 + j;
-          float p0 = ex2(fmaf(__uint_as_float(sr[c][j]), p.scale_log2, -lse_t[j0] * kLog2e));
-          float p1 = ex2(fmaf(__uint_as_float(sr[c][j + 1]), p.scale_log2, -lse_t[j0 + 1] * kLog2e));
+          float p0 = ex2_mix(fmaf(__uint_as_float(sr[c][j]), p.scale_log2, -lse_t[j0]), j);
+          float p1 = ex2_mix(fmaf(__uint_as_float(sr[c][j + 1]), p.scale_log2, -lse_t[j0 + 1]), j + 1);
           if (cls == kDiag) {
             if (j0 < thr) p0 = 0.f;
             if (j0 + 1 < thr) p1 = 0.f;
@@ -450,11 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qpos0 = (n_q_tiles - 1 - ti) * kTile;
   const int qslot0 = p.m.slot(qpos0);
   const int r_own = qslot0 / p.m.c;
-  const int c_tiles = p.m.c / kTile;
-  const int n_walk = p.m.cp * c_tiles;
-  auto kv_slot = [&](int n) {
-    const int step = n / c_tiles, t = n - step * c_tiles;
-    return ((r_own - step + p.m.cp) % p.m.cp) * p.m.c + t * kTile;
+  // K/V tiles in ring order (chunks r, r-1, ...), hidden tiles skipped
+  auto walk_start = [&](TileWalk& w) {
+    w.start(p.m, r_own, p.m.cp, -1, 1);
+    while (!w.done() && classify(qpos0, w.pos()) == kEmpty) w.next();
+  };
+  auto walk_next = [&](TileWalk& w) {
+    do w.next(); while (!w.done() && classify(qpos0, w.pos()) == kEmpty);
   };
   const int64_t qrow = ((int64_t)b * p.Hq + h) * p.T + qslot0;
   const int kv_row_base = (b * p.Hkv + g) * p.T;
@@ -470,13 +466,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)qrow, qdo_full);
         tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)qrow, qdo_full);
       }
-      int stage = 0, par = 0, issued[S], ipar[S];
-      for (int s = 0; s < S; ++s) issued[s] = 0, ipar[s] = 0;
-      for (int n = 0; n < n_walk; ++n) {
-        const int ks = kv_slot(n);
-        if (classify(qpos0, p.m.pos(ks)) == kEmpty) continue;
+      int stage = 0, par = 0;
+      uint32_t issued = 0, ipar = 0;  // bit s: stage s loaded / its phase parity
+      TileWalk wk;
+      for (walk_start(wk); !wk.done(); walk_next(wk)) {
         if (!mbar_wait(kv_empty(stage), par ^ 1, abort, p.status, kTimeoutNs)) break;
-        const int row = kv_row_base + ks;
+        const int row = kv_row_base + wk.slot();
         mbar_expect_tx(k_full(stage), L::kTB);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kK + stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64, row,
@@ -485,15 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kV + stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64, row,
                       v_full(stage));
-        issued[stage] = 1;
-        ipar[stage] = par;
+        issued |= 1u << stage;
+        ipar = (ipar & ~(1u << stage)) | ((uint32_t)par << stage);
         if (++stage == S) stage = 0, par ^= 1;
       }
       drain_wait(qdo_full, 0);
       for (int s = 0; s < S; ++s)
-        if (issued[s]) {
-          drain_wait(k_full(s), ipar[s]);
-          drain_wait(v_full(s), ipar[s]);
+        if ((issued >> s) & 1u) {
+          drain_wait(k_full(s), (ipar >> s) & 1u);
+          drain_wait(v_full(s), (ipar >> s) & 1u);
         }
     }
   } else if (warp == 1) {
@@ -502,23 +497,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(qdo_full, 0, abort, p.status, kTimeoutNs);
       tc_fence_after();
+      // descriptor bases (16-byte units)
+      constexpr uint32_t kTD = L::kTB >> 4;
+      const uint64_t qd = sdesc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dod = sdesc_sw128(sbase + L::kDO, 16, 1024);
+      const uint64_t kd_k0 = sdesc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t vd_k0 = sdesc_sw128(sbase + L::kV, 16, 1024);
+      const uint64_t kd_mn0 = sdesc_sw128(sbase + L::kK, kTile * 128, 1024);
       // visited tiles in order; S/dP of tile j+1 are issued before dQ of tile j
-      int n_next = 0;
-      auto next_visit = [&](int from) {
-        for (int n = from; n < n_walk; ++n)
-          if (classify(qpos0, p.m.pos(kv_slot(n))) != kEmpty) return n;
-        return n_walk;
-      };
       int stage = 0, par = 0;
       auto issue_s = [&](int st, int pr) -> bool {
         if (!mbar_wait(k_full(st), pr, abort, p.status, kTimeoutNs)) return false;
         tc_fence_after();
-        const uint32_t ka = sbase + L::kK + st * L::kTB;
+        const uint64_t kd = kd_k0 + (uint64_t)(st * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_ss(tmem, sdesc_sw128(sbase + L::kQ + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 kIdSS, kk > 0);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+          mma_ss(tmem, qd + off, kd + off, kIdSS, kk > 0);
         }
         mma_commit(s_full);
         return true;
@@ -526,43 +521,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_dp = [&](int st, int pr, int buf) -> bool {
         if (!mbar_wait(v_full(st), pr, abort, p.status, kTimeoutNs)) return false;
         tc_fence_after();
-        const uint32_t va = sbase + L::kV + st * L::kTB;
+        const uint64_t vd = vd_k0 + (uint64_t)(st * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_ss(tmem + 128 + 128 * buf, sdesc_sw128(sbase + L::kDO + off, 16, 1024),
-                 sdesc_sw128(va + off, 16, 1024), kIdSS, kk > 0);
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+          mma_ss(tmem + 128 + 128 * buf, dod + off, vd + off, kIdSS, kk > 0);
         }
         mma_commit(dp_full);
         return true;
       };
       int j = 0;
-      n_next = next_visit(0);
-      if (ok && n_next < n_walk) ok = issue_s(stage, par) && issue_dp(stage, par, 0);
-      while (ok && n_next < n_walk) {
-        const int n_after = next_visit(n_next + 1);
+      TileWalk cur;
+      walk_start(cur);
+      if (ok && !cur.done()) ok = issue_s(stage, par) && issue_dp(stage, par, 0);
+      while (ok && !cur.done()) {
+        TileWalk nxt = cur;
+        walk_next(nxt);
+        const bool has_next = !nxt.done();
         const int cur_stage = stage, cur_buf = j & 1;
         int nstage = stage + 1, npar = par;
         if (nstage == S) nstage = 0, npar ^= 1;
         // S of the next tile as soon as this tile's S has been read out
-        if (n_after < n_walk) {
+        if (has_next) {
           if (!(ok = mbar_wait(s_free, j & 1, abort, p.status, kTimeoutNs))) break;
           if (!(ok = issue_s(nstage, npar))) break;
         }
         // dQ += dS K
         if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
-        const uint32_t ka = sbase + L::kK + cur_stage * L::kTB;
+        const uint64_t kd_mn = kd_mn0 + (uint64_t)(cur_stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t acol = 128 + 128 * cur_buf + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + kDqCol, tmem + acol, sdesc_sw128(ka + kk * 2048, kTile * 128, 1024), kIdTS,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(dq_done(cur_buf));
         mma_commit(kv_empty(cur_stage));
         // dP of the next tile into the other buffer, once dQ of tile j-1 has read it
-        if (n_after < n_walk) {
+        if (has_next) {
           if (j >= 1 &&
               !(ok = mbar_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status,
                                kTimeoutNs)))
@@ -572,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         stage = nstage;
         par = npar;
-        n_next = n_after;
+        cur = nxt;
         ++j;
       }
       mma_commit(final_bar);
@@ -583,15 +579,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;  // query row of the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + half * 64;
-    const float lse2 = p.lse[qrow + row] * kLog2e;
+    const float lse2 = p.lse2[qrow + row];
     const float dl = p.delta[qrow + row];
     int j = 0;
     bool ok = true;
-    for (int n = 0; n < n_walk; ++n) {
-      const int ks = kv_slot(n);
-      const int kpos0 = p.m.pos(ks);
+    TileWalk wk;
+    for (walk_start(wk); !wk.done(); walk_next(wk)) {
+      const int kpos0 = wk.pos();
       const int cls = classify(qpos0, kpos0);
-      if (cls == kEmpty) continue;
       if (!(ok = warp_wait(s_full, j & 1, abort, p.status))) break;
       tc_fence_after();
       uint32_t sr[2][32];
@@ -608,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j0 = c * 32 + jj;
-          float pv = ex2(fmaf(__uint_as_float(sr[c][jj]), p.scale_log2, -lse2));
+          float pv = ex2_mix(fmaf(__uint_as_float(sr[c][jj]), p.scale_log2, -lse2), jj);
           if (cls == kDiag && j0 > thr) pv = 0.f;
           pr[j0] = pv;
         }
@@ -704,7 +699,7 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
 }  // namespace tcbwd
 
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
-                          const float* lse, const float* delta, const void* dO, void* dq,
+                          const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st) {
   tcbwd::Params p;
   p.B = R.B;
@@ -715,7 +710,7 @@ cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const voi
   p.m = SeqMap::make(R.T, R.cp, R.zz);
   p.scale = R.scale;
   p.scale_log2 = R.scale * tcbwd::kLog2e;
-  p.lse = lse;
+  p.lse2 = lse2;
   p.delta = delta;
   p.status = status;
   if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st);

@@ -116,15 +116,6 @@ __device__ __forceinline__ Item decode(const Params& p, int w) {
   return it;
 }
 
-// Key/value tile n of the walk: step n / c_tiles of the ring, tile n % c_tiles
-// of the chunk held at that step.
-__device__ __forceinline__ int walk_slot(const Params& p, const Item& it, int n, int c_tiles) {
-  const int step = n / c_tiles;
-  const int t = n - step * c_tiles;
-  const int s = p.q_rank >= 0 ? p.kv_rank : (it.rank - step + p.m.cp) % p.m.cp;
-  return s * p.m.c + t * kTile;
-}
-
 __device__ __forceinline__ int classify(int qpos0, int kpos0) {
   if (kpos0 + kTile - 1 <= qpos0) return kFull;
   if (kpos0 > qpos0 + kTile - 1) return kEmpty;
@@ -188,8 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const Item it = decode(p, blockIdx.x);
-  const int c_tiles = p.m.c / kTile;
-  const int n_walk = (p.q_rank >= 0 ? 1 : p.m.cp) * c_tiles;
+  // K/V tiles in ring order: chunks r, r-1, ..., r-cp+1 (mod cp), or one chunk
+  const int kv_first = p.q_rank >= 0 ? p.kv_rank : it.rank;
+  const int kv_chunks = p.q_rank >= 0 ? 1 : p.m.cp;
   const int kv_row_base = (it.b * p.Hkv + it.g) * p.T;
 
   if (warp == 0) {
@@ -210,16 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         q_issued[x] = 1;
       }
       int stage = 0, par = 0;
-      int issued[S], issued_par[S];
-      for (int s = 0; s < S; ++s) issued[s] = 0, issued_par[s] = 0;
-      for (int n = 0; n < n_walk; ++n) {
-        const int kslot = walk_slot(p, it, n, c_tiles);
-        const int kpos = p.m.pos(kslot);
+      uint32_t issued = 0, issued_par = 0;  // bit s: stage s loaded / its phase parity
+      TileWalk wk;
+      for (wk.start(p.m, kv_first, kv_chunks, -1, 1); !wk.done(); wk.next()) {
+        const int kpos = wk.pos();
         const int ca = classify(it.pos0[0], kpos);
         const int cb = it.active[1] ? classify(it.pos0[1], kpos) : kEmpty;
         if (ca == kEmpty && cb == kEmpty) continue;
         if (!mbar_wait(kv_empty(stage), par ^ 1, abort, p.status, tmo)) break;
-        const int row = kv_row_base + kslot;
+        const int row = kv_row_base + wk.slot();
         mbar_expect_tx(k_full(stage), L::kTileBytes);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kK + stage * L::kTileBytes + kb * (kTile * 128), &tm_k, kb * 64,
@@ -228,17 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kV + stage * L::kTileBytes + kb * (kTile * 128), &tm_v, kb * 64,
                       row, v_full(stage));
-        issued[stage] = 1;
-        issued_par[stage] = par;
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | ((uint32_t)par << stage);
         if (++stage == S) stage = 0, par ^= 1;
       }
       // never leave with a copy still writing into this CTA's shared memory
       for (int x = 0; x < 2; ++x)
         if (q_issued[x]) drain_wait(q_full(x), 0);
       for (int s = 0; s < S; ++s)
-        if (issued[s]) {
-          drain_wait(k_full(s), issued_par[s]);
-          drain_wait(v_full(s), issued_par[s]);
+        if ((issued >> s) & 1u) {
+          drain_wait(k_full(s), (issued_par >> s) & 1u);
+          drain_wait(v_full(s), (issued_par >> s) & 1u);
         }
     }
   } else if (warp == 1) {
@@ -250,43 +241,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = 0; x < 2 && ok; ++x)
         if (it.active[x]) ok = mbar_wait(q_full(x), 0, abort, p.status, tmo);
       tc_fence_after();
+      // descriptor bases; per k-step offsets are compile-time constants (16-byte units)
+      constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
+      const uint64_t qd0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t kd0 = sdesc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t vd0 = sdesc_sw128(sbase + L::kV, kTile * 128, 1024);
       int stage = 0, par = 0, cnt[2] = {0, 0};
-      for (int n = 0; n < n_walk && ok; ++n) {
-        const int kslot = walk_slot(p, it, n, c_tiles);
-        const int kpos = p.m.pos(kslot);
+      TileWalk wk;
+      for (wk.start(p.m, kv_first, kv_chunks, -1, 1); !wk.done() && ok; wk.next()) {
+        const int kpos = wk.pos();
         int cls[2];
         cls[0] = classify(it.pos0[0], kpos);
         cls[1] = it.active[1] ? classify(it.pos0[1], kpos) : kEmpty;
         if (cls[0] == kEmpty && cls[1] == kEmpty) continue;
         if (!(ok = mbar_wait(k_full(stage), par, abort, p.status, tmo))) break;
         tc_fence_after();
-        const uint32_t kaddr = sbase + L::kK + stage * L::kTileBytes;
+        const uint64_t kd = kd0 + (uint64_t)(stage * kTileDesc);
         for (int x = 0; x < 2 && ok; ++x) {
           if (cls[x] == kEmpty) continue;
           if (cnt[x] > 0 && !(ok = mbar_wait(pv_done(x), (cnt[x] - 1) & 1, abort, p.status, tmo)))
             break;
           tc_fence_after();
-          const uint32_t qaddr = sbase + L::kQ + x * L::kTileBytes;
+          const uint64_t qd = qd0 + (uint64_t)(x * kTileDesc);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-            mma_ss(tmem + x * 128, sdesc_sw128(qaddr + off, 16, 1024),
-                   sdesc_sw128(kaddr + off, 16, 1024), kIdescS, kk > 0);
+            const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KiB blocks, 32 B steps
+            mma_ss(tmem + x * 128, qd + off, kd + off, kIdescS, kk > 0);
           }
           mma_commit(s_full(x));
         }
         if (!ok) break;
         if (!(ok = mbar_wait(v_full(stage), par, abort, p.status, tmo))) break;
         tc_fence_after();
-        const uint32_t vaddr = sbase + L::kV + stage * L::kTileBytes;
+        const uint64_t vd = vd0 + (uint64_t)(stage * kTileDesc);
         for (int x = 0; x < 2 && ok; ++x) {
           if (cls[x] == kEmpty) continue;
           if (!(ok = mbar_wait(p_full(x), cnt[x] & 1, abort, p.status, tmo))) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8,
-                   sdesc_sw128(vaddr + kk * 2048, kTile * 128, 1024), kIdescPV,
+          for (int kk = 0; kk < kTile / 16; ++kk)  // 16 key rows = 2048 B per k-step
+            mma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, vd + kk * 128, kIdescPV,
                    (cnt[x] > 0 || kk > 0) ? 1u : 0u);
           mma_commit(pv_done(x));
           ++cnt[x];
@@ -312,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cnt = 0;
     bool ok = true;
     if (it.active[x]) {
-      for (int n = 0; n < n_walk; ++n) {
-        const int kslot = walk_slot(p, it, n, c_tiles);
-        const int kpos = p.m.pos(kslot);
+      TileWalk wk;
+      for (wk.start(p.m, kv_first, kv_chunks, -1, 1); !wk.done(); wk.next()) {
+        const int kpos = wk.pos();
         const int cls = classify(it.pos0[x], kpos);
         if (cls == kEmpty) continue;
         if (!(ok = warp_wait(s_full(x), cnt & 1, abort, p.status, tmo))) break;
@@ -333,10 +327,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 32; ++j)
               if (c * 32 + j > thr) r[c][j] = __float_as_uint(-INFINITY);
         }
+        {
+          // 8 independent max chains instead of one 128-long dependency chain
+          float m8[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(r[c][j]));
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(r[c][j]));
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        }
         const float m_new = fmaxf(m_run, mx * sl2);
         bool rescale = false;
         float factor = 1.f;
@@ -349,20 +351,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float mu = m_run == -INFINITY ? 0.f : m_run;
-        float lsum = 0.f;
+        float l8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) l8[i] = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float p0 = ex2(fmaf(__uint_as_float(r[c][2 * j]), sl2, -mu));
-            const float p1 = ex2(fmaf(__uint_as_float(r[c][2 * j + 1]), sl2, -mu));
-            lsum += p0 + p1;
+            const float p0 = ex2_mix(fmaf(__uint_as_float(r[c][2 * j]), sl2, -mu), 2 * j);
+            const float p1 = ex2_mix(fmaf(__uint_as_float(r[c][2 * j + 1]), sl2, -mu), 2 * j + 1);
+            l8[(2 * j) & 7] += p0;
+            l8[(2 * j + 1) & 7] += p1;
             pk[j] = pack_bf16(p0, p1);
           }
           tmem_st16(t_s + c * 16, pk);
         }
-        l_run += lsum;
+        l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         tmem_wait_st();
         if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
           // the output so far must be final in TMEM before it is rescaled
