@@ -312,6 +312,19 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Register split between warpgroups (setmaxnreg): the control warpgroup (TMA
+// producer, MMA issuer) gives registers back, the math warpgroups take them.
+// The sum over the block must not exceed what the launch allocated (checked on
+// the host against the kernel's compiled register count before every launch).
+constexpr uint32_t kRegsCtl = 80;
+constexpr uint32_t kRegsMath = 208;
+__device__ __forceinline__ void regs_ctl() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+}
+__device__ __forceinline__ void regs_math() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsMath));
+}
+
 // ---------------------------------------------------------------------------
 // Small arithmetic helpers
 // ---------------------------------------------------------------------------
@@ -322,29 +335,41 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, to take part of the exponentials off the special-
-// function unit.  Cody-Waite style split x = n + f with n = round(x) (via the
-// 1.5 * 2^23 rounding constant) and |f| <= 1/2; 2^f from a degree-3 polynomial
-// whose coefficients were fitted in this repository by the Remez exchange on
-// the relative error over [-1/2, 1/2]; 2^n is added to the exponent field.  Max
-// relative error 7.5e-5 for -125 <= x <= 127 (far below the 2^-9 rounding of a
-// bf16 probability); x < -126 (including -inf) returns exactly 0.
-__device__ __forceinline__ float ex2_poly(float x) {
-  const float t = x + 12582912.f;
-  const float n = t - 12582912.f;
-  const float f = x - n;
-  float q = fmaf(0.0551716685295105f, f, 0.2426111251115799f);
-  q = fmaf(q, f, 0.6932609677314758f);
-  q = fmaf(q, f, 0.9999280571937561f);
-  const float r = __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
-  return x < -126.f ? 0.f : r;
+// Packed two-lane fp32 arithmetic (sm_100 and later): one issue slot for two
+// lanes' worth of FP32 work.  The kernels' softmax phases are issue-bound, so
+// these halve their FMA/ADD/MUL instruction count.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
-
-// Exponential of column j of a row: columns with (j & 7) >= 6 (a quarter) go to
-// the FMA-pipe polynomial, the rest to the special-function unit.  j is a
-// constant in the fully unrolled loops that call this, so the choice folds away.
-__device__ __forceinline__ float ex2_mix(float x, int j) {
-  return (j & 7) >= 6 ? ex2_poly(x) : ex2(x);
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// max(a, b, c) in one instruction (three-input form of max.f32, sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

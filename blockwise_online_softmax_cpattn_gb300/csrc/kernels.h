@@ -30,8 +30,9 @@ cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cud
 // ---- merge.cu --------------------------------------------------------------
 cudaError_t launch_merge(int64_t rows, int D, const float* oa, const float* la, const float* ob,
                          const float* lb, float* oo, float* lo, cudaStream_t st);
-// delta[row] = sum_d dO[row, d] * O[row, d] (float32 accumulation); when lse2 is
-// not null also lse2[row] = lse[row] * log2(e).
+// delta[row] = sum_d dO[row, d] * O[row, d] (float32 accumulation).  When lse2 is
+// not null (the tensor-core backward's form) the statistics are stored negated:
+// delta[row] = -Delta and lse2[row] = -lse[row] * log2(e).
 cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const void* dO,
                          const float* lse, float* delta, float* lse2, cudaStream_t st);
 
@@ -55,6 +56,18 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st);
+
+// The register split of the tensor-core kernels (3 warpgroups: one control, two
+// math) must fit in what a launch of `kern` allocates; a split that does not fit
+// would make setmaxnreg.inc wait forever, so such a launch is refused.
+template <typename K>
+inline cudaError_t check_register_split(K kern, int threads) {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, kern);
+  if (e != cudaSuccess) return e;
+  const long need = 128L * kRegsCtl + (long)(threads - 128) * kRegsMath;
+  return (long)a.numRegs * threads >= need ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
 
 // ---- api.cu: kernel timing hooks -------------------------------------------
 void timing_begin(const char* name, cudaStream_t st);

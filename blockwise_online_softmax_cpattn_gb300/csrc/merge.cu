@@ -106,8 +106,12 @@ __global__ void __launch_bounds__(256) delta_kernel(int64_t rows, int D, const T
 #pragma unroll
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-      delta[row] = acc;
-      if (lse2) lse2[row] = lse[row] * 1.44269504088896340736f;
+      if (lse2) {  // tensor-core form: both statistics negated, LSE in base 2
+        delta[row] = -acc;
+        lse2[row] = -lse[row] * 1.44269504088896340736f;
+      } else {
+        delta[row] = acc;
+      }
     }
   }
 }

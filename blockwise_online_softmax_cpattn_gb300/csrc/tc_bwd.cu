@@ -43,8 +43,8 @@ struct Params {
   int B, Hq, Hkv, T, n_rep;
   SeqMap m;
   float scale, scale_log2;
-  const float* lse2;   // LSE * log2(e), from the pre-pass
-  const float* delta;
+  const float* lse2;   // -LSE * log2(e) per query row, from the pre-pass
+  const float* delta;  // -Delta per query row, from the pre-pass
   void* out0;  // dkdv: dK ; dq: dQ
   void* out1;  // dkdv: dV
   int* status;
@@ -159,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // owner: ranks s, s+1, ..., s-1; every query head of the group per rank
   auto walk_start = [&](TileWalk& w) { w.start(p.m, s_own, p.m.cp, +1, p.n_rep); };
 
+  if (warp < 4) {
+  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuer (warp 1)
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -267,7 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(final_bar);
       drain_wait(final_bar, 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    regs_math();  // warpgroups 1 and 2: softmax / gradient math
     const int quad = warp & 3, half = (warp - 4) >> 2;
     const int row = quad * 32 + lane;  // key row of the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -294,14 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // query column j (of this half) sees this key row iff kpos0 + row <= qpos0 + 64*half + j
       const int thr = kpos0 + row - qpos0 - half * 64;
       float pr[64];
+      const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const int j0 = c * 32 + j;
-          float p0 = ex2_mix(fmaf(__uint_as_float(sr[c][j]), p.scale_log2, -lse_t[j0]), j);
-          float p1 = ex2_mix(fmaf(__uint_as_float(sr[c][j + 1]), p.scale_log2, -lse_t[j0 + 1]), j + 1);
+          // P = 2^(S scale log2e - LSE log2e), the exponent argument two lanes at a time
+          const float2 nl = reinterpret_cast<const float2*>(lse_t)[j0 >> 1];
+          const float2 x = fma2(make_float2(__uint_as_float(sr[c][j]), __uint_as_float(sr[c][j + 1])),
+                                sl2v, nl);
+          float p0 = ex2(x.x), p1 = ex2(x.y);
           if (cls == kDiag) {
             if (j0 < thr) p0 = 0.f;
             if (j0 + 1 < thr) p1 = 0.f;
@@ -326,9 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const int j0 = c * 32 + j;
-          const float d0 = pr[j0] * (__uint_as_float(sr[c][j]) - del_t[j0]);
-          const float d1 = pr[j0 + 1] * (__uint_as_float(sr[c][j + 1]) - del_t[j0 + 1]);
-          pk[j >> 1] = pack_bf16(d0, d1);
+          // dS = P (dP - Delta), two lanes per instruction (del_t holds -Delta)
+          const float2 nd = reinterpret_cast<const float2*>(del_t)[j0 >> 1];
+          const float2 d = mul2(make_float2(pr[j0], pr[j0 + 1]),
+                                add2(make_float2(__uint_as_float(sr[c][j]),
+                                                 __uint_as_float(sr[c][j + 1])), nd));
+          pk[j >> 1] = pack_bf16(d.x, d.y);
         }
         tmem_st16(t_dp + c * 16, pk);
       }
@@ -455,6 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t qrow = ((int64_t)b * p.Hq + h) * p.T + qslot0;
   const int kv_row_base = (b * p.Hkv + g) * p.T;
 
+  if (warp < 4) {
+  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuer (warp 1)
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -541,10 +554,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cur_stage = stage, cur_buf = j & 1;
         int nstage = stage + 1, npar = par;
         if (nstage == S) nstage = 0, npar ^= 1;
-        // S of the next tile as soon as this tile's S has been read out
+        // S of the next tile as soon as this tile's S has been read out, and dP of the
+        // next tile into the other buffer once dQ of tile j-1 has read it, both ahead
+        // of dQ of this tile so the compute warps never wait on this tile's dS
         if (has_next) {
           if (!(ok = mbar_wait(s_free, j & 1, abort, p.status, kTimeoutNs))) break;
           if (!(ok = issue_s(nstage, npar))) break;
+          if (j >= 1 &&
+              !(ok = mbar_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status,
+                               kTimeoutNs)))
+            break;
+          tc_fence_after();
+          if (!(ok = issue_dp(nstage, npar, (j + 1) & 1))) break;
         }
         // dQ += dS K
         if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status, kTimeoutNs))) break;
@@ -557,15 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(dq_done(cur_buf));
         mma_commit(kv_empty(cur_stage));
-        // dP of the next tile into the other buffer, once dQ of tile j-1 has read it
-        if (has_next) {
-          if (j >= 1 &&
-              !(ok = mbar_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status,
-                               kTimeoutNs)))
-            break;
-          tc_fence_after();
-          if (!(ok = issue_dp(nstage, npar, (j + 1) & 1))) break;
-        }
         stage = nstage;
         par = npar;
         cur = nxt;
@@ -574,13 +586,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(final_bar);
       drain_wait(final_bar, 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    regs_math();  // warpgroups 1 and 2: softmax / gradient math
     const int quad = warp & 3, half = (warp - 4) >> 2;
     const int row = quad * 32 + lane;  // query row of the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + half * 64;
-    const float lse2 = p.lse2[qrow + row];
-    const float dl = p.delta[qrow + row];
+    const float2 nl2 = make_float2(p.lse2[qrow + row], p.lse2[qrow + row]);  // -LSE log2e
+    const float2 ndl = make_float2(p.delta[qrow + row], p.delta[qrow + row]);  // -Delta
+    const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
     int j = 0;
     bool ok = true;
     TileWalk wk;
@@ -601,11 +616,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
+        for (int jj = 0; jj < 32; jj += 2) {
           const int j0 = c * 32 + jj;
-          float pv = ex2_mix(fmaf(__uint_as_float(sr[c][jj]), p.scale_log2, -lse2), jj);
-          if (cls == kDiag && j0 > thr) pv = 0.f;
-          pr[j0] = pv;
+          const float2 x = fma2(make_float2(__uint_as_float(sr[c][jj]), __uint_as_float(sr[c][jj + 1])),
+                                sl2v, nl2);
+          float p0 = ex2(x.x), p1 = ex2(x.y);
+          if (cls == kDiag) {
+            if (j0 > thr) p0 = 0.f;
+            if (j0 + 1 > thr) p1 = 0.f;
+          }
+          pr[j0] = p0;
+          pr[j0 + 1] = p1;
         }
       if (!(ok = warp_wait(dp_full, j & 1, abort, p.status))) break;
       tc_fence_after();
@@ -619,8 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < 32; jj += 2) {
           const int j0 = c * 32 + jj;
-          pk[jj >> 1] = pack_bf16(pr[j0] * (__uint_as_float(sr[c][jj]) - dl),
-                                  pr[j0 + 1] * (__uint_as_float(sr[c][jj + 1]) - dl));
+          const float2 d = mul2(make_float2(pr[j0], pr[j0 + 1]),
+                                add2(make_float2(__uint_as_float(sr[c][jj]),
+                                                 __uint_as_float(sr[c][jj + 1])), ndl));
+          pk[jj >> 1] = pack_bf16(d.x, d.y);
         }
         tmem_st16(t_dp + c * 16, pk);
       }
@@ -658,7 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename K>
 static cudaError_t prep(K kern, int smem) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return check_register_split(kern, kThreads);
 }
 
 template <int D>

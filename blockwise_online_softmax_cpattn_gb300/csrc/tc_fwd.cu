@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kv_chunks = p.q_rank >= 0 ? 1 : p.m.cp;
   const int kv_row_base = (it.b * p.Hkv + it.g) * p.T;
 
+  if (warp < 4) {
+  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuer (warp 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -293,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(final_bar);
       drain_wait(final_bar, 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    regs_math();  // warpgroups 1 and 2: softmax / gradient math
     // ------------------------------------------------------------ softmax
     const int x = (warp - 4) >> 2;  // tile A (warps 4..7) or B (warps 8..11)
     const int quad = warp & 3;      // TMEM lane quadrant this warp may access
@@ -328,16 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (c * 32 + j > thr) r[c][j] = __float_as_uint(-INFINITY);
         }
         {
-          // 8 independent max chains instead of one 128-long dependency chain
+          // 8 independent chains of three-input max over the 128 scores
           float m8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(r[c][j]));
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int j = 0; j < 32; j += 2)
+              m8[(c * 16 + j / 2) & 7] = max3(m8[(c * 16 + j / 2) & 7], __uint_as_float(r[c][j]),
+                                              __uint_as_float(r[c][j + 1]));
+          mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
         const float m_new = fmaxf(m_run, mx * sl2);
         bool rescale = false;
@@ -351,23 +356,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
         const float mu = m_run == -INFINITY ? 0.f : m_run;
-        float l8[8];
+        // P = 2^(s * scale * log2e - m): exponent arguments and row sums two lanes per
+        // instruction (packed fp32x2), 2^x on the special-function unit
+        const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
+        float2 l4[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+        for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float p0 = ex2_mix(fmaf(__uint_as_float(r[c][2 * j]), sl2, -mu), 2 * j);
-            const float p1 = ex2_mix(fmaf(__uint_as_float(r[c][2 * j + 1]), sl2, -mu), 2 * j + 1);
-            l8[(2 * j) & 7] += p0;
-            l8[(2 * j + 1) & 7] += p1;
-            pk[j] = pack_bf16(p0, p1);
+            const float2 x = fma2(make_float2(__uint_as_float(r[c][2 * j]),
+                                              __uint_as_float(r[c][2 * j + 1])), sl2v, nmu);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            l4[j & 3] = add2(l4[j & 3], pp);
+            pk[j] = pack_bf16(pp.x, pp.y);
           }
           tmem_st16(t_s + c * 16, pk);
         }
-        l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        l_run += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
         tmem_wait_st();
         if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
           // the output so far must be final in TMEM before it is rescaled
@@ -469,6 +477,7 @@ static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, con
   auto kern = tcfwd::fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
+  if ((e = check_register_split(kern, tcfwd::kThreads)) != cudaSuccess) return e;
   kern<<<items, tcfwd::kThreads, kSmem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
