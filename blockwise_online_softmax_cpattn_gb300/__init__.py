@@ -64,6 +64,8 @@ _sigs = {
     "cpattn_ring_bwd_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
     "cpattn_ring_bwd": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, ctypes.c_size_t, _vp]),
+    "cpattn_ring_bwd_noalloc": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp]),
     "cpattn_layout": (_st, [ctypes.c_int, ctypes.POINTER(CpattnDesc), _vp, _vp, ctypes.c_int, _vp]),
     "cpattn_check": (_st, [_vp]),
     "cpattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -132,6 +134,14 @@ def cpattn_ring_bwd(desc, q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes=N
     return _lib.cpattn_ring_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                 _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes,
                                 _stream(stream))
+
+
+def cpattn_ring_bwd_noalloc(desc, q, k, v, o, lse, dO, dq, dk, dv, stream=None) -> int:
+    """The backward without a caller workspace (for callers that cannot allocate
+    device memory): the library's own 16 MiB scratch per device is used instead."""
+    return _lib.cpattn_ring_bwd_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                        _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                                        _stream(stream))
 
 
 def cpattn_layout(permute, desc, src, dst, n_heads, stream=None) -> int:

@@ -152,6 +152,33 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
                               void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The backward pass for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is an interface addition of this library.  Callers
+ * such as engine plugins that may only enqueue work into buffers handed to them,
+ * or programs that reserve all device memory up front and forbid allocation
+ * while a step runs, cannot provide the workspace cpattn_ring_bwd asks for.
+ * This call computes exactly what cpattn_ring_bwd computes (same arguments
+ * minus the workspace) and uses instead a scratch array compiled into the
+ * library: 16 MiB of device memory that every GPU loading the library holds
+ * until the process exits.  It allocates nothing, on the device or through any
+ * allocating library routine.
+ *   Limit: cpattn_ring_bwd_workspace(desc) <= 16 MiB, i.e. B * H_q * T <=
+ *   2,097,152 query rows; larger problems return CPATTN_ERR_UNSUPPORTED before
+ *   anything is enqueued.
+ *   Set-up: the first call on a device looks up the scratch's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Sharing: every call on a device uses the same scratch, which keeps the last
+ *   call's contents (nothing needs clearing: each call writes what it reads).
+ *   Two calls that overlap on the GPU race on it; order them on one stream.
+ * Other errors as cpattn_ring_bwd.
+ */
+cpattn_status cpattn_ring_bwd_noalloc(const cpattn_desc* desc, const void* q, const void* k,
+                                      const void* v, const void* o, const float* lse,
+                                      const void* dO, void* dq, void* dk, void* dv,
+                                      void* stream);
+
+/*
  * Permutes one tensor of n_heads heads (H_q or H_kv) between orders:
  *  CPATTN_ZIGZAG_FWD / _INV : [B][n_heads][T][D] natural <-> layout order of
  *      desc->layout over the ring's cp/a2a ranks (tutorial, section "Zig-Zag Ring
