@@ -287,14 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cls = classify(qpos0, kpos0);
       if (cls == kEmpty) continue;
       if (!(ok = warp_wait(q_full(stage), par, abort, p.status))) break;  // LSE, Delta landed
+      const float* lse_t = lse_s + stage * 128 + half * 64;
+      const float* del_t = del_s + stage * 128 + half * 64;
+      // this half's 64 per-query LSE values, fetched while S^T is still being computed
+      float4 nl4[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) nl4[i] = reinterpret_cast<const float4*>(lse_t)[i];
       if (!(ok = warp_wait(s_full, cnt & 1, abort, p.status))) break;
       tc_fence_after();
       uint32_t sr[2][32];
       tmem_ld32(t_s, sr[0]);
       tmem_ld32(t_s + 32, sr[1]);
       tmem_wait_ld();
-      const float* lse_t = lse_s + stage * 128 + half * 64;
-      const float* del_t = del_s + stage * 128 + half * 64;
       // query column j (of this half) sees this key row iff kpos0 + row <= qpos0 + 64*half + j
       const int thr = kpos0 + row - qpos0 - half * 64;
       float pr[64];
@@ -306,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; j += 2) {
           const int j0 = c * 32 + j;
           // P = 2^(S scale log2e - LSE log2e), the exponent argument two lanes at a time
-          const float2 nl = reinterpret_cast<const float2*>(lse_t)[j0 >> 1];
+          const float4 n4 = nl4[j0 >> 2];
+          const float2 nl = (j0 & 2) ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
           const float2 x = fma2(make_float2(__uint_as_float(sr[c][j]), __uint_as_float(sr[c][j + 1])),
                                 sl2v, nl);
           float p0 = ex2(x.x), p1 = ex2(x.y);
@@ -323,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full);
+      float4 nd4[16];  // -Delta of this half's 64 queries, fetched before dP^T is ready
+#pragma unroll
+      for (int i = 0; i < 16; ++i) nd4[i] = reinterpret_cast<const float4*>(del_t)[i];
       if (!(ok = warp_wait(dp_full, cnt & 1, abort, p.status))) break;
       tc_fence_after();
       tmem_ld32(t_dp, sr[0]);
@@ -335,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; j += 2) {
           const int j0 = c * 32 + j;
           // dS = P (dP - Delta), two lanes per instruction (del_t holds -Delta)
-          const float2 nd = reinterpret_cast<const float2*>(del_t)[j0 >> 1];
+          const float4 d4 = nd4[j0 >> 2];
+          const float2 nd = (j0 & 2) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
           const float2 d = mul2(make_float2(pr[j0], pr[j0 + 1]),
                                 add2(make_float2(__uint_as_float(sr[c][j]),
                                                  __uint_as_float(sr[c][j + 1])), nd));
