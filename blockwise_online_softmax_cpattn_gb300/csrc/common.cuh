@@ -89,6 +89,28 @@ struct TileWalk {
   }
 };
 
+// Position in a ring of N shared-memory stages fed by TMA: the current stage,
+// the parity of its current mbarrier phase, and (for the producer's drain
+// before exit) which stages ever received a copy and the parity of the last one.
+template <int N>
+struct StageRing {
+  int stage = 0;
+  uint32_t par = 0;
+  uint32_t issued = 0, ipar = 0;
+  __device__ __forceinline__ void advance() {
+    if (++stage == N) {
+      stage = 0;
+      par ^= 1u;
+    }
+  }
+  __device__ __forceinline__ void mark_issued() {
+    issued |= 1u << stage;
+    ipar = (ipar & ~(1u << stage)) | (par << stage);
+  }
+  __device__ __forceinline__ bool was_issued(int st) const { return (issued >> st) & 1u; }
+  __device__ __forceinline__ uint32_t issued_parity(int st) const { return (ipar >> st) & 1u; }
+};
+
 __device__ __forceinline__ void latch_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

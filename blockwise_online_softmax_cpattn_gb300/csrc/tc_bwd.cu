@@ -97,8 +97,8 @@ struct DkdvSmem {
   static constexpr int kDelta = kLse + kStages * 512;
   static constexpr int kBar = kDelta + kStages * 512;
   // kv_full, q_full[S], do_full[S], qdo_empty[S], s_full, dp_full, p_full,
-  // ds_full, dv_done, dk_done, final
-  static constexpr int kNumBars = 1 + 3 * kStages + 7;
+  // ds_full, dv_done, dk_done, final (gradient issuer), final_a (score issuer)
+  static constexpr int kNumBars = 1 + 3 * kStages + 8;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;
 };
@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t dv_done = s_full + 32;
   const uint32_t dk_done = s_full + 40;
   const uint32_t final_bar = s_full + 48;
+  const uint32_t final_a = s_full + 56;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,24 +204,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // Score issuer: S^T = K Q^T and dP^T = V dO^T.  A tcgen05.mma takes a thread
+      // about 35-50 cycles to issue against 64 cycles to run at N = 128, and the
+      // tensor pipe queues only a few, so a single issuer that also waits on the
+      // softmax warps leaves the pipe idle; the gradient products come from a
+      // second issuer (warp 2) whose waits overlap these.
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(kv_full, 0, abort, p.status, kTimeoutNs);
       tc_fence_after();
-      // descriptor bases (16-byte units); K-major for S^T/dP^T, MN-major for dV/dK
+      // descriptor bases (16-byte units), K-major
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t kd = sdesc_sw128(sbase + L::kK, 16, 1024);
       const uint64_t vd = sdesc_sw128(sbase + L::kV, 16, 1024);
       const uint64_t qd_k0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
       const uint64_t dod_k0 = sdesc_sw128(sbase + L::kDO, 16, 1024);
-      const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQ, kTile * 128, 1024);
-      const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
       int stage = 0, par = 0, cnt = 0;
       TileWalk wk;
       for (walk_start(wk); !wk.done() && ok; wk.next()) {
         if (classify(wk.pos(), kpos0) == kEmpty) continue;
         const uint64_t soff = (uint64_t)(stage * kTD);
-        // S^T = K Q^T  (the S region is free once the previous dV has read P^T)
+        // S^T  (the S region is free once the previous dV has read P^T)
         if (!(ok = mbar_wait(q_full(stage), par, abort, p.status, kTimeoutNs))) break;
         if (cnt > 0 && !(ok = mbar_wait(dv_done, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
           break;
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem, kd + off, qd_k0 + soff + off, kIdSS, kk > 0);
         }
         mma_commit(s_full);
-        // dP^T = V dO^T  (the dP region is free once the previous dK has read dS^T)
+        // dP^T  (the dP region is free once the previous dK has read dS^T)
         if (!(ok = mbar_wait(do_full(stage), par, abort, p.status, kTimeoutNs))) break;
         if (cnt > 0 && !(ok = mbar_wait(dk_done, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
           break;
@@ -242,8 +245,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + 128, vd + off, dod_k0 + soff + off, kIdSS, kk > 0);
         }
         mma_commit(dp_full);
-        // dV += P^T dO
+        ++cnt;
+        if (++stage == S) stage = 0, par ^= 1;
+      }
+      mma_commit(final_a);
+      drain_wait(final_a, 0);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // Gradient issuer: dV += P^T dO and dK += dS^T Q (TS, P^T / dS^T in TMEM,
+      // Q / dO MN-major from shared memory)
+      constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kTD = L::kTB >> 4;
+      const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQ, kTile * 128, 1024);
+      const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
+      bool ok = true;
+      int stage = 0, par = 0, cnt = 0;
+      TileWalk wk;
+      for (walk_start(wk); !wk.done() && ok; wk.next()) {
+        if (classify(wk.pos(), kpos0) == kEmpty) continue;
+        const uint64_t soff = (uint64_t)(stage * kTD);
+        // dV += P^T dO  (dO of this stage has landed: its copy completed do_full)
         if (!(ok = mbar_wait(p_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
+        if (!(ok = mbar_wait(do_full(stage), par, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -252,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  (cnt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(dv_done);
-        // dK += dS^T Q
+        // dK += dS^T Q  (Q landed before S^T of this tile was issued)
         if (!(ok = mbar_wait(ds_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
 #pragma unroll
@@ -262,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  (cnt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(dk_done);
+        // both issuers' reads of this Q/dO stage are over: S^T and dP^T completed
+        // before the compute warps released p_full / ds_full
         mma_commit(qdo_empty(stage));
         ++cnt;
         if (++stage == S) stage = 0, par ^= 1;
@@ -397,16 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 template <int D>
 struct DqSmem {
-  static constexpr int kStages = 2;
+  // K and V have separate rings: V is last read by dP (early in a tile), K by dQ
+  // (late), so each is refilled as soon as its own consumer is done, and K gets
+  // the extra stage that the freed shared memory allows.
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
   static constexpr int kTB = kTile * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kDO = kTB;
   static constexpr int kK = 2 * kTB;
-  static constexpr int kV = kK + kStages * kTB;
-  static constexpr int kBar = kV + kStages * kTB;
-  // qdo_full, k_full[S], v_full[S], kv_empty[S], s_full, s_free, dp_full, ds_full,
-  // dq_done[2], final
-  static constexpr int kNumBars = 1 + 3 * kStages + 7;
+  static constexpr int kV = kK + kKStages * kTB;
+  static constexpr int kBar = kV + kVStages * kTB;
+  // qdo_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full, s_free,
+  // dp_full, ds_full, dq_done[2], final (gradient issuer), final_a (score issuer)
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;
 };
@@ -417,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const Params p) {
   using L = DqSmem<D>;
-  constexpr int S = L::kStages;
+  constexpr int KS = L::kKStages, VS = L::kVStages;
   constexpr int kDqCol = 384;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -426,14 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + L::kBar;
   const uint32_t qdo_full = bars;
   auto k_full = [&](int s) { return bars + 8 * (1 + s); };
-  auto v_full = [&](int s) { return bars + 8 * (1 + S + s); };
-  auto kv_empty = [&](int s) { return bars + 8 * (1 + 2 * S + s); };
-  const uint32_t s_full = bars + 8 * (1 + 3 * S);
+  auto k_empty = [&](int s) { return bars + 8 * (1 + KS + s); };
+  auto v_full = [&](int s) { return bars + 8 * (1 + 2 * KS + s); };
+  auto v_empty = [&](int s) { return bars + 8 * (1 + 2 * KS + VS + s); };
+  const uint32_t s_full = bars + 8 * (1 + 2 * KS + 2 * VS);
   const uint32_t s_free = s_full + 8;
   const uint32_t dp_full = s_full + 16;
   const uint32_t ds_full = s_full + 24;
   auto dq_done = [&](int x) { return s_full + 32 + 8 * x; };
   const uint32_t final_bar = s_full + 48;
+  const uint32_t final_a = s_full + 56;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -488,110 +520,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)qrow, qdo_full);
         tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)qrow, qdo_full);
       }
-      int stage = 0, par = 0;
-      uint32_t issued = 0, ipar = 0;  // bit s: stage s loaded / its phase parity
+      StageRing<KS> kr;
+      StageRing<VS> vr;
       TileWalk wk;
       for (walk_start(wk); !wk.done(); walk_next(wk)) {
-        if (!mbar_wait(kv_empty(stage), par ^ 1, abort, p.status, kTimeoutNs)) break;
         const int row = kv_row_base + wk.slot();
-        mbar_expect_tx(k_full(stage), L::kTB);
+        if (!mbar_wait(k_empty(kr.stage), kr.par ^ 1, abort, p.status, kTimeoutNs)) break;
+        mbar_expect_tx(k_full(kr.stage), L::kTB);
         for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kK + stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64, row,
-                      k_full(stage));
-        mbar_expect_tx(v_full(stage), L::kTB);
+          tma_load_2d(sbase + L::kK + kr.stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64, row,
+                      k_full(kr.stage));
+        kr.mark_issued();
+        if (!mbar_wait(v_empty(vr.stage), vr.par ^ 1, abort, p.status, kTimeoutNs)) break;
+        mbar_expect_tx(v_full(vr.stage), L::kTB);
         for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kV + stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64, row,
-                      v_full(stage));
-        issued |= 1u << stage;
-        ipar = (ipar & ~(1u << stage)) | ((uint32_t)par << stage);
-        if (++stage == S) stage = 0, par ^= 1;
+          tma_load_2d(sbase + L::kV + vr.stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64, row,
+                      v_full(vr.stage));
+        vr.mark_issued();
+        kr.advance();
+        vr.advance();
       }
       drain_wait(qdo_full, 0);
-      for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u) {
-          drain_wait(k_full(s), (ipar >> s) & 1u);
-          drain_wait(v_full(s), (ipar >> s) & 1u);
-        }
+      for (int s = 0; s < KS; ++s)
+        if (kr.was_issued(s)) drain_wait(k_full(s), kr.issued_parity(s));
+      for (int s = 0; s < VS; ++s)
+        if (vr.was_issued(s)) drain_wait(v_full(s), vr.issued_parity(s));
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // Score issuer: S = Q K^T and dP = dO V^T of every visited tile, in order.
+      // A tcgen05.mma takes a thread about 35-50 cycles to issue against 64 cycles
+      // to run at N = 128 and the pipe queues only a few, so the dQ products come
+      // from a second issuer (warp 2) whose waits overlap these.
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(qdo_full, 0, abort, p.status, kTimeoutNs);
       tc_fence_after();
-      // descriptor bases (16-byte units)
+      // descriptor bases (16-byte units), K-major
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t qd = sdesc_sw128(sbase + L::kQ, 16, 1024);
       const uint64_t dod = sdesc_sw128(sbase + L::kDO, 16, 1024);
       const uint64_t kd_k0 = sdesc_sw128(sbase + L::kK, 16, 1024);
       const uint64_t vd_k0 = sdesc_sw128(sbase + L::kV, 16, 1024);
-      const uint64_t kd_mn0 = sdesc_sw128(sbase + L::kK, kTile * 128, 1024);
-      // visited tiles in order; S/dP of tile j+1 are issued before dQ of tile j
-      int stage = 0, par = 0;
-      auto issue_s = [&](int st, int pr) -> bool {
-        if (!mbar_wait(k_full(st), pr, abort, p.status, kTimeoutNs)) return false;
+      StageRing<KS> kr;
+      StageRing<VS> vr;
+      int j = 0;
+      TileWalk wk;
+      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
+        // S(j): the S region is free once the compute warps have read S(j-1)
+        if (j > 0 && !(ok = mbar_wait(s_free, (j - 1) & 1, abort, p.status, kTimeoutNs))) break;
+        if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
-        const uint64_t kd = kd_k0 + (uint64_t)(st * kTD);
+        const uint64_t kd = kd_k0 + (uint64_t)(kr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
           mma_ss(tmem, qd + off, kd + off, kIdSS, kk > 0);
         }
         mma_commit(s_full);
-        return true;
-      };
-      auto issue_dp = [&](int st, int pr, int buf) -> bool {
-        if (!mbar_wait(v_full(st), pr, abort, p.status, kTimeoutNs)) return false;
+        // dP(j) into buffer j&1: free once dQ(j-2) has read the dS stored there
+        if (j >= 2 && !(ok = mbar_wait(dq_done(j & 1), ((j - 2) >> 1) & 1, abort, p.status,
+                                       kTimeoutNs)))
+          break;
+        if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
-        const uint64_t vd = vd_k0 + (uint64_t)(st * kTD);
+        const uint64_t vd = vd_k0 + (uint64_t)(vr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          mma_ss(tmem + 128 + 128 * buf, dod + off, vd + off, kIdSS, kk > 0);
+          mma_ss(tmem + 128 + 128 * (j & 1), dod + off, vd + off, kIdSS, kk > 0);
         }
         mma_commit(dp_full);
-        return true;
-      };
-      int j = 0;
-      TileWalk cur;
-      walk_start(cur);
-      if (ok && !cur.done()) ok = issue_s(stage, par) && issue_dp(stage, par, 0);
-      while (ok && !cur.done()) {
-        TileWalk nxt = cur;
-        walk_next(nxt);
-        const bool has_next = !nxt.done();
-        const int cur_stage = stage, cur_buf = j & 1;
-        int nstage = stage + 1, npar = par;
-        if (nstage == S) nstage = 0, npar ^= 1;
-        // S of the next tile as soon as this tile's S has been read out, and dP of the
-        // next tile into the other buffer once dQ of tile j-1 has read it, both ahead
-        // of dQ of this tile so the compute warps never wait on this tile's dS
-        if (has_next) {
-          if (!(ok = mbar_wait(s_free, j & 1, abort, p.status, kTimeoutNs))) break;
-          if (!(ok = issue_s(nstage, npar))) break;
-          if (j >= 1 &&
-              !(ok = mbar_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status,
-                               kTimeoutNs)))
-            break;
-          tc_fence_after();
-          if (!(ok = issue_dp(nstage, npar, (j + 1) & 1))) break;
-        }
-        // dQ += dS K
-        if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status, kTimeoutNs))) break;
-        tc_fence_after();
-        const uint64_t kd_mn = kd_mn0 + (uint64_t)(cur_stage * kTD);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acol = 128 + 128 * cur_buf + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(dq_done(cur_buf));
-        mma_commit(kv_empty(cur_stage));
-        stage = nstage;
-        par = npar;
-        cur = nxt;
+        mma_commit(v_empty(vr.stage));  // V of this tile is not read again
+        kr.advance();
+        vr.advance();
         ++j;
       }
+      mma_commit(final_a);
+      drain_wait(final_a, 0);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // Gradient issuer: dQ += dS K (TS: dS in TMEM, K MN-major from shared memory)
+      constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kTD = L::kTB >> 4;
+      const uint64_t kd_mn0 = sdesc_sw128(sbase + L::kK, kTile * 128, 1024);
+      StageRing<KS> kr;
+      bool ok = true;
+      int j = 0;
+      TileWalk wk;
+      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
+        if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status, kTimeoutNs))) break;
+        // dq_done of tile j-1 is committed only now, after dS(j) is seen: the score
+        // issuer's next dP (into that buffer) waits for it, so ds_full cannot run
+        // two phases ahead of this wait
+        if (j > 0) mma_commit(dq_done((j - 1) & 1));
+        tc_fence_after();
+        // K(j) landed before S(j), which the compute warps read before storing dS(j)
+        const uint64_t kd_mn = kd_mn0 + (uint64_t)(kr.stage * kTD);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acol = 128 + 128 * (j & 1) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        // both S(j) and dQ(j) have read K(j) once dQ(j) completes
+        mma_commit(k_empty(kr.stage));
+        kr.advance();
+        ++j;
+      }
+      if (j > 0) mma_commit(dq_done((j - 1) & 1));
       mma_commit(final_bar);
       drain_wait(final_bar, 0);
     }
