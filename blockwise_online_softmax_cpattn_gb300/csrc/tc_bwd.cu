@@ -23,6 +23,8 @@
 //
 // Delta = rowsum(dO * O) comes from the pre-pass kernel (merge.cu).  Compute
 // warps: 8, warp w handles TMEM lane quadrant w%4 and column half (w-4)/4.
+// Warp 0 loads through TMA; warp 1 issues the score products (S, dP) and
+// warp 2 the gradient products (dV/dK or dQ), one thread each.
 // Every mbarrier wait is bounded (see tc_fwd.cu for the abort protocol).
 #include <math.h>
 
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto walk_start = [&](TileWalk& w) { w.start(p.m, s_own, p.m.cp, +1, p.n_rep); };
 
   if (warp < 4) {
-  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuer (warp 1)
+  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2)
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kv_row_base = (b * p.Hkv + g) * p.T;
 
   if (warp < 4) {
-  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuer (warp 1)
+  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2)
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);

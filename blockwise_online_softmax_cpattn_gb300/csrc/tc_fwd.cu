@@ -14,10 +14,12 @@
 // consecutive 128-token tiles of one head.
 //
 // Warp roles (384 threads):
-//   warp 0        TMA producer: Q tiles once, then K/V tiles through a ring of
-//                 shared-memory stages (128-byte swizzle).
-//   warp 1        MMA issuer (one thread): S_X = Q_X K^T into TMEM (SS form),
-//                 O_X += P_X V with P read from TMEM (TS form).
+//   warp 0        TMA producer: Q tiles once, then K tiles through a ring of
+//                 shared-memory stages (128-byte swizzle); warp 3: V tiles
+//                 through a ring of their own.
+//   warps 1, 2    MMA issuers, one thread each, warp 1 for tile A and warp 2
+//                 for tile B: S_X = Q_X K^T into TMEM (SS form), O_X += P_X V
+//                 with P read from TMEM (TS form).
 //   warps 4..7    softmax of tile A; warps 8..11 softmax of tile B.  Thread =
 //                 row: tcgen05.ld of its S row, causal mask, row max, P =
 //                 2^(s*scale*log2e - m) rounded to bf16 into TMEM, row sum in
@@ -61,15 +63,19 @@ struct Params {
 
 template <int D>
 struct Smem {
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  // K and V have rings of their own: K is last read by the S products early in a
+  // step, V by the PV products at its end, so K is refilled a step sooner and
+  // takes the extra stage.
+  static constexpr int kKStages = D == 128 ? 3 : 5;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = 2 * kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
-  // barriers: q_full[2], k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2],
-  // pv_done[2], final
-  static constexpr int kNumBars = 2 + 3 * kStages + 6 + 1;
+  static constexpr int kV = kK + kKStages * kTileBytes;
+  static constexpr int kBar = kV + kVStages * kTileBytes;
+  // barriers: q_full[2], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
+  // p_full[2], pv_done[2], final[2] (one per issuer)
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 6 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;  // + alignment slack
 };
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using L = Smem<D>;
-  constexpr int S = L::kStages;
+  constexpr int KS = L::kKStages, VS = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -148,12 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + L::kBar;
   auto q_full = [&](int x) { return bars + 8 * x; };
   auto k_full = [&](int s) { return bars + 8 * (2 + s); };
-  auto v_full = [&](int s) { return bars + 8 * (2 + S + s); };
-  auto kv_empty = [&](int s) { return bars + 8 * (2 + 2 * S + s); };
-  auto s_full = [&](int x) { return bars + 8 * (2 + 3 * S + x); };
-  auto p_full = [&](int x) { return bars + 8 * (4 + 3 * S + x); };
-  auto pv_done = [&](int x) { return bars + 8 * (6 + 3 * S + x); };
-  const uint32_t final_bar = bars + 8 * (8 + 3 * S);
+  auto k_empty = [&](int s) { return bars + 8 * (2 + KS + s); };
+  auto v_full = [&](int s) { return bars + 8 * (2 + 2 * KS + s); };
+  auto v_empty = [&](int s) { return bars + 8 * (2 + 2 * KS + VS + s); };
+  const uint32_t tile_bars = bars + 8 * (2 + 2 * KS + 2 * VS);
+  auto s_full = [&](int x) { return tile_bars + 8 * x; };
+  auto p_full = [&](int x) { return tile_bars + 8 * (2 + x); };
+  auto pv_done = [&](int x) { return tile_bars + 8 * (4 + x); };
+  auto final_bar = [&](int x) { return tile_bars + 8 * (6 + x); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -163,8 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
-      const bool softmax_arrivals = bars + 8 * i == p_full(0) || bars + 8 * i == p_full(1);
-      mbar_init(bars + 8 * i, softmax_arrivals ? 128 : 1);
+      const uint32_t b = bars + 8 * i;
+      const bool softmax_arrivals = b == p_full(0) || b == p_full(1);
+      // a K or V stage is free once both issuers' MMAs that read it have completed
+      const bool both_issuers = (b >= k_empty(0) && b < k_empty(0) + 8 * KS) ||
+                                (b >= v_empty(0) && b < v_empty(0) + 8 * VS);
+      mbar_init(b, softmax_arrivals ? 128 : both_issuers ? 2 : 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -185,24 +197,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kv_row_base = (it.b * p.Hkv + it.g) * p.T;
 
   if (warp < 4) {
-  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuer (warp 1)
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  regs_ctl();  // warpgroup 0: TMA producers (warps 0, 3) and MMA issuers (warps 1, 2)
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ producers
+    // warp 0: the Q tiles, then the K tiles; warp 3: the V tiles
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+      const bool is_k = warp == 0;
+      const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+      tma_prefetch_desc(tm);
       int q_issued[2] = {0, 0};
-      for (int x = 0; x < 2; ++x) {
-        if (!it.active[x]) continue;
-        if (x == 0 && p.debug_fault) continue;  // fault hook: this load never happens
-        mbar_expect_tx(q_full(x), L::kTileBytes);
-        const int row = (it.b * p.Hq + it.h[x]) * p.T + it.slot0[x];
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kQ + x * L::kTileBytes + kb * (kTile * 128), &tm_q, kb * 64, row,
-                      q_full(x));
-        q_issued[x] = 1;
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        for (int x = 0; x < 2; ++x) {
+          if (!it.active[x]) continue;
+          if (x == 0 && p.debug_fault) continue;  // fault hook: this load never happens
+          mbar_expect_tx(q_full(x), L::kTileBytes);
+          const int row = (it.b * p.Hq + it.h[x]) * p.T + it.slot0[x];
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(sbase + L::kQ + x * L::kTileBytes + kb * (kTile * 128), &tm_q, kb * 64,
+                        row, q_full(x));
+          q_issued[x] = 1;
+        }
       }
+      const int nst = is_k ? KS : VS;
+      const uint32_t base = sbase + (is_k ? L::kK : L::kV);
       int stage = 0, par = 0;
       uint32_t issued = 0, issued_par = 0;  // bit s: stage s loaded / its phase parity
       TileWalk wk;
@@ -211,60 +229,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ca = classify(it.pos0[0], kpos);
         const int cb = it.active[1] ? classify(it.pos0[1], kpos) : kEmpty;
         if (ca == kEmpty && cb == kEmpty) continue;
-        if (!mbar_wait(kv_empty(stage), par ^ 1, abort, p.status, tmo)) break;
+        const uint32_t empty = is_k ? k_empty(stage) : v_empty(stage);
+        const uint32_t full = is_k ? k_full(stage) : v_full(stage);
+        if (!mbar_wait(empty, par ^ 1, abort, p.status, tmo)) break;
         const int row = kv_row_base + wk.slot();
-        mbar_expect_tx(k_full(stage), L::kTileBytes);
+        mbar_expect_tx(full, L::kTileBytes);
         for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kK + stage * L::kTileBytes + kb * (kTile * 128), &tm_k, kb * 64,
-                      row, k_full(stage));
-        mbar_expect_tx(v_full(stage), L::kTileBytes);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kV + stage * L::kTileBytes + kb * (kTile * 128), &tm_v, kb * 64,
-                      row, v_full(stage));
+          tma_load_2d(base + stage * L::kTileBytes + kb * (kTile * 128), tm, kb * 64, row, full);
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | ((uint32_t)par << stage);
-        if (++stage == S) stage = 0, par ^= 1;
+        if (++stage == nst) stage = 0, par ^= 1;
       }
       // never leave with a copy still writing into this CTA's shared memory
       for (int x = 0; x < 2; ++x)
         if (q_issued[x]) drain_wait(q_full(x), 0);
-      for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u) {
-          drain_wait(k_full(s), (issued_par >> s) & 1u);
-          drain_wait(v_full(s), (issued_par >> s) & 1u);
-        }
+      for (int st = 0; st < nst; ++st)
+        if ((issued >> st) & 1u)
+          drain_wait(is_k ? k_full(st) : v_full(st), (issued_par >> st) & 1u);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuer per query tile (warp 1: A, warp 2: B).  A tcgen05.mma takes a
+    // thread about 35-50 cycles to issue against 64 cycles to run at N = 128 and
+    // the tensor pipe queues only a few, so a single thread serving both softmax
+    // warpgroups in turn puts one tile's PV and the next step's waits on the other
+    // tile's S -> softmax -> PV chain; with a thread per tile each chain runs on
+    // its own.  Both issuers wait for every K and V load, even one their tile does
+    // not use, so their k_empty / v_empty arrivals stay one per load.
     if (lane == 0) {
+      const int x = warp - 1;
       constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
       bool ok = true;
-      for (int x = 0; x < 2 && ok; ++x)
-        if (it.active[x]) ok = mbar_wait(q_full(x), 0, abort, p.status, tmo);
+      if (it.active[x]) ok = mbar_wait(q_full(x), 0, abort, p.status, tmo);
       tc_fence_after();
       // descriptor bases; per k-step offsets are compile-time constants (16-byte units)
       constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
-      const uint64_t qd0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t qd = sdesc_sw128(sbase + L::kQ, 16, 1024) + (uint64_t)(x * kTileDesc);
       const uint64_t kd0 = sdesc_sw128(sbase + L::kK, 16, 1024);
       const uint64_t vd0 = sdesc_sw128(sbase + L::kV, kTile * 128, 1024);
-      int stage = 0, par = 0, cnt[2] = {0, 0};
+      StageRing<KS> kr;
+      StageRing<VS> vr;
+      int cnt = 0, cnt_other = 0;  // S products issued so far by this / the other issuer
       TileWalk wk;
       for (wk.start(p.m, kv_first, kv_chunks, -1, 1); !wk.done() && ok; wk.next()) {
         const int kpos = wk.pos();
-        int cls[2];
-        cls[0] = classify(it.pos0[0], kpos);
-        cls[1] = it.active[1] ? classify(it.pos0[1], kpos) : kEmpty;
-        if (cls[0] == kEmpty && cls[1] == kEmpty) continue;
-        if (!(ok = mbar_wait(k_full(stage), par, abort, p.status, tmo))) break;
-        tc_fence_after();
-        const uint64_t kd = kd0 + (uint64_t)(stage * kTileDesc);
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (cls[x] == kEmpty) continue;
-          if (cnt[x] > 0 && !(ok = mbar_wait(pv_done(x), (cnt[x] - 1) & 1, abort, p.status, tmo)))
+        const int ca = classify(it.pos0[0], kpos);
+        const int cb = it.active[1] ? classify(it.pos0[1], kpos) : kEmpty;
+        if (ca == kEmpty && cb == kEmpty) continue;  // the producers skip these too
+        const bool mine = (x == 0 ? ca : cb) != kEmpty;
+        const bool other = (x == 0 ? cb : ca) != kEmpty;
+        if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
+        if (mine) {
+          // S_X = Q_X K^T; the S region is free once the previous PV has read P_X
+          if (cnt > 0 && !(ok = mbar_wait(pv_done(x), (cnt - 1) & 1, abort, p.status, tmo)))
+            break;
+          // Ping-pong: the S products alternate A(j), B(j), A(j+1), ... -- S_B of a
+          // K/V tile waits for S_A of the same tile and S_A for S_B of the tile
+          // before -- so one tile's softmax runs while the tensor pipe serves the
+          // other tile instead of both softmax warpgroups contending at once.  Each
+          // issuer is thereby at most one S phase ahead of the other, which keeps
+          // these parity waits unambiguous.
+          if (x == 1 && other &&
+              !(ok = mbar_wait(s_full(0), cnt_other & 1, abort, p.status, tmo)))
+            break;
+          if (x == 0 && cnt_other > 0 &&
+              !(ok = mbar_wait(s_full(1), (cnt_other - 1) & 1, abort, p.status, tmo)))
             break;
           tc_fence_after();
-          const uint64_t qd = qd0 + (uint64_t)(x * kTileDesc);
+          const uint64_t kd = kd0 + (uint64_t)(kr.stage * kTileDesc);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KiB blocks, 32 B steps
@@ -272,28 +305,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(s_full(x));
         }
-        if (!ok) break;
-        if (!(ok = mbar_wait(v_full(stage), par, abort, p.status, tmo))) break;
-        tc_fence_after();
-        const uint64_t vd = vd0 + (uint64_t)(stage * kTileDesc);
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (cls[x] == kEmpty) continue;
-          if (!(ok = mbar_wait(p_full(x), cnt[x] & 1, abort, p.status, tmo))) break;
+        mma_commit(k_empty(kr.stage));  // arrives at once if nothing was issued
+        if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
+        if (mine) {
+          // O_X += P_X V
+          if (!(ok = mbar_wait(p_full(x), cnt & 1, abort, p.status, tmo))) break;
           tc_fence_after();
+          const uint64_t vd = vd0 + (uint64_t)(vr.stage * kTileDesc);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)  // 16 key rows = 2048 B per k-step
             mma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, vd + kk * 128, kIdescPV,
-                   (cnt[x] > 0 || kk > 0) ? 1u : 0u);
+                   (cnt > 0 || kk > 0) ? 1u : 0u);
           mma_commit(pv_done(x));
-          ++cnt[x];
+          ++cnt;
         }
-        if (!ok) break;
-        mma_commit(kv_empty(stage));
-        if (++stage == S) stage = 0, par ^= 1;
+        mma_commit(v_empty(vr.stage));
+        if (other) ++cnt_other;
+        kr.advance();
+        vr.advance();
       }
       // every MMA this thread issued has finished before TMEM can be freed
-      mma_commit(final_bar);
-      drain_wait(final_bar, 0);
+      mma_commit(final_bar(x));
+      drain_wait(final_bar(x), 0);
     }
   }
   } else {
