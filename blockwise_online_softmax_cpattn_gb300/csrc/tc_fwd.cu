@@ -1,33 +1,46 @@
 // Ring-attention forward on the 5th-generation tensor cores (sm_103a).
 //
-// What one CTA computes: two 128-row query tiles (A and B) of one sequence
-// against every key/value tile their rows can see, visited in ring order --
-// step i of rank r holds the K/V chunk of rank (r - i) mod cp (tutorial
-// "上下文并行", section "朴素 Ring Attention") -- with the running max / sum /
-// output carried across steps, i.e. the per-step partials merged by the
-// single-pass online softmax (pull request "Feat: Context Parallel" #181, mode
-// "p2p").  Tiles wholly hidden by the causal mask (key position > query
-// position for every pair) are skipped; diagonal tiles are masked per element
-// from global positions.  Pairing: with an even number of query heads per K/V
-// head the two tiles are two query heads of the same group at the same rows
-// (they share every K/V tile and every mask decision); otherwise they are two
-// consecutive 128-token tiles of one head.
+// What one CTA computes: one 128-row query tile of one (batch, head) against
+// every key/value tile its rows can see, visited in ring order -- step i of
+// rank r holds the K/V chunk of rank (r - i) mod cp (tutorial "上下文并行",
+// section "朴素 Ring Attention") -- with the running max / sum / output carried
+// across steps, i.e. the per-step partials merged by the single-pass online
+// softmax (pull request "Feat: Context Parallel" #181, mode "p2p").  Tiles
+// wholly hidden by the causal mask (key position > query position for every
+// pair) are skipped; diagonal tiles are masked per element from global
+// positions.
+//
+// Two softmax threads per query row: thread (row, h) owns key columns
+// [64h, 64h+64) of every tile and runs an online softmax of its own over them
+// into an output accumulator of its own, O_h.  The two halves are partial
+// results over disjoint key sets; the epilogue merges them once with the
+// (O, LSE) merge rule (tutorial, section "朴素 Ring Attention"), so the two
+// threads of a row never exchange anything per tile.
 //
 // Warp roles (384 threads):
-//   warp 0        TMA producer: Q tiles once, then K tiles through a ring of
-//                 shared-memory stages (128-byte swizzle); warp 3: V tiles
+//   warp 0        TMA producer: the Q tile, then the K tiles through a ring of
+//                 shared-memory stages (128-byte swizzle); warp 3: the V tiles
 //                 through a ring of their own.
-//   warps 1, 2    MMA issuers, one thread each, warp 1 for tile A and warp 2
-//                 for tile B: S_X = Q_X K^T into TMEM (SS form), O_X += P_X V
-//                 with P read from TMEM (TS form).
-//   warps 4..7    softmax of tile A; warps 8..11 softmax of tile B.  Thread =
-//                 row: tcgen05.ld of its S row, causal mask, row max, P =
-//                 2^(s*scale*log2e - m) rounded to bf16 into TMEM, row sum in
-//                 fp32.  The output is rescaled only when the running max grows
-//                 by more than 2^8 (exact after the final division by the sum).
-//   epilogue      O / l rounded once to the output dtype, LSE = ln(l) + m.
-// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256, 256+D),
-// O_B [256+D, 256+2D); P_X overwrites the first 64 columns of S_X.
+//   warp 1        S issuer (one thread): S = Q K^T (SS form) into one of two
+//                 TMEM buffers, so S of the next tile is formed while the
+//                 softmax of this one runs.
+//   warp 2        PV issuer (one thread): O_h += P_h V_h (TS form, P_h read from
+//                 TMEM) for each half as soon as that half's P is stored.
+//                 Two issuers because a thread needs about 35-50 cycles to issue
+//                 one tcgen05.mma that runs 64 cycles at N = 128, the pipe queues
+//                 only a few, and a thread's next memory access after a
+//                 tcgen05.commit waits for the committed MMAs: one thread that
+//                 also waited on the softmax would leave the pipe idle.
+//   warps 4..11   softmax: warp w serves TMEM lane quadrant w%4 (32 rows) and
+//                 column half (w-4)/4.  tcgen05.ld of its 64 scores, causal
+//                 mask, max, P = 2^(s*scale*log2e - m) rounded to bf16 into
+//                 TMEM, sum in fp32.  O_h is rescaled only when the running max
+//                 grows by more than 2^8 (exact after the final division).
+//   epilogue      M = max(m_0, m_1), w_h = 2^(m_h - M), L = w_0 l_0 + w_1 l_1,
+//                 O = (w_0 O_0 + w_1 O_1) / L rounded once to the output dtype,
+//                 LSE = ln 2 (M + log2 L).
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+D),
+// O_1 [256+D, 256+2D); P of half h overwrites columns [64h, 64h+32) of its S.
 // Every mbarrier wait is bounded; on time-out the CTA raises its abort flag,
 // latches CPATTN_ERR_TIMEOUT in the device status word, drains its own TMA
 // loads and MMAs, frees TMEM and exits.
@@ -43,6 +56,7 @@ constexpr int kThreads = 384;
 constexpr uint64_t kTimeoutNs = 2000000000ull;     // 2 s
 constexpr uint64_t kDebugTimeoutNs = 50000000ull;  // 50 ms under the fault hook
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;
+constexpr float kLn2 = 0.69314718055994530942f;
 
 enum : int { kEmpty = 0, kFull = 1, kDiag = 2 };
 
@@ -50,11 +64,8 @@ struct Params {
   int B, Hq, Hkv, T, n_rep;
   SeqMap m;
   float scale_log2;
-  int head_pairs;      // 1: tiles A/B are query heads 2u, 2u+1 at the same rows
-  int tiles_per_item;  // row pairing: 2 consecutive 128-token tiles, or 1
-  int n_hu;            // head units per batch (H_q/2 with head pairs, else H_q)
-  int q_tiles;         // 128-row query tiles per sequence in the launch
-  int q_rank, kv_rank; // partial mode when q_rank >= 0
+  int q_tiles;          // 128-row query tiles per (batch, head) in the launch
+  int q_rank, kv_rank;  // partial mode when q_rank >= 0
   void* o;
   float* lse;
   int* status;
@@ -63,62 +74,42 @@ struct Params {
 
 template <int D>
 struct Smem {
-  // K and V have rings of their own: K is last read by the S products early in a
-  // step, V by the PV products at its end, so K is refilled a step sooner and
-  // takes the extra stage.
-  static constexpr int kKStages = D == 128 ? 3 : 5;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
+  // one Q tile; K and V in rings of their own (K is last read by S, V by PV)
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 3 : 4;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kQ = 0;
-  static constexpr int kK = 2 * kTileBytes;
+  static constexpr int kK = kTileBytes;
   static constexpr int kV = kK + kKStages * kTileBytes;
   static constexpr int kBar = kV + kVStages * kTileBytes;
-  // barriers: q_full[2], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
-  // p_full[2], pv_done[2], final[2] (one per issuer)
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 6 + 2;
+  // barriers: q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
+  // p_full[2 buffers][2 halves], pv_done[2], final_s, final_pv
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 4 + 2 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;  // + alignment slack
 };
 
 struct Item {
-  int b, g, rank;
-  int h[2], slot0[2], pos0[2];
-  int active[2];
+  int b, h, g, rank, slot0, pos0;
 };
 
 __device__ __forceinline__ Item decode(const Params& p, int w) {
   Item it;
-  const int units = p.B * p.n_hu;
+  const int units = p.B * p.Hq;
   const int ti = w / units;
   const int rem = w - ti * units;
-  it.b = rem / p.n_hu;
-  const int hu = rem - it.b * p.n_hu;
-  const int tpi = p.tiles_per_item;
+  it.b = rem / p.Hq;
+  it.h = rem - it.b * p.Hq;
+  it.g = it.h / p.n_rep;
   if (p.q_rank >= 0) {
-    it.slot0[0] = p.q_rank * p.m.c + ti * tpi * kTile;
-    it.pos0[0] = p.m.pos(it.slot0[0]);
+    it.slot0 = p.q_rank * p.m.c + ti * kTile;
+    it.pos0 = p.m.pos(it.slot0);
   } else {
     // heaviest (latest) query positions first: causal work grows with position
-    const int n_pos_items = p.q_tiles / tpi;
-    it.pos0[0] = (n_pos_items - 1 - ti) * tpi * kTile;
-    it.slot0[0] = p.m.slot(it.pos0[0]);
+    it.pos0 = (p.q_tiles - 1 - ti) * kTile;
+    it.slot0 = p.m.slot(it.pos0);
   }
-  if (p.head_pairs) {
-    it.h[0] = 2 * hu;
-    it.h[1] = 2 * hu + 1;
-    it.slot0[1] = it.slot0[0];
-    it.pos0[1] = it.pos0[0];
-    it.active[1] = 1;
-  } else {
-    it.h[0] = hu;
-    it.h[1] = hu;
-    it.slot0[1] = it.slot0[0] + kTile;
-    it.pos0[1] = it.pos0[0] + kTile;
-    it.active[1] = tpi == 2;
-  }
-  it.active[0] = 1;
-  it.g = it.h[0] / p.n_rep;
-  it.rank = it.slot0[0] / p.m.c;
+  it.rank = it.slot0 / p.m.c;
   return it;
 }
 
@@ -141,6 +132,11 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t par) {
   return mbar_wait(bar, par, &never, nullptr, kDrainTimeoutNs);
 }
 
+// Named barrier of the two softmax warps that serve one TMEM lane quadrant.
+__device__ __forceinline__ void pair_sync(int quad) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+}
+
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -152,16 +148,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::kBar;
-  auto q_full = [&](int x) { return bars + 8 * x; };
-  auto k_full = [&](int s) { return bars + 8 * (2 + s); };
-  auto k_empty = [&](int s) { return bars + 8 * (2 + KS + s); };
-  auto v_full = [&](int s) { return bars + 8 * (2 + 2 * KS + s); };
-  auto v_empty = [&](int s) { return bars + 8 * (2 + 2 * KS + VS + s); };
-  const uint32_t tile_bars = bars + 8 * (2 + 2 * KS + 2 * VS);
-  auto s_full = [&](int x) { return tile_bars + 8 * x; };
-  auto p_full = [&](int x) { return tile_bars + 8 * (2 + x); };
-  auto pv_done = [&](int x) { return tile_bars + 8 * (4 + x); };
-  auto final_bar = [&](int x) { return tile_bars + 8 * (6 + x); };
+  const uint32_t q_full = bars;
+  auto k_full = [&](int s) { return bars + 8 * (1 + s); };
+  auto k_empty = [&](int s) { return bars + 8 * (1 + KS + s); };
+  auto v_full = [&](int s) { return bars + 8 * (1 + 2 * KS + s); };
+  auto v_empty = [&](int s) { return bars + 8 * (1 + 2 * KS + VS + s); };
+  const uint32_t tile_bars = bars + 8 * (1 + 2 * KS + 2 * VS);
+  auto s_full = [&](int b) { return tile_bars + 8 * b; };
+  auto p_full = [&](int b, int h) { return tile_bars + 8 * (2 + 2 * b + h); };
+  auto pv_done = [&](int b) { return tile_bars + 8 * (6 + b); };
+  const uint32_t final_s = tile_bars + 8 * 8;
+  const uint32_t final_pv = tile_bars + 8 * 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -172,11 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t b = bars + 8 * i;
-      const bool softmax_arrivals = b == p_full(0) || b == p_full(1);
-      // a K or V stage is free once both issuers' MMAs that read it have completed
-      const bool both_issuers = (b >= k_empty(0) && b < k_empty(0) + 8 * KS) ||
-                                (b >= v_empty(0) && b < v_empty(0) + 8 * VS);
-      mbar_init(b, softmax_arrivals ? 128 : both_issuers ? 2 : 1);
+      // p_full: the 128 softmax threads of one column half
+      const bool softmax_arrivals = b >= p_full(0, 0) && b <= p_full(1, 1);
+      mbar_init(b, softmax_arrivals ? 128 : 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -191,44 +186,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const Item it = decode(p, blockIdx.x);
-  // K/V tiles in ring order: chunks r, r-1, ..., r-cp+1 (mod cp), or one chunk
+  // K/V tiles in ring order: chunks r, r-1, ..., r-cp+1 (mod cp), or one chunk;
+  // every role walks the same list and skips the tiles the causal mask hides
   const int kv_first = p.q_rank >= 0 ? p.kv_rank : it.rank;
   const int kv_chunks = p.q_rank >= 0 ? 1 : p.m.cp;
   const int kv_row_base = (it.b * p.Hkv + it.g) * p.T;
+  auto walk_start = [&](TileWalk& w) {
+    w.start(p.m, kv_first, kv_chunks, -1, 1);
+    while (!w.done() && classify(it.pos0, w.pos()) == kEmpty) w.next();
+  };
+  auto walk_next = [&](TileWalk& w) {
+    do w.next(); while (!w.done() && classify(it.pos0, w.pos()) == kEmpty);
+  };
 
   if (warp < 4) {
   regs_ctl();  // warpgroup 0: TMA producers (warps 0, 3) and MMA issuers (warps 1, 2)
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ producers
-    // warp 0: the Q tiles, then the K tiles; warp 3: the V tiles
     if (lane == 0) {
       const bool is_k = warp == 0;
       const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
       tma_prefetch_desc(tm);
-      int q_issued[2] = {0, 0};
-      if (is_k) {
+      bool q_issued = false;
+      if (is_k && !p.debug_fault) {  // fault hook: the Q load never happens
         tma_prefetch_desc(&tm_q);
-        for (int x = 0; x < 2; ++x) {
-          if (!it.active[x]) continue;
-          if (x == 0 && p.debug_fault) continue;  // fault hook: this load never happens
-          mbar_expect_tx(q_full(x), L::kTileBytes);
-          const int row = (it.b * p.Hq + it.h[x]) * p.T + it.slot0[x];
-          for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_2d(sbase + L::kQ + x * L::kTileBytes + kb * (kTile * 128), &tm_q, kb * 64,
-                        row, q_full(x));
-          q_issued[x] = 1;
-        }
+        mbar_expect_tx(q_full, L::kTileBytes);
+        const int row = (it.b * p.Hq + it.h) * p.T + it.slot0;
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, row, q_full);
+        q_issued = true;
       }
       const int nst = is_k ? KS : VS;
       const uint32_t base = sbase + (is_k ? L::kK : L::kV);
       int stage = 0, par = 0;
       uint32_t issued = 0, issued_par = 0;  // bit s: stage s loaded / its phase parity
       TileWalk wk;
-      for (wk.start(p.m, kv_first, kv_chunks, -1, 1); !wk.done(); wk.next()) {
-        const int kpos = wk.pos();
-        const int ca = classify(it.pos0[0], kpos);
-        const int cb = it.active[1] ? classify(it.pos0[1], kpos) : kEmpty;
-        if (ca == kEmpty && cb == kEmpty) continue;
+      for (walk_start(wk); !wk.done(); walk_next(wk)) {
         const uint32_t empty = is_k ? k_empty(stage) : v_empty(stage);
         const uint32_t full = is_k ? k_full(stage) : v_full(stage);
         if (!mbar_wait(empty, par ^ 1, abort, p.status, tmo)) break;
@@ -241,241 +234,238 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == nst) stage = 0, par ^= 1;
       }
       // never leave with a copy still writing into this CTA's shared memory
-      for (int x = 0; x < 2; ++x)
-        if (q_issued[x]) drain_wait(q_full(x), 0);
+      if (q_issued) drain_wait(q_full, 0);
       for (int st = 0; st < nst; ++st)
         if ((issued >> st) & 1u)
           drain_wait(is_k ? k_full(st) : v_full(st), (issued_par >> st) & 1u);
     }
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // One issuer per query tile (warp 1: A, warp 2: B).  A tcgen05.mma takes a
-    // thread about 35-50 cycles to issue against 64 cycles to run at N = 128 and
-    // the tensor pipe queues only a few, so a single thread serving both softmax
-    // warpgroups in turn puts one tile's PV and the next step's waits on the other
-    // tile's S -> softmax -> PV chain; with a thread per tile each chain runs on
-    // its own.  Both issuers wait for every K and V load, even one their tile does
-    // not use, so their k_empty / v_empty arrivals stay one per load.
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      const int x = warp - 1;
       constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
-      bool ok = true;
-      if (it.active[x]) ok = mbar_wait(q_full(x), 0, abort, p.status, tmo);
+      constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
+      bool ok = mbar_wait(q_full, 0, abort, p.status, tmo);
       tc_fence_after();
       // descriptor bases; per k-step offsets are compile-time constants (16-byte units)
-      constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
-      const uint64_t qd = sdesc_sw128(sbase + L::kQ, 16, 1024) + (uint64_t)(x * kTileDesc);
+      const uint64_t qd = sdesc_sw128(sbase + L::kQ, 16, 1024);
       const uint64_t kd0 = sdesc_sw128(sbase + L::kK, 16, 1024);
-      const uint64_t vd0 = sdesc_sw128(sbase + L::kV, kTile * 128, 1024);
       StageRing<KS> kr;
-      StageRing<VS> vr;
-      int cnt = 0, cnt_other = 0;  // S products issued so far by this / the other issuer
+      int j = 0;
       TileWalk wk;
-      for (wk.start(p.m, kv_first, kv_chunks, -1, 1); !wk.done() && ok; wk.next()) {
-        const int kpos = wk.pos();
-        const int ca = classify(it.pos0[0], kpos);
-        const int cb = it.active[1] ? classify(it.pos0[1], kpos) : kEmpty;
-        if (ca == kEmpty && cb == kEmpty) continue;  // the producers skip these too
-        const bool mine = (x == 0 ? ca : cb) != kEmpty;
-        const bool other = (x == 0 ? cb : ca) != kEmpty;
+      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
+        const int b = j & 1;
         if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
-        if (mine) {
-          // S_X = Q_X K^T; the S region is free once the previous PV has read P_X
-          if (cnt > 0 && !(ok = mbar_wait(pv_done(x), (cnt - 1) & 1, abort, p.status, tmo)))
-            break;
-          // Ping-pong: the S products alternate A(j), B(j), A(j+1), ... -- S_B of a
-          // K/V tile waits for S_A of the same tile and S_A for S_B of the tile
-          // before -- so one tile's softmax runs while the tensor pipe serves the
-          // other tile instead of both softmax warpgroups contending at once.  Each
-          // issuer is thereby at most one S phase ahead of the other, which keeps
-          // these parity waits unambiguous.
-          if (x == 1 && other &&
-              !(ok = mbar_wait(s_full(0), cnt_other & 1, abort, p.status, tmo)))
-            break;
-          if (x == 0 && cnt_other > 0 &&
-              !(ok = mbar_wait(s_full(1), (cnt_other - 1) & 1, abort, p.status, tmo)))
-            break;
-          tc_fence_after();
-          const uint64_t kd = kd0 + (uint64_t)(kr.stage * kTileDesc);
+        // buffer b is free once PV of tile j-2 has read the P stored there
+        if (j >= 2 && !(ok = mbar_wait(pv_done(b), ((j - 2) >> 1) & 1, abort, p.status, tmo)))
+          break;
+        tc_fence_after();
+        const uint64_t kd = kd0 + (uint64_t)(kr.stage * kTileDesc);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KiB blocks, 32 B steps
-            mma_ss(tmem + x * 128, qd + off, kd + off, kIdescS, kk > 0);
-          }
-          mma_commit(s_full(x));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KiB blocks, 32 B steps
+          mma_ss(tmem + b * 128, qd + off, kd + off, kIdescS, kk > 0);
         }
-        mma_commit(k_empty(kr.stage));  // arrives at once if nothing was issued
-        if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
-        if (mine) {
-          // O_X += P_X V
-          if (!(ok = mbar_wait(p_full(x), cnt & 1, abort, p.status, tmo))) break;
-          tc_fence_after();
-          const uint64_t vd = vd0 + (uint64_t)(vr.stage * kTileDesc);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)  // 16 key rows = 2048 B per k-step
-            mma_ts(tmem + 256 + x * D, tmem + x * 128 + kk * 8, vd + kk * 128, kIdescPV,
-                   (cnt > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(pv_done(x));
-          ++cnt;
-        }
-        mma_commit(v_empty(vr.stage));
-        if (other) ++cnt_other;
+        mma_commit(s_full(b));
+        mma_commit(k_empty(kr.stage));
         kr.advance();
-        vr.advance();
+        ++j;
       }
       // every MMA this thread issued has finished before TMEM can be freed
-      mma_commit(final_bar(x));
-      drain_wait(final_bar(x), 0);
+      mma_commit(final_s);
+      drain_wait(final_s, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
+      const uint64_t vd0 = sdesc_sw128(sbase + L::kV, kTile * 128, 1024);
+      StageRing<VS> vr;
+      bool ok = true;
+      int j = 0;
+      TileWalk wk;
+      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
+        const int b = j & 1;
+        if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
+        const uint64_t vd = vd0 + (uint64_t)(vr.stage * kTileDesc);
+        for (int h = 0; h < 2 && ok; ++h) {
+          // O_h += P_h V_h: keys [64h, 64h+64), 16 key rows = 2048 B per k-step
+          if (!(ok = mbar_wait(p_full(b, h), (j >> 1) & 1, abort, p.status, tmo))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + 256 + h * D, tmem + b * 128 + h * 64 + kk * 8,
+                   vd + (uint64_t)((h * 4 + kk) * 128), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit(pv_done(b));
+        mma_commit(v_empty(vr.stage));
+        vr.advance();
+        ++j;
+      }
+      mma_commit(final_pv);
+      drain_wait(final_pv, 0);
     }
   }
   } else {
-    regs_math();  // warpgroups 1 and 2: softmax / gradient math
+    regs_math();  // warpgroups 1 and 2: softmax
     // ------------------------------------------------------------ softmax
-    const int x = (warp - 4) >> 2;  // tile A (warps 4..7) or B (warps 8..11)
-    const int quad = warp & 3;      // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int half = (warp - 4) >> 2;  // key columns [64 half, 64 half + 64) of a tile
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + x * 128;
-    const uint32_t t_o = tmem + lane_off + 256 + x * D;
-    const float sl2 = p.scale_log2;
+    const uint32_t t_o = tmem + lane_off + 256 + half * D;
+    const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
     float m_run = -INFINITY, l_run = 0.f;
     int cnt = 0;
     bool ok = true;
-    if (it.active[x]) {
-      TileWalk wk;
-      for (wk.start(p.m, kv_first, kv_chunks, -1, 1); !wk.done(); wk.next()) {
-        const int kpos = wk.pos();
-        const int cls = classify(it.pos0[x], kpos);
-        if (cls == kEmpty) continue;
-        if (!(ok = warp_wait(s_full(x), cnt & 1, abort, p.status, tmo))) break;
-        tc_fence_after();
-        uint32_t r[4][32];
+    TileWalk wk;
+    for (walk_start(wk); !wk.done(); walk_next(wk)) {
+      const int kpos = wk.pos();
+      const int cls = classify(it.pos0, kpos);
+      const int b = cnt & 1;
+      const uint32_t t_s = tmem + lane_off + b * 128 + half * 64;
+      if (!(ok = warp_wait(s_full(b), (cnt >> 1) & 1, abort, p.status, tmo))) break;
+      tc_fence_after();
+      uint32_t r[2][32];
+      tmem_ld32(t_s, r[0]);
+      tmem_ld32(t_s + 32, r[1]);
+      tmem_wait_ld();
+      if (cls == kDiag) {
+        // key column j of this half is visible iff kpos + 64 half + j <= qpos + row
+        const int thr = row + it.pos0 - kpos - half * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, r[c]);
-        tmem_wait_ld();
-        float mx = -INFINITY;
-        if (cls == kDiag) {
-          // key column j is visible iff kpos + j <= qpos + row
-          const int thr = row + it.pos0[x] - kpos;
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c * 32 + j > thr) r[c][j] = __float_as_uint(-INFINITY);
-        }
-        {
-          // 8 independent chains of three-input max over the 128 scores
-          float m8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int j = 0; j < 32; j += 2)
-              m8[(c * 16 + j / 2) & 7] = max3(m8[(c * 16 + j / 2) & 7], __uint_as_float(r[c][j]),
-                                              __uint_as_float(r[c][j + 1]));
-          mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        }
-        const float m_new = fmaxf(m_run, mx * sl2);
-        bool rescale = false;
-        float factor = 1.f;
-        if (cnt == 0) {
-          m_run = m_new;
-        } else if (m_new > m_run + 8.f) {
-          factor = ex2(m_run - m_new);
-          l_run *= factor;
-          m_run = m_new;
-          rescale = true;
-        }
-        const float mu = m_run == -INFINITY ? 0.f : m_run;
-        // P = 2^(s * scale * log2e - m): exponent arguments and row sums two lanes per
-        // instruction (packed fp32x2), 2^x on the special-function unit
-        const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
-        float2 l4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 x = fma2(make_float2(__uint_as_float(r[c][2 * j]),
-                                              __uint_as_float(r[c][2 * j + 1])), sl2v, nmu);
-            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-            l4[j & 3] = add2(l4[j & 3], pp);
-            pk[j] = pack_bf16(pp.x, pp.y);
-          }
-          tmem_st16(t_s + c * 16, pk);
-        }
-        l_run += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
-        tmem_wait_st();
-        if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
-          // the output so far must be final in TMEM before it is rescaled
-          if (!(ok = warp_wait(pv_done(x), (cnt - 1) & 1, abort, p.status, tmo))) break;
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o32[32];
-            tmem_ld32(t_o + c * 32, o32);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * factor);
-            tmem_st32(t_o + c * 32, o32);
-          }
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(p_full(x));
-        ++cnt;
+          for (int j = 0; j < 32; ++j)
+            if (c * 32 + j > thr) r[c][j] = __float_as_uint(-INFINITY);
       }
-      // -------------------------------------------------------- epilogue
-      if (ok && cnt > 0) ok = warp_wait(pv_done(x), (cnt - 1) & 1, abort, p.status, tmo);
-      if (ok) {
+      float mx;
+      {
+        // 4 independent chains of three-input max over the 64 scores
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; j += 2)
+            m4[(c * 16 + j / 2) & 3] = max3(m4[(c * 16 + j / 2) & 3], __uint_as_float(r[c][j]),
+                                            __uint_as_float(r[c][j + 1]));
+        mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+      }
+      const float m_new = fmaxf(m_run, mx * p.scale_log2);
+      bool rescale = false;
+      float factor = 1.f;
+      if (cnt == 0) {
+        m_run = m_new;
+      } else if (m_new > m_run + 8.f) {
+        factor = ex2(m_run - m_new);
+        l_run *= factor;
+        m_run = m_new;
+        rescale = true;
+      }
+      const float mu = m_run == -INFINITY ? 0.f : m_run;
+      // P = 2^(s * scale * log2e - m): exponent arguments and row sums two lanes per
+      // instruction (packed fp32x2), 2^x on the special-function unit
+      const float2 nmu = make_float2(-mu, -mu);
+      float2 l4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 x = fma2(make_float2(__uint_as_float(r[c][2 * j]),
+                                            __uint_as_float(r[c][2 * j + 1])), sl2v, nmu);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          l4[j & 3] = add2(l4[j & 3], pp);
+          pk[j] = pack_bf16(pp.x, pp.y);
+        }
+        tmem_st16(t_s + c * 16, pk);
+      }
+      l_run += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+      tmem_wait_st();
+      if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O_h so far must be final in TMEM before it is rescaled
+        if (!(ok = warp_wait(pv_done((cnt - 1) & 1), ((cnt - 1) >> 1) & 1, abort, p.status, tmo)))
+          break;
         tc_fence_after();
-        const bool partial = p.q_rank >= 0;
-        const int64_t bh = (int64_t)it.b * p.Hq + it.h[x];
-        const int64_t orow = partial ? bh * p.m.c + (it.slot0[x] - p.q_rank * p.m.c) + row
-                                     : bh * p.T + it.slot0[x] + row;
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o32[32];
-          if (cnt > 0) {
-            tmem_ld32(t_o + c * 32, o32);
-            tmem_wait_ld();
-          } else {
+          tmem_ld32(t_o + c * 32, o32);
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o32[j] = 0u;
-          }
-          if (OUT_F32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(__uint_as_float(o32[4 * j]) * inv,
-                                   __uint_as_float(o32[4 * j + 1]) * inv,
-                                   __uint_as_float(o32[4 * j + 2]) * inv,
-                                   __uint_as_float(o32[4 * j + 3]) * inv);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D +
-                                                  c * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 v4;
-              v4.x = pack_bf16(__uint_as_float(o32[8 * j + 0]) * inv,
-                               __uint_as_float(o32[8 * j + 1]) * inv);
-              v4.y = pack_bf16(__uint_as_float(o32[8 * j + 2]) * inv,
-                               __uint_as_float(o32[8 * j + 3]) * inv);
-              v4.z = pack_bf16(__uint_as_float(o32[8 * j + 4]) * inv,
-                               __uint_as_float(o32[8 * j + 5]) * inv);
-              v4.w = pack_bf16(__uint_as_float(o32[8 * j + 6]) * inv,
-                               __uint_as_float(o32[8 * j + 7]) * inv);
-              dst[j] = v4;
-            }
-          }
+          for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * factor);
+          tmem_st32(t_o + c * 32, o32);
         }
-        p.lse[orow] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+        tmem_wait_st();
       }
+      tc_fence_before();
+      mbar_arrive(p_full(b, half));
+      ++cnt;
+    }
+    // -------------------------------------------------------- epilogue
+    if (ok && cnt > 0)
+      ok = warp_wait(pv_done((cnt - 1) & 1), ((cnt - 1) >> 1) & 1, abort, p.status, tmo);
+    // The two halves' (m, l) meet in shared memory, in the Q tile's space: its load
+    // has landed (q_full) and its last reader, S of the last tile, completed before
+    // the softmax of that tile began.  Both warps of the pair always reach the barrier.
+    if (ok) ok = warp_wait(q_full, 0, abort, p.status, tmo);
+    float2* xch = reinterpret_cast<float2*>(smem + L::kQ);
+    if (ok) xch[half * 128 + row] = make_float2(m_run, l_run);
+    pair_sync(quad);
+    const float2 other = xch[(1 - half) * 128 + row];
+    if (ok) {
+      tc_fence_after();
+      const float m0 = half == 0 ? m_run : other.x, l0 = half == 0 ? l_run : other.y;
+      const float m1 = half == 0 ? other.x : m_run, l1 = half == 0 ? other.y : l_run;
+      const float mm = fmaxf(m0, m1);
+      float w0 = 0.f, w1 = 0.f;
+      if (mm != -INFINITY) {
+        w0 = ex2(m0 - mm);
+        w1 = ex2(m1 - mm);
+      }
+      const float lsum = w0 * l0 + w1 * l1;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float a0 = w0 * inv, a1 = w1 * inv;
+      const bool partial = p.q_rank >= 0;
+      const int64_t bh = (int64_t)it.b * p.Hq + it.h;
+      const int64_t orow = partial ? bh * p.m.c + (it.slot0 - p.q_rank * p.m.c) + row
+                                   : bh * p.T + it.slot0 + row;
+      // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = half * (D / 2) + c * 32;
+        uint32_t o0[32], o1[32];
+        if (cnt > 0) {
+          tmem_ld32(tmem + lane_off + 256 + col, o0);
+          tmem_ld32(tmem + lane_off + 256 + D + col, o1);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o0[j] = o1[j] = 0u;
+        }
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          v[j] = a0 * __uint_as_float(o0[j]) + a1 * __uint_as_float(o1[j]);
+        if (OUT_F32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + col);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+          uint4* dst =
+              reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                                pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                                pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+        }
+      }
+      if (half == 0) p.lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * kLn2 : -INFINITY;
     }
   }
 
@@ -525,10 +515,6 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
   p.n_rep = R.Hq / R.Hkv;
   p.m = SeqMap::make(R.T, R.cp, R.zz);
   p.scale_log2 = R.scale * 1.44269504088896340736f;
-  p.head_pairs = (p.n_rep % 2) == 0;
-  const int seg_tiles = (R.zz ? p.m.c / 2 : p.m.c) / tcfwd::kTile;
-  p.tiles_per_item = (!p.head_pairs && seg_tiles % 2 == 0) ? 2 : 1;
-  p.n_hu = p.head_pairs ? R.Hq / 2 : R.Hq;
   const bool partial = q_rank >= 0;
   p.q_tiles = (partial ? p.m.c : R.T) / tcfwd::kTile;
   p.q_rank = partial ? q_rank : -1;
@@ -537,7 +523,7 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
   p.lse = lse;
   p.status = status;
   p.debug_fault = R.debug_fault;
-  const int items = R.B * p.n_hu * (p.q_tiles / p.tiles_per_item);
+  const int items = R.B * R.Hq * p.q_tiles;
   if (items == 0) return cudaSuccess;
   timing_begin(partial ? "tc_partial_fwd" : "tc_ring_fwd", st);
   cudaError_t e;
