@@ -23,8 +23,8 @@
 //
 // Delta = rowsum(dO * O) comes from the pre-pass kernel (merge.cu).  Compute
 // warps: 8, warp w handles TMEM lane quadrant w%4 and column half (w-4)/4.
-// Warp 0 loads through TMA; warp 1 issues the score products (S, dP) and
-// warp 2 the gradient products (dV/dK or dQ), one thread each.
+// Warp 0 loads through TMA; warps 1 and 3 issue the score products (S and dP)
+// and warp 2 the gradient products (dV/dK or dQ), one thread each.
 // Every mbarrier wait is bounded (see tc_fwd.cu for the abort protocol).
 #include <math.h>
 
@@ -99,8 +99,9 @@ struct DkdvSmem {
   static constexpr int kDelta = kLse + kStages * 512;
   static constexpr int kBar = kDelta + kStages * 512;
   // kv_full, q_full[S], do_full[S], qdo_empty[S], s_full, dp_full, p_full,
-  // ds_full, dv_done, dk_done, final (gradient issuer), final_a (score issuer)
-  static constexpr int kNumBars = 1 + 3 * kStages + 8;
+  // ds_full, dv_done, dk_done, final (gradient issuer), final_s (S^T issuer),
+  // final_p (dP^T issuer)
+  static constexpr int kNumBars = 1 + 3 * kStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;
 };
@@ -128,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t dv_done = s_full + 32;
   const uint32_t dk_done = s_full + 40;
   const uint32_t final_bar = s_full + 48;
-  const uint32_t final_a = s_full + 56;
+  const uint32_t final_s = s_full + 56;
+  const uint32_t final_p = s_full + 64;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto walk_start = [&](TileWalk& w) { w.start(p.m, s_own, p.m.cp, +1, p.n_rep); };
 
   if (warp < 4) {
-  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2)
+  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2, 3)
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -204,54 +206,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_wait(do_full(s), (ipar >> s) & 1u);
         }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
     if (lane == 0) {
-      // Score issuer: S^T = K Q^T and dP^T = V dO^T.  A tcgen05.mma takes a thread
-      // about 35-50 cycles to issue against 64 cycles to run at N = 128, and the
-      // tensor pipe queues only a few, so a single issuer that also waits on the
-      // softmax warps leaves the pipe idle; the gradient products come from a
-      // second issuer (warp 2) whose waits overlap these.
+      // Score issuers: warp 1 S^T = K Q^T, warp 3 dP^T = V dO^T (SS, K-major); warp 2
+      // issues the gradient products.  A thread takes about 35-50 cycles to issue a
+      // tcgen05.mma that runs 64 cycles at N = 128, and its next memory access after
+      // a tcgen05.commit waits for the committed MMAs, so a thread per product keeps
+      // each product's waits from holding up the others.
+      const bool is_s = warp == 1;
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
       bool ok = mbar_wait(kv_full, 0, abort, p.status, kTimeoutNs);
       tc_fence_after();
       // descriptor bases (16-byte units), K-major
       constexpr uint32_t kTD = L::kTB >> 4;
-      const uint64_t kd = sdesc_sw128(sbase + L::kK, 16, 1024);
-      const uint64_t vd = sdesc_sw128(sbase + L::kV, 16, 1024);
-      const uint64_t qd_k0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
-      const uint64_t dod_k0 = sdesc_sw128(sbase + L::kDO, 16, 1024);
+      const uint64_t ad = sdesc_sw128(sbase + (is_s ? L::kK : L::kV), 16, 1024);
+      const uint64_t bd0 = sdesc_sw128(sbase + (is_s ? L::kQ : L::kDO), 16, 1024);
+      const uint32_t dst = tmem + (is_s ? 0 : 128);
       int stage = 0, par = 0, cnt = 0;
       TileWalk wk;
       for (walk_start(wk); !wk.done() && ok; wk.next()) {
         if (classify(wk.pos(), kpos0) == kEmpty) continue;
-        const uint64_t soff = (uint64_t)(stage * kTD);
-        // S^T  (the S region is free once the previous dV has read P^T)
-        if (!(ok = mbar_wait(q_full(stage), par, abort, p.status, kTimeoutNs))) break;
-        if (cnt > 0 && !(ok = mbar_wait(dv_done, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
+        // S^T: the S region is free once the previous dV has read P^T;
+        // dP^T: the dP region is free once the previous dK has read dS^T
+        if (!(ok = mbar_wait(is_s ? q_full(stage) : do_full(stage), par, abort, p.status,
+                             kTimeoutNs)))
+          break;
+        if (cnt > 0 && !(ok = mbar_wait(is_s ? dv_done : dk_done, (cnt - 1) & 1, abort, p.status,
+                                        kTimeoutNs)))
           break;
         tc_fence_after();
+        const uint64_t bd = bd0 + (uint64_t)(stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          mma_ss(tmem, kd + off, qd_k0 + soff + off, kIdSS, kk > 0);
+          mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
         }
-        mma_commit(s_full);
-        // dP^T  (the dP region is free once the previous dK has read dS^T)
-        if (!(ok = mbar_wait(do_full(stage), par, abort, p.status, kTimeoutNs))) break;
-        if (cnt > 0 && !(ok = mbar_wait(dk_done, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
-          break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          mma_ss(tmem + 128, vd + off, dod_k0 + soff + off, kIdSS, kk > 0);
-        }
-        mma_commit(dp_full);
+        mma_commit(is_s ? s_full : dp_full);
         ++cnt;
         if (++stage == S) stage = 0, par ^= 1;
       }
-      mma_commit(final_a);
-      drain_wait(final_a, 0);
+      mma_commit(is_s ? final_s : final_p);
+      drain_wait(is_s ? final_s : final_p, 0);
     }
   } else if (warp == 2) {
     if (lane == 0) {
@@ -437,8 +432,9 @@ struct DqSmem {
   static constexpr int kV = kK + kKStages * kTB;
   static constexpr int kBar = kV + kVStages * kTB;
   // qdo_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full, s_free,
-  // dp_full, ds_full, dq_done[2], final (gradient issuer), final_a (score issuer)
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 8;
+  // dp_full[2], ds_full[2] (one per dP buffer), dq_done[2], final_q (dQ issuer),
+  // final_s (S issuer), final_p (dP issuer)
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 11;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;
 };
@@ -463,11 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto v_empty = [&](int s) { return bars + 8 * (1 + 2 * KS + VS + s); };
   const uint32_t s_full = bars + 8 * (1 + 2 * KS + 2 * VS);
   const uint32_t s_free = s_full + 8;
-  const uint32_t dp_full = s_full + 16;
-  const uint32_t ds_full = s_full + 24;
-  auto dq_done = [&](int x) { return s_full + 32 + 8 * x; };
-  const uint32_t final_bar = s_full + 48;
-  const uint32_t final_a = s_full + 56;
+  // per-buffer barriers: a second arrival on a buffer's barrier needs that buffer
+  // to have been recycled, so no waiter can ever be two phases behind
+  auto dp_full = [&](int x) { return s_full + 16 + 8 * x; };
+  auto ds_full = [&](int x) { return s_full + 32 + 8 * x; };
+  auto dq_done = [&](int x) { return s_full + 48 + 8 * x; };
+  const uint32_t final_q = s_full + 64;
+  const uint32_t final_s = s_full + 72;
+  const uint32_t final_p = s_full + 80;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -475,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t b = bars + 8 * i;
-      mbar_init(b, (b == s_free || b == ds_full) ? 256 : 1);
+      mbar_init(b, (b == s_free || b == ds_full(0) || b == ds_full(1)) ? 256 : 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -510,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kv_row_base = (b * p.Hkv + g) * p.T;
 
   if (warp < 4) {
-  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2)
+  regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2, 3)
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -548,57 +547,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < VS; ++s)
         if (vr.was_issued(s)) drain_wait(v_full(s), vr.issued_parity(s));
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
+    // One issuer per product: warp 1 S = Q K^T, warp 3 dP = dO V^T, warp 2 dQ.  A
+    // thread takes about 35-50 cycles to issue a tcgen05.mma that runs 64 cycles at
+    // N = 128, and its next memory access after a tcgen05.commit waits for the
+    // committed MMAs, so one thread alternating products would keep a single group
+    // in flight and wait on each product's consumers in turn.
     if (lane == 0) {
-      // Score issuer: S = Q K^T and dP = dO V^T of every visited tile, in order.
-      // A tcgen05.mma takes a thread about 35-50 cycles to issue against 64 cycles
-      // to run at N = 128 and the pipe queues only a few, so the dQ products come
-      // from a second issuer (warp 2) whose waits overlap these.
+      const bool is_s = warp == 1;
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
       bool ok = mbar_wait(qdo_full, 0, abort, p.status, kTimeoutNs);
       tc_fence_after();
       // descriptor bases (16-byte units), K-major
       constexpr uint32_t kTD = L::kTB >> 4;
-      const uint64_t qd = sdesc_sw128(sbase + L::kQ, 16, 1024);
-      const uint64_t dod = sdesc_sw128(sbase + L::kDO, 16, 1024);
-      const uint64_t kd_k0 = sdesc_sw128(sbase + L::kK, 16, 1024);
-      const uint64_t vd_k0 = sdesc_sw128(sbase + L::kV, 16, 1024);
+      const uint64_t ad = sdesc_sw128(sbase + (is_s ? L::kQ : L::kDO), 16, 1024);
+      const uint64_t bd0 = sdesc_sw128(sbase + (is_s ? L::kK : L::kV), 16, 1024);
       StageRing<KS> kr;
       StageRing<VS> vr;
       int j = 0;
       TileWalk wk;
       for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        // S(j): the S region is free once the compute warps have read S(j-1)
-        if (j > 0 && !(ok = mbar_wait(s_free, (j - 1) & 1, abort, p.status, kTimeoutNs))) break;
-        if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, kTimeoutNs))) break;
+        uint32_t dst;
+        uint64_t bd;
+        if (is_s) {
+          // S(j): the S region is free once the compute warps have read S(j-1)
+          if (j > 0 && !(ok = mbar_wait(s_free, (j - 1) & 1, abort, p.status, kTimeoutNs))) break;
+          if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, kTimeoutNs))) break;
+          dst = tmem;
+          bd = bd0 + (uint64_t)(kr.stage * kTD);
+        } else {
+          // dP(j) into buffer j&1: free once dQ(j-2) has read the dS stored there
+          if (j >= 2 && !(ok = mbar_wait(dq_done(j & 1), ((j - 2) >> 1) & 1, abort, p.status,
+                                         kTimeoutNs)))
+            break;
+          if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, kTimeoutNs))) break;
+          dst = tmem + 128 + 128 * (j & 1);
+          bd = bd0 + (uint64_t)(vr.stage * kTD);
+        }
         tc_fence_after();
-        const uint64_t kd = kd_k0 + (uint64_t)(kr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          mma_ss(tmem, qd + off, kd + off, kIdSS, kk > 0);
+          mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
         }
-        mma_commit(s_full);
-        // dP(j) into buffer j&1: free once dQ(j-2) has read the dS stored there
-        if (j >= 2 && !(ok = mbar_wait(dq_done(j & 1), ((j - 2) >> 1) & 1, abort, p.status,
-                                       kTimeoutNs)))
-          break;
-        if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, kTimeoutNs))) break;
-        tc_fence_after();
-        const uint64_t vd = vd_k0 + (uint64_t)(vr.stage * kTD);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          mma_ss(tmem + 128 + 128 * (j & 1), dod + off, vd + off, kIdSS, kk > 0);
+        if (is_s) {
+          mma_commit(s_full);
+        } else {
+          mma_commit(dp_full(j & 1));
+          mma_commit(v_empty(vr.stage));  // V of this tile is not read again
         }
-        mma_commit(dp_full);
-        mma_commit(v_empty(vr.stage));  // V of this tile is not read again
         kr.advance();
         vr.advance();
         ++j;
       }
-      mma_commit(final_a);
-      drain_wait(final_a, 0);
+      mma_commit(is_s ? final_s : final_p);
+      drain_wait(is_s ? final_s : final_p, 0);
     }
   } else if (warp == 2) {
     if (lane == 0) {
@@ -611,11 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0;
       TileWalk wk;
       for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        if (!(ok = mbar_wait(ds_full, j & 1, abort, p.status, kTimeoutNs))) break;
-        // dq_done of tile j-1 is committed only now, after dS(j) is seen: the score
-        // issuer's next dP (into that buffer) waits for it, so ds_full cannot run
-        // two phases ahead of this wait
-        if (j > 0) mma_commit(dq_done((j - 1) & 1));
+        if (!(ok = mbar_wait(ds_full(j & 1), (j >> 1) & 1, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
         // K(j) landed before S(j), which the compute warps read before storing dS(j)
         const uint64_t kd_mn = kd_mn0 + (uint64_t)(kr.stage * kTD);
@@ -624,14 +623,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acol = 128 + 128 * (j & 1) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
           mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
         }
+        mma_commit(dq_done(j & 1));  // the dS buffer may take dP(j+2)
         // both S(j) and dQ(j) have read K(j) once dQ(j) completes
         mma_commit(k_empty(kr.stage));
         kr.advance();
         ++j;
       }
-      if (j > 0) mma_commit(dq_done((j - 1) & 1));
-      mma_commit(final_bar);
-      drain_wait(final_bar, 0);
+      mma_commit(final_q);
+      drain_wait(final_q, 0);
     }
   }
   } else {
@@ -675,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[j0] = p0;
           pr[j0 + 1] = p1;
         }
-      if (!(ok = warp_wait(dp_full, j & 1, abort, p.status))) break;
+      if (!(ok = warp_wait(dp_full(j & 1), (j >> 1) & 1, abort, p.status))) break;
       tc_fence_after();
       const uint32_t t_dp = tmem + lane_off + 128 + 128 * (j & 1) + half * 64;
       tmem_ld32(t_dp, sr[0]);
@@ -696,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      mbar_arrive(ds_full(j & 1));
       ++j;
     }
     if (ok && j > 0) ok = warp_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status);
