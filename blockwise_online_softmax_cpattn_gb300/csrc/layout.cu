@@ -68,6 +68,67 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteDev p, const V* __r
   }
 }
 
+// Zigzag permutes as chunk moves.  Each (batch, head) sequence is 2*cp chunks of
+// h = T/(2cp) rows (cp chunks of T/cp rows for the contiguous layout, where the
+// map is the identity); slot-chunk k holds natural chunk k/2 for even k and
+// 2cp-1-k/2 for odd k (tutorial "上下文并行", section "Zig-Zag Ring
+// Attention").  A block copies one part of one destination chunk with streaming
+// 16-byte loads, kUnroll of them in flight per thread; no per-element index math.
+constexpr int kChunkThreads = 256;
+constexpr int kUnroll = 8;
+
+__global__ void __launch_bounds__(kChunkThreads) chunk_copy_kernel(
+    const int4* __restrict__ src, int4* __restrict__ dst, int64_t chunk_vecs, int nchunk,
+    int cp, int zz, int inverse, int splits) {
+  const int64_t blk = blockIdx.x;
+  const int part = (int)(blk % splits);
+  const int64_t rest = blk / splits;
+  const int k = (int)(rest % nchunk);  // destination chunk
+  const int64_t bh = rest / nchunk;
+  int c = k;                            // source chunk
+  if (zz) {
+    if (!inverse) c = (k & 1) ? 2 * cp - 1 - (k >> 1) : (k >> 1);
+    else c = k < cp ? 2 * k : 2 * (2 * cp - 1 - k) + 1;
+  }
+  const int64_t per = chunk_vecs / splits;
+  const int4* s = src + (bh * nchunk + c) * chunk_vecs + part * per;
+  int4* d = dst + (bh * nchunk + k) * chunk_vecs + part * per;
+  for (int64_t i0 = threadIdx.x; i0 < per; i0 += (int64_t)kChunkThreads * kUnroll) {
+    int4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + (int64_t)u * kChunkThreads;
+      if (i < per) v[u] = __ldcs(s + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + (int64_t)u * kChunkThreads;
+      if (i < per) __stcs(d + i, v[u]);
+    }
+  }
+}
+
+static cudaError_t run_chunks(const PermuteArgs& a, const void* src, void* dst, int row_bytes,
+                              cudaStream_t st) {
+  const int cpr = a.cp / a.a2a;  // ranks of the ring the permute serves
+  const int nchunk = a.zz ? 2 * cpr : cpr;
+  const int64_t chunk_vecs = (int64_t)(a.T / nchunk) * row_bytes / 16;
+  const int64_t seqs = (int64_t)a.B * a.H;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // enough blocks to cover every SM several times over
+  int splits = 1;
+  while (splits < 64 && seqs * nchunk * splits < 4LL * sms && chunk_vecs % (2 * splits) == 0 &&
+         chunk_vecs / (2 * splits) >= kChunkThreads)
+    splits *= 2;
+  const int64_t blocks = seqs * nchunk * splits;
+  if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  chunk_copy_kernel<<<(unsigned)blocks, kChunkThreads, 0, st>>>(
+      (const int4*)src, (int4*)dst, chunk_vecs, nchunk, cpr, a.zz, a.kind == kZigzagInv, splits);
+  return cudaGetLastError();
+}
+
 template <typename V>
 static cudaError_t run(const PermuteDev& p, const void* src, void* dst, int64_t rows, int vpr,
                        cudaStream_t st) {
@@ -99,7 +160,10 @@ cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cud
   const uintptr_t al = (uintptr_t)src | (uintptr_t)dst;
   timing_begin(a.kind <= kZigzagInv ? "layout_zigzag" : "layout_a2a", st);
   cudaError_t e;
-  if (row_bytes % 16 == 0 && al % 16 == 0)
+  const int nchunk = a.zz ? 2 * (a.cp / a.a2a) : a.cp / a.a2a;
+  if (a.kind <= kZigzagInv && row_bytes % 16 == 0 && al % 16 == 0 && a.T % nchunk == 0)
+    e = run_chunks(a, src, dst, row_bytes, st);
+  else if (row_bytes % 16 == 0 && al % 16 == 0)
     e = run<int4>(p, src, dst, rows, row_bytes / 16, st);
   else if (row_bytes % 8 == 0 && al % 8 == 0)
     e = run<int2>(p, src, dst, rows, row_bytes / 8, st);
