@@ -11,6 +11,7 @@
 namespace cpattn {
 
 // Device status codes (the values of cpattn_status).
+constexpr int kStatusLaunch = 3;   // a kernel found its launch unusable (reported as a CUDA error)
 constexpr int kStatusTimeout = 4;
 
 // ---------------------------------------------------------------------------

@@ -1,6 +1,6 @@
 // Ring-attention forward on the 5th-generation tensor cores (sm_103a).
 //
-// What one CTA computes: one 128-row query tile of one (batch, head) against
+// What one work item computes: one 128-row query tile of one (batch, head) against
 // every key/value tile its rows can see, visited in ring order -- step i of
 // rank r holds the K/V chunk of rank (r - i) mod cp (tutorial "上下文并行",
 // section "朴素 Ring Attention") -- with the running max / sum / output carried
@@ -9,6 +9,10 @@
 // wholly hidden by the causal mask (key position > query position for every
 // pair) are skipped; diagonal tiles are masked per element from global
 // positions.
+//
+// The CTAs are persistent (at most one per SM) and walk the heaviest-first item
+// list in a snake order; every pipeline keeps running across items, so the next
+// item's loads and first S overlap the current item's last tiles and epilogue.
 //
 // Two softmax threads per query row: thread (row, h) owns key columns
 // [64h, 64h+64) of every tile and runs an online softmax of its own over them
@@ -65,6 +69,7 @@ struct Params {
   SeqMap m;
   float scale_log2;
   int q_tiles;          // 128-row query tiles per (batch, head) in the launch
+  int n_items;          // work items (B * Hq * q_tiles), walked by resident CTAs
   int q_rank, kv_rank;  // partial mode when q_rank >= 0
   void* o;
   float* lse;
@@ -74,19 +79,24 @@ struct Params {
 
 template <int D>
 struct Smem {
-  // one Q tile; K and V in rings of their own (K is last read by S, V by PV)
+  // one Q tile; K and V in rings of their own (K is last read by S, V by PV); the
+  // (m, l) exchange of the two column halves of each row
   static constexpr int kKStages = D == 128 ? 3 : 4;
   static constexpr int kVStages = D == 128 ? 3 : 4;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kTileBytes;
   static constexpr int kV = kK + kKStages * kTileBytes;
-  static constexpr int kBar = kV + kVStages * kTileBytes;
-  // barriers: q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
-  // p_full[2 buffers][2 halves], pv_done[2], final_s, final_pv
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 4 + 2 + 2;
+  static constexpr int kXch = kV + kVStages * kTileBytes;
+  static constexpr int kBar = kXch + 2 * kTile * 8;
+  // barriers: q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+  // s_full[2], p_full[2 buffers][2 halves], pv_done[2], o_free, xch_full, xch_free,
+  // final_s, final_pv
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 4 + 2 + 3 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16 + 1024;  // + alignment slack
+  // no alignment slack: the kernel declares its dynamic shared memory 1024-byte
+  // aligned and checks it
+  static constexpr int kBytes = kMisc + 16;
 };
 
 struct Item {
@@ -113,6 +123,15 @@ __device__ __forceinline__ Item decode(const Params& p, int w) {
   return it;
 }
 
+// The k-th work item of this CTA, or -1: the CTAs stay resident and walk the
+// heaviest-first item list in a snake (rounds of gridDim.x items, every other
+// round reversed), which evens out the per-CTA totals.
+__device__ __forceinline__ int item_of(int k, int n_items) {
+  const int G = gridDim.x;
+  const int w = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return w < n_items ? w : -1;
+}
+
 __device__ __forceinline__ int classify(int qpos0, int kpos0) {
   if (kpos0 + kTile - 1 <= qpos0) return kFull;
   if (kpos0 > qpos0 + kTile - 1) return kEmpty;
@@ -132,35 +151,38 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t par) {
   return mbar_wait(bar, par, &never, nullptr, kDrainTimeoutNs);
 }
 
-// Named barrier of the two softmax warps that serve one TMEM lane quadrant.
-__device__ __forceinline__ void pair_sync(int quad) {
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-}
-
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using L = Smem<D>;
   constexpr int KS = L::kKStages, VS = L::kVStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the layout has no alignment slack
+    if (threadIdx.x == 0) latch_status(p.status, kStatusLaunch);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::kBar;
   const uint32_t q_full = bars;
-  auto k_full = [&](int s) { return bars + 8 * (1 + s); };
-  auto k_empty = [&](int s) { return bars + 8 * (1 + KS + s); };
-  auto v_full = [&](int s) { return bars + 8 * (1 + 2 * KS + s); };
-  auto v_empty = [&](int s) { return bars + 8 * (1 + 2 * KS + VS + s); };
-  const uint32_t tile_bars = bars + 8 * (1 + 2 * KS + 2 * VS);
+  const uint32_t q_empty = bars + 8;
+  auto k_full = [&](int s) { return bars + 8 * (2 + s); };
+  auto k_empty = [&](int s) { return bars + 8 * (2 + KS + s); };
+  auto v_full = [&](int s) { return bars + 8 * (2 + 2 * KS + s); };
+  auto v_empty = [&](int s) { return bars + 8 * (2 + 2 * KS + VS + s); };
+  const uint32_t tile_bars = bars + 8 * (2 + 2 * KS + 2 * VS);
   auto s_full = [&](int b) { return tile_bars + 8 * b; };
   auto p_full = [&](int b, int h) { return tile_bars + 8 * (2 + 2 * b + h); };
   auto pv_done = [&](int b) { return tile_bars + 8 * (6 + b); };
-  const uint32_t final_s = tile_bars + 8 * 8;
-  const uint32_t final_pv = tile_bars + 8 * 9;
+  const uint32_t o_free = tile_bars + 8 * 8;
+  const uint32_t xch_full = tile_bars + 8 * 9;
+  const uint32_t xch_free = tile_bars + 8 * 10;
+  const uint32_t final_s = tile_bars + 8 * 11;
+  const uint32_t final_pv = tile_bars + 8 * 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  float2* xch = reinterpret_cast<float2*>(smem + L::kXch);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -169,9 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t b = bars + 8 * i;
-      // p_full: the 128 softmax threads of one column half
-      const bool softmax_arrivals = b >= p_full(0, 0) && b <= p_full(1, 1);
-      mbar_init(b, softmax_arrivals ? 128 : 1);
+      // p_full: the 128 softmax threads of one column half; o_free / xch_*: all 256
+      const bool half_arrivals = b >= p_full(0, 0) && b <= p_full(1, 1);
+      const bool all_arrivals = b == o_free || b == xch_full || b == xch_free;
+      mbar_init(b, half_arrivals ? 128 : all_arrivals ? 256 : 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -185,17 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const Item it = decode(p, blockIdx.x);
-  // K/V tiles in ring order: chunks r, r-1, ..., r-cp+1 (mod cp), or one chunk;
-  // every role walks the same list and skips the tiles the causal mask hides
-  const int kv_first = p.q_rank >= 0 ? p.kv_rank : it.rank;
-  const int kv_chunks = p.q_rank >= 0 ? 1 : p.m.cp;
-  const int kv_row_base = (it.b * p.Hkv + it.g) * p.T;
-  auto walk_start = [&](TileWalk& w) {
-    w.start(p.m, kv_first, kv_chunks, -1, 1);
+  // K/V tiles of an item in ring order: chunks r, r-1, ..., r-cp+1 (mod cp), or one
+  // chunk; every role walks the same list and skips the tiles the causal mask hides
+  auto walk_start = [&](TileWalk& w, const Item& it) {
+    w.start(p.m, p.q_rank >= 0 ? p.kv_rank : it.rank, p.q_rank >= 0 ? 1 : p.m.cp, -1, 1);
     while (!w.done() && classify(it.pos0, w.pos()) == kEmpty) w.next();
   };
-  auto walk_next = [&](TileWalk& w) {
+  auto walk_next = [&](TileWalk& w, const Item& it) {
     do w.next(); while (!w.done() && classify(it.pos0, w.pos()) == kEmpty);
   };
 
@@ -203,38 +222,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   regs_ctl();  // warpgroup 0: TMA producers (warps 0, 3) and MMA issuers (warps 1, 2)
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ producers
+    // warp 0: each item's Q tile, then its K tiles; warp 3: the V tiles
     if (lane == 0) {
       const bool is_k = warp == 0;
       const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
       tma_prefetch_desc(tm);
-      bool q_issued = false;
-      if (is_k && !p.debug_fault) {  // fault hook: the Q load never happens
-        tma_prefetch_desc(&tm_q);
-        mbar_expect_tx(q_full, L::kTileBytes);
-        const int row = (it.b * p.Hq + it.h) * p.T + it.slot0;
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, row, q_full);
-        q_issued = true;
-      }
+      if (is_k) tma_prefetch_desc(&tm_q);
       const int nst = is_k ? KS : VS;
       const uint32_t base = sbase + (is_k ? L::kK : L::kV);
-      int stage = 0, par = 0;
+      int stage = 0, par = 0, q_last = -1;
       uint32_t issued = 0, issued_par = 0;  // bit s: stage s loaded / its phase parity
-      TileWalk wk;
-      for (walk_start(wk); !wk.done(); walk_next(wk)) {
-        const uint32_t empty = is_k ? k_empty(stage) : v_empty(stage);
-        const uint32_t full = is_k ? k_full(stage) : v_full(stage);
-        if (!mbar_wait(empty, par ^ 1, abort, p.status, tmo)) break;
-        const int row = kv_row_base + wk.slot();
-        mbar_expect_tx(full, L::kTileBytes);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(base + stage * L::kTileBytes + kb * (kTile * 128), tm, kb * 64, row, full);
-        issued |= 1u << stage;
-        issued_par = (issued_par & ~(1u << stage)) | ((uint32_t)par << stage);
-        if (++stage == nst) stage = 0, par ^= 1;
+      bool ok = true;
+      int w;
+      for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
+        const Item it = decode(p, w);
+        const int kv_row_base = (it.b * p.Hkv + it.g) * p.T;
+        if (is_k) {
+          // the Q buffer is free once the last S of the previous item has read it
+          if (k > 0 && !(ok = mbar_wait(q_empty, (k - 1) & 1, abort, p.status, tmo))) break;
+          if (!(k == 0 && p.debug_fault)) {  // fault hook: the first Q load never happens
+            mbar_expect_tx(q_full, L::kTileBytes);
+            const int row = (it.b * p.Hq + it.h) * p.T + it.slot0;
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, row, q_full);
+            q_last = k;
+          }
+        }
+        TileWalk wk;
+        for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+          const uint32_t empty = is_k ? k_empty(stage) : v_empty(stage);
+          const uint32_t full = is_k ? k_full(stage) : v_full(stage);
+          if (!(ok = mbar_wait(empty, par ^ 1, abort, p.status, tmo))) break;
+          const int row = kv_row_base + wk.slot();
+          mbar_expect_tx(full, L::kTileBytes);
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(base + stage * L::kTileBytes + kb * (kTile * 128), tm, kb * 64, row, full);
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | ((uint32_t)par << stage);
+          if (++stage == nst) stage = 0, par ^= 1;
+        }
       }
       // never leave with a copy still writing into this CTA's shared memory
-      if (q_issued) drain_wait(q_full, 0);
+      if (q_last >= 0) drain_wait(q_full, q_last & 1);
       for (int st = 0; st < nst; ++st)
         if ((issued >> st) & 1u)
           drain_wait(is_k ? k_full(st) : v_full(st), (issued_par >> st) & 1u);
@@ -244,31 +273,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
-      bool ok = mbar_wait(q_full, 0, abort, p.status, tmo);
-      tc_fence_after();
       // descriptor bases; per k-step offsets are compile-time constants (16-byte units)
       const uint64_t qd = sdesc_sw128(sbase + L::kQ, 16, 1024);
       const uint64_t kd0 = sdesc_sw128(sbase + L::kK, 16, 1024);
       StageRing<KS> kr;
-      int j = 0;
-      TileWalk wk;
-      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        const int b = j & 1;
-        if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
-        // buffer b is free once PV of tile j-2 has read the P stored there
-        if (j >= 2 && !(ok = mbar_wait(pv_done(b), ((j - 2) >> 1) & 1, abort, p.status, tmo)))
-          break;
-        tc_fence_after();
-        const uint64_t kd = kd0 + (uint64_t)(kr.stage * kTileDesc);
+      int g = 0;  // tiles so far over all items: buffer g&1, its phase (g>>1)&1
+      bool ok = true;
+      int w;
+      for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
+        const Item it = decode(p, w);
+        if (!(ok = mbar_wait(q_full, k & 1, abort, p.status, tmo))) break;
+        TileWalk wk;
+        for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+          const int b = g & 1;
+          if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
+          // buffer b is free once PV of tile g-2 has read the P stored there
+          if (g >= 2 && !(ok = mbar_wait(pv_done(b), ((g - 2) >> 1) & 1, abort, p.status, tmo)))
+            break;
+          tc_fence_after();
+          const uint64_t kd = kd0 + (uint64_t)(kr.stage * kTileDesc);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KiB blocks, 32 B steps
-          mma_ss(tmem + b * 128, qd + off, kd + off, kIdescS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KiB blocks, 32 B steps
+            mma_ss(tmem + b * 128, qd + off, kd + off, kIdescS, kk > 0);
+          }
+          mma_commit(s_full(b));
+          mma_commit(k_empty(kr.stage));
+          kr.advance();
+          ++g;
         }
-        mma_commit(s_full(b));
-        mma_commit(k_empty(kr.stage));
-        kr.advance();
-        ++j;
+        if (!ok) break;
+        mma_commit(q_empty);  // the Q buffer may take the next item's tile
       }
       // every MMA this thread issued has finished before TMEM can be freed
       mma_commit(final_s);
@@ -281,27 +316,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
       const uint64_t vd0 = sdesc_sw128(sbase + L::kV, kTile * 128, 1024);
       StageRing<VS> vr;
+      int g = 0;
       bool ok = true;
-      int j = 0;
-      TileWalk wk;
-      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        const int b = j & 1;
-        if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
-        const uint64_t vd = vd0 + (uint64_t)(vr.stage * kTileDesc);
-        for (int h = 0; h < 2 && ok; ++h) {
-          // O_h += P_h V_h: keys [64h, 64h+64), 16 key rows = 2048 B per k-step
-          if (!(ok = mbar_wait(p_full(b, h), (j >> 1) & 1, abort, p.status, tmo))) break;
-          tc_fence_after();
+      int w;
+      for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
+        const Item it = decode(p, w);
+        int t = 0;  // tile of this item
+        TileWalk wk;
+        for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+          const int b = g & 1;
+          if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
+          // the first PV of an item overwrites O: the previous item's epilogue has read it
+          if (t == 0 && k > 0 && !(ok = mbar_wait(o_free, (k - 1) & 1, abort, p.status, tmo)))
+            break;
+          const uint64_t vd = vd0 + (uint64_t)(vr.stage * kTileDesc);
+          for (int h = 0; h < 2 && ok; ++h) {
+            // O_h += P_h V_h: keys [64h, 64h+64), 16 key rows = 2048 B per k-step
+            if (!(ok = mbar_wait(p_full(b, h), (g >> 1) & 1, abort, p.status, tmo))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + 256 + h * D, tmem + b * 128 + h * 64 + kk * 8,
-                   vd + (uint64_t)((h * 4 + kk) * 128), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + 256 + h * D, tmem + b * 128 + h * 64 + kk * 8,
+                     vd + (uint64_t)((h * 4 + kk) * 128), kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          mma_commit(pv_done(b));
+          mma_commit(v_empty(vr.stage));
+          vr.advance();
+          ++g;
+          ++t;
         }
-        if (!ok) break;
-        mma_commit(pv_done(b));
-        mma_commit(v_empty(vr.stage));
-        vr.advance();
-        ++j;
       }
       mma_commit(final_pv);
       drain_wait(final_pv, 0);
@@ -316,107 +360,113 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_o = tmem + lane_off + 256 + half * D;
     const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
-    float m_run = -INFINITY, l_run = 0.f;
-    int cnt = 0;
+    int g = 0;
     bool ok = true;
-    TileWalk wk;
-    for (walk_start(wk); !wk.done(); walk_next(wk)) {
-      const int kpos = wk.pos();
-      const int cls = classify(it.pos0, kpos);
-      const int b = cnt & 1;
-      const uint32_t t_s = tmem + lane_off + b * 128 + half * 64;
-      if (!(ok = warp_wait(s_full(b), (cnt >> 1) & 1, abort, p.status, tmo))) break;
-      tc_fence_after();
-      uint32_t r[2][32];
-      tmem_ld32(t_s, r[0]);
-      tmem_ld32(t_s + 32, r[1]);
-      tmem_wait_ld();
-      if (cls == kDiag) {
-        // key column j of this half is visible iff kpos + 64 half + j <= qpos + row
-        const int thr = row + it.pos0 - kpos - half * 64;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j > thr) r[c][j] = __float_as_uint(-INFINITY);
-      }
-      float mx;
-      {
-        // 4 independent chains of three-input max over the 64 scores
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            m4[(c * 16 + j / 2) & 3] = max3(m4[(c * 16 + j / 2) & 3], __uint_as_float(r[c][j]),
-                                            __uint_as_float(r[c][j + 1]));
-        mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
-      }
-      const float m_new = fmaxf(m_run, mx * p.scale_log2);
-      bool rescale = false;
-      float factor = 1.f;
-      if (cnt == 0) {
-        m_run = m_new;
-      } else if (m_new > m_run + 8.f) {
-        factor = ex2(m_run - m_new);
-        l_run *= factor;
-        m_run = m_new;
-        rescale = true;
-      }
-      const float mu = m_run == -INFINITY ? 0.f : m_run;
-      // P = 2^(s * scale * log2e - m): exponent arguments and row sums two lanes per
-      // instruction (packed fp32x2), 2^x on the special-function unit
-      const float2 nmu = make_float2(-mu, -mu);
-      float2 l4[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 x = fma2(make_float2(__uint_as_float(r[c][2 * j]),
-                                            __uint_as_float(r[c][2 * j + 1])), sl2v, nmu);
-          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-          l4[j & 3] = add2(l4[j & 3], pp);
-          pk[j] = pack_bf16(pp.x, pp.y);
-        }
-        tmem_st16(t_s + c * 16, pk);
-      }
-      l_run += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
-      tmem_wait_st();
-      if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O_h so far must be final in TMEM before it is rescaled
-        if (!(ok = warp_wait(pv_done((cnt - 1) & 1), ((cnt - 1) >> 1) & 1, abort, p.status, tmo)))
-          break;
+    int w;
+    for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
+      const Item it = decode(p, w);
+      float m_run = -INFINITY, l_run = 0.f;
+      int cnt = 0;  // tiles of this item
+      TileWalk wk;
+      for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+        const int kpos = wk.pos();
+        const int cls = classify(it.pos0, kpos);
+        const int b = g & 1;
+        const uint32_t t_s = tmem + lane_off + b * 128 + half * 64;
+        if (!(ok = warp_wait(s_full(b), (g >> 1) & 1, abort, p.status, tmo))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o32[32];
-          tmem_ld32(t_o + c * 32, o32);
-          tmem_wait_ld();
+        uint32_t r[2][32];
+        tmem_ld32(t_s, r[0]);
+        tmem_ld32(t_s + 32, r[1]);
+        tmem_wait_ld();
+        if (cls == kDiag) {
+          // key column j of this half is visible iff kpos + 64 half + j <= qpos + row
+          const int thr = row + it.pos0 - kpos - half * 64;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * factor);
-          tmem_st32(t_o + c * 32, o32);
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c * 32 + j > thr) r[c][j] = __float_as_uint(-INFINITY);
         }
+        float mx;
+        {
+          // 4 independent chains of three-input max over the 64 scores
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+              m4[(c * 16 + j / 2) & 3] = max3(m4[(c * 16 + j / 2) & 3], __uint_as_float(r[c][j]),
+                                              __uint_as_float(r[c][j + 1]));
+          mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+        }
+        const float m_new = fmaxf(m_run, mx * p.scale_log2);
+        bool rescale = false;
+        float factor = 1.f;
+        if (cnt == 0) {
+          m_run = m_new;
+        } else if (m_new > m_run + 8.f) {
+          factor = ex2(m_run - m_new);
+          l_run *= factor;
+          m_run = m_new;
+          rescale = true;
+        }
+        const float mu = m_run == -INFINITY ? 0.f : m_run;
+        // P = 2^(s * scale * log2e - m): exponent arguments and row sums two lanes per
+        // instruction (packed fp32x2), 2^x on the special-function unit
+        const float2 nmu = make_float2(-mu, -mu);
+        float2 l4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 x = fma2(make_float2(__uint_as_float(r[c][2 * j]),
+                                              __uint_as_float(r[c][2 * j + 1])), sl2v, nmu);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            l4[j & 3] = add2(l4[j & 3], pp);
+            pk[j] = pack_bf16(pp.x, pp.y);
+          }
+          tmem_st16(t_s + c * 16, pk);
+        }
+        l_run += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
         tmem_wait_st();
+        if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O_h so far must be final in TMEM before it is rescaled
+          if (!(ok = warp_wait(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.status, tmo)))
+            break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o32[32];
+            tmem_ld32(t_o + c * 32, o32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o32[j] = __float_as_uint(__uint_as_float(o32[j]) * factor);
+            tmem_st32(t_o + c * 32, o32);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(p_full(b, half));
+        ++cnt;
+        ++g;
       }
-      tc_fence_before();
-      mbar_arrive(p_full(b, half));
-      ++cnt;
-    }
-    // -------------------------------------------------------- epilogue
-    if (ok && cnt > 0)
-      ok = warp_wait(pv_done((cnt - 1) & 1), ((cnt - 1) >> 1) & 1, abort, p.status, tmo);
-    // The two halves' (m, l) meet in shared memory, in the Q tile's space: its load
-    // has landed (q_full) and its last reader, S of the last tile, completed before
-    // the softmax of that tile began.  Both warps of the pair always reach the barrier.
-    if (ok) ok = warp_wait(q_full, 0, abort, p.status, tmo);
-    float2* xch = reinterpret_cast<float2*>(smem + L::kQ);
-    if (ok) xch[half * 128 + row] = make_float2(m_run, l_run);
-    pair_sync(quad);
-    const float2 other = xch[(1 - half) * 128 + row];
-    if (ok) {
+      if (!ok) break;
+      // ------------------------------------------------------ epilogue of the item
+      if (cnt > 0 && !(ok = warp_wait(pv_done((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.status,
+                                      tmo)))
+        break;
+      // the two halves' (m, l) meet in shared memory; the slot is free once the
+      // partner has read the previous item's value
+      if (k > 0 && !(ok = warp_wait(xch_free, (k - 1) & 1, abort, p.status, tmo))) break;
+      xch[half * 128 + row] = make_float2(m_run, l_run);
+      mbar_arrive(xch_full);
+      if (!(ok = warp_wait(xch_full, k & 1, abort, p.status, tmo))) break;
+      const float2 other = xch[(1 - half) * 128 + row];
+      mbar_arrive(xch_free);
       tc_fence_after();
       const float m0 = half == 0 ? m_run : other.x, l0 = half == 0 ? l_run : other.y;
       const float m1 = half == 0 ? other.x : m_run, l1 = half == 0 ? other.y : l_run;
@@ -466,6 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (half == 0) p.lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * kLn2 : -INFINITY;
+      // O has been read: the next item's first PV may overwrite it
+      tc_fence_before();
+      mbar_arrive(o_free);
     }
   }
 
@@ -501,7 +554,13 @@ static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   if ((e = check_register_split(kern, tcfwd::kThreads)) != cudaSuccess) return e;
-  kern<<<items, tcfwd::kThreads, kSmem, st>>>(tq, tk, tv, p);
+  // persistent: at most one resident CTA per SM, each walking its share of the items
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int grid = items < sms ? items : sms;
+  kern<<<grid, tcfwd::kThreads, kSmem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -525,6 +584,7 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
   p.debug_fault = R.debug_fault;
   const int items = R.B * R.Hq * p.q_tiles;
   if (items == 0) return cudaSuccess;
+  p.n_items = items;
   timing_begin(partial ? "tc_partial_fwd" : "tc_ring_fwd", st);
   cudaError_t e;
   if (R.D == 128)
