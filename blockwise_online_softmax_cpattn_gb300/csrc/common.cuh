@@ -112,6 +112,15 @@ struct StageRing {
   __device__ __forceinline__ uint32_t issued_parity(int st) const { return (ipar >> st) & 1u; }
 };
 
+// The k-th work item of a persistent CTA, or -1: resident CTAs walk a
+// heaviest-first item list in a snake (rounds of gridDim.x items, every other
+// round reversed), which evens out the per-CTA totals.
+__device__ __forceinline__ int item_of(int k, int n_items) {
+  const int G = gridDim.x;
+  const int w = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return w < n_items ? w : -1;
+}
+
 __device__ __forceinline__ void latch_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

@@ -431,12 +431,21 @@ struct DqSmem {
   static constexpr int kK = 2 * kTB;
   static constexpr int kV = kK + kKStages * kTB;
   static constexpr int kBar = kV + kVStages * kTB;
-  // qdo_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full, s_free,
-  // dp_full[2], ds_full[2] (one per dP buffer), dq_done[2], final_q (dQ issuer),
-  // final_s (S issuer), final_p (dP issuer)
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 11;
+  // qdo_full, qdo_empty (released by the S and the dP issuer), k_full[KS], k_empty[KS],
+  // v_full[VS], v_empty[VS], s_full, s_free, dp_full[2], ds_full[2] (one per dP
+  // buffer), dq_done[2], dq_free, final_q (dQ issuer), final_s (S issuer), final_p
+  // (dP issuer)
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 12;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16 + 1024;
+};
+
+// One work item of the dQ kernel: a 128-row query tile of one (batch, head), the
+// latest query positions (the most keys) first.
+struct DqItem {
+  int b, h, g, qpos0, qslot0, r_own;
+  int64_t qrow;
+  int kv_row_base;
 };
 
 template <int D>
@@ -453,20 +462,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::kBar;
   const uint32_t qdo_full = bars;
-  auto k_full = [&](int s) { return bars + 8 * (1 + s); };
-  auto k_empty = [&](int s) { return bars + 8 * (1 + KS + s); };
-  auto v_full = [&](int s) { return bars + 8 * (1 + 2 * KS + s); };
-  auto v_empty = [&](int s) { return bars + 8 * (1 + 2 * KS + VS + s); };
-  const uint32_t s_full = bars + 8 * (1 + 2 * KS + 2 * VS);
+  const uint32_t qdo_empty = bars + 8;
+  auto k_full = [&](int s) { return bars + 8 * (2 + s); };
+  auto k_empty = [&](int s) { return bars + 8 * (2 + KS + s); };
+  auto v_full = [&](int s) { return bars + 8 * (2 + 2 * KS + s); };
+  auto v_empty = [&](int s) { return bars + 8 * (2 + 2 * KS + VS + s); };
+  const uint32_t s_full = bars + 8 * (2 + 2 * KS + 2 * VS);
   const uint32_t s_free = s_full + 8;
   // per-buffer barriers: a second arrival on a buffer's barrier needs that buffer
   // to have been recycled, so no waiter can ever be two phases behind
   auto dp_full = [&](int x) { return s_full + 16 + 8 * x; };
   auto ds_full = [&](int x) { return s_full + 32 + 8 * x; };
   auto dq_done = [&](int x) { return s_full + 48 + 8 * x; };
-  const uint32_t final_q = s_full + 64;
-  const uint32_t final_s = s_full + 72;
-  const uint32_t final_p = s_full + 80;
+  const uint32_t dq_free = s_full + 64;
+  const uint32_t final_q = s_full + 72;
+  const uint32_t final_s = s_full + 80;
+  const uint32_t final_p = s_full + 88;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -474,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t b = bars + 8 * i;
-      mbar_init(b, (b == s_free || b == ds_full(0) || b == ds_full(1)) ? 256 : 1);
+      const bool compute_arrivals = b == s_free || b == ds_full(0) || b == ds_full(1) || b == dq_free;
+      mbar_init(b, compute_arrivals ? 256 : b == qdo_empty ? 2 : 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -488,25 +500,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // work item: latest query positions (the most keys) first
-  const int units = p.B * p.Hq;
-  const int ti = blockIdx.x / units;
-  const int rem = blockIdx.x - ti * units;
-  const int b = rem / p.Hq, h = rem - (rem / p.Hq) * p.Hq, g = h / p.n_rep;
+  // Persistent: the CTAs stay resident and walk the items (latest query positions
+  // first) in the order item_of gives; every pipeline keeps running across items.
   const int n_q_tiles = p.T / kTile;
-  const int qpos0 = (n_q_tiles - 1 - ti) * kTile;
-  const int qslot0 = p.m.slot(qpos0);
-  const int r_own = qslot0 / p.m.c;
-  // K/V tiles in ring order (chunks r, r-1, ...), hidden tiles skipped
-  auto walk_start = [&](TileWalk& w) {
-    w.start(p.m, r_own, p.m.cp, -1, 1);
-    while (!w.done() && classify(qpos0, w.pos()) == kEmpty) w.next();
+  const int n_items = p.B * p.Hq * n_q_tiles;
+  auto decode = [&](int w) {
+    DqItem it;
+    const int units = p.B * p.Hq;
+    const int ti = w / units;
+    const int rem = w - ti * units;
+    it.b = rem / p.Hq;
+    it.h = rem - it.b * p.Hq;
+    it.g = it.h / p.n_rep;
+    it.qpos0 = (n_q_tiles - 1 - ti) * kTile;
+    it.qslot0 = p.m.slot(it.qpos0);
+    it.r_own = it.qslot0 / p.m.c;
+    it.qrow = ((int64_t)it.b * p.Hq + it.h) * p.T + it.qslot0;
+    it.kv_row_base = (it.b * p.Hkv + it.g) * p.T;
+    return it;
   };
-  auto walk_next = [&](TileWalk& w) {
-    do w.next(); while (!w.done() && classify(qpos0, w.pos()) == kEmpty);
+  // K/V tiles of an item in ring order (chunks r, r-1, ...), hidden tiles skipped
+  auto walk_start = [&](TileWalk& w, const DqItem& it) {
+    w.start(p.m, it.r_own, p.m.cp, -1, 1);
+    while (!w.done() && classify(it.qpos0, w.pos()) == kEmpty) w.next();
   };
-  const int64_t qrow = ((int64_t)b * p.Hq + h) * p.T + qslot0;
-  const int kv_row_base = (b * p.Hkv + g) * p.T;
+  auto walk_next = [&](TileWalk& w, const DqItem& it) {
+    do w.next(); while (!w.done() && classify(it.qpos0, w.pos()) == kEmpty);
+  };
 
   if (warp < 4) {
   regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2, 3)
@@ -516,32 +536,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_expect_tx(qdo_full, 2 * L::kTB);
-      for (int kb = 0; kb < D / 64; ++kb) {
-        tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)qrow, qdo_full);
-        tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)qrow, qdo_full);
-      }
       StageRing<KS> kr;
       StageRing<VS> vr;
-      TileWalk wk;
-      for (walk_start(wk); !wk.done(); walk_next(wk)) {
-        const int row = kv_row_base + wk.slot();
-        if (!mbar_wait(k_empty(kr.stage), kr.par ^ 1, abort, p.status, kTimeoutNs)) break;
-        mbar_expect_tx(k_full(kr.stage), L::kTB);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kK + kr.stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64, row,
-                      k_full(kr.stage));
-        kr.mark_issued();
-        if (!mbar_wait(v_empty(vr.stage), vr.par ^ 1, abort, p.status, kTimeoutNs)) break;
-        mbar_expect_tx(v_full(vr.stage), L::kTB);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kV + vr.stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64, row,
-                      v_full(vr.stage));
-        vr.mark_issued();
-        kr.advance();
-        vr.advance();
+      int q_last = -1;
+      bool ok = true;
+      int w;
+      for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+        const DqItem it = decode(w);
+        // Q and dO of this item once the S and dP issuers are done with the last one's
+        if (k > 0 && !(ok = mbar_wait(qdo_empty, (k - 1) & 1, abort, p.status, kTimeoutNs))) break;
+        mbar_expect_tx(qdo_full, 2 * L::kTB);
+        for (int kb = 0; kb < D / 64; ++kb) {
+          tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)it.qrow, qdo_full);
+          tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)it.qrow, qdo_full);
+        }
+        q_last = k;
+        TileWalk wk;
+        for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+          const int row = it.kv_row_base + wk.slot();
+          if (!(ok = mbar_wait(k_empty(kr.stage), kr.par ^ 1, abort, p.status, kTimeoutNs))) break;
+          mbar_expect_tx(k_full(kr.stage), L::kTB);
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(sbase + L::kK + kr.stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64, row,
+                        k_full(kr.stage));
+          kr.mark_issued();
+          if (!(ok = mbar_wait(v_empty(vr.stage), vr.par ^ 1, abort, p.status, kTimeoutNs))) break;
+          mbar_expect_tx(v_full(vr.stage), L::kTB);
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(sbase + L::kV + vr.stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64, row,
+                        v_full(vr.stage));
+          vr.mark_issued();
+          kr.advance();
+          vr.advance();
+        }
       }
-      drain_wait(qdo_full, 0);
+      if (q_last >= 0) drain_wait(qdo_full, q_last & 1);
       for (int s = 0; s < KS; ++s)
         if (kr.was_issued(s)) drain_wait(k_full(s), kr.issued_parity(s));
       for (int s = 0; s < VS; ++s)
@@ -556,49 +585,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const bool is_s = warp == 1;
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
-      bool ok = mbar_wait(qdo_full, 0, abort, p.status, kTimeoutNs);
-      tc_fence_after();
       // descriptor bases (16-byte units), K-major
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t ad = sdesc_sw128(sbase + (is_s ? L::kQ : L::kDO), 16, 1024);
       const uint64_t bd0 = sdesc_sw128(sbase + (is_s ? L::kK : L::kV), 16, 1024);
       StageRing<KS> kr;
       StageRing<VS> vr;
-      int j = 0;
-      TileWalk wk;
-      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        uint32_t dst;
-        uint64_t bd;
-        if (is_s) {
-          // S(j): the S region is free once the compute warps have read S(j-1)
-          if (j > 0 && !(ok = mbar_wait(s_free, (j - 1) & 1, abort, p.status, kTimeoutNs))) break;
-          if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, kTimeoutNs))) break;
-          dst = tmem;
-          bd = bd0 + (uint64_t)(kr.stage * kTD);
-        } else {
-          // dP(j) into buffer j&1: free once dQ(j-2) has read the dS stored there
-          if (j >= 2 && !(ok = mbar_wait(dq_done(j & 1), ((j - 2) >> 1) & 1, abort, p.status,
-                                         kTimeoutNs)))
-            break;
-          if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, kTimeoutNs))) break;
-          dst = tmem + 128 + 128 * (j & 1);
-          bd = bd0 + (uint64_t)(vr.stage * kTD);
-        }
-        tc_fence_after();
+      int g = 0;  // tiles so far over all items
+      bool ok = true;
+      int w;
+      for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+        const DqItem it = decode(w);
+        if (!(ok = mbar_wait(qdo_full, k & 1, abort, p.status, kTimeoutNs))) break;
+        TileWalk wk;
+        for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+          uint32_t dst;
+          uint64_t bd;
+          if (is_s) {
+            // S(g): the S region is free once the compute warps have read S(g-1)
+            if (g > 0 && !(ok = mbar_wait(s_free, (g - 1) & 1, abort, p.status, kTimeoutNs))) break;
+            if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, kTimeoutNs))) break;
+            dst = tmem;
+            bd = bd0 + (uint64_t)(kr.stage * kTD);
+          } else {
+            // dP(g) into buffer g&1: free once dQ(g-2) has read the dS stored there
+            if (g >= 2 && !(ok = mbar_wait(dq_done(g & 1), ((g - 2) >> 1) & 1, abort, p.status,
+                                           kTimeoutNs)))
+              break;
+            if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, kTimeoutNs))) break;
+            dst = tmem + 128 + 128 * (g & 1);
+            bd = bd0 + (uint64_t)(vr.stage * kTD);
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+            mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
+          }
+          if (is_s) {
+            mma_commit(s_full);
+          } else {
+            mma_commit(dp_full(g & 1));
+            mma_commit(v_empty(vr.stage));  // V of this tile is not read again
+          }
+          kr.advance();
+          vr.advance();
+          ++g;
         }
-        if (is_s) {
-          mma_commit(s_full);
-        } else {
-          mma_commit(dp_full(j & 1));
-          mma_commit(v_empty(vr.stage));  // V of this tile is not read again
-        }
-        kr.advance();
-        vr.advance();
-        ++j;
+        if (!ok) break;
+        mma_commit(qdo_empty);  // this issuer is done with the item's Q (or dO)
       }
       mma_commit(is_s ? final_s : final_p);
       drain_wait(is_s ? final_s : final_p, 0);
@@ -610,24 +645,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t kd_mn0 = sdesc_sw128(sbase + L::kK, kTile * 128, 1024);
       StageRing<KS> kr;
+      int g = 0;
       bool ok = true;
-      int j = 0;
-      TileWalk wk;
-      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        if (!(ok = mbar_wait(ds_full(j & 1), (j >> 1) & 1, abort, p.status, kTimeoutNs))) break;
-        tc_fence_after();
-        // K(j) landed before S(j), which the compute warps read before storing dS(j)
-        const uint64_t kd_mn = kd_mn0 + (uint64_t)(kr.stage * kTD);
+      int w;
+      for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+        const DqItem it = decode(w);
+        int t = 0;  // tile of this item
+        TileWalk wk;
+        for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+          if (!(ok = mbar_wait(ds_full(g & 1), (g >> 1) & 1, abort, p.status, kTimeoutNs))) break;
+          // the item's first dQ overwrites the accumulator the previous epilogue read
+          if (t == 0 && k > 0 && !(ok = mbar_wait(dq_free, (k - 1) & 1, abort, p.status, kTimeoutNs)))
+            break;
+          tc_fence_after();
+          // K(g) landed before S(g), which the compute warps read before storing dS(g)
+          const uint64_t kd_mn = kd_mn0 + (uint64_t)(kr.stage * kTD);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acol = 128 + 128 * (j & 1) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t acol = 128 + 128 * (g & 1) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+            mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(dq_done(g & 1));  // the dS buffer may take dP(g+2)
+          // both S(g) and dQ(g) have read K(g) once dQ(g) completes
+          mma_commit(k_empty(kr.stage));
+          kr.advance();
+          ++g;
+          ++t;
         }
-        mma_commit(dq_done(j & 1));  // the dS buffer may take dP(j+2)
-        // both S(j) and dQ(j) have read K(j) once dQ(j) completes
-        mma_commit(k_empty(kr.stage));
-        kr.advance();
-        ++j;
       }
       mma_commit(final_q);
       drain_wait(final_q, 0);
@@ -639,73 +683,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;  // query row of the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + half * 64;
-    const float2 nl2 = make_float2(p.lse2[qrow + row], p.lse2[qrow + row]);  // -LSE log2e
-    const float2 ndl = make_float2(p.delta[qrow + row], p.delta[qrow + row]);  // -Delta
     const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
-    int j = 0;
+    int g = 0;
     bool ok = true;
-    TileWalk wk;
-    for (walk_start(wk); !wk.done(); walk_next(wk)) {
-      const int kpos0 = wk.pos();
-      const int cls = classify(qpos0, kpos0);
-      if (!(ok = warp_wait(s_full, j & 1, abort, p.status))) break;
-      tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(t_s, sr[0]);
-      tmem_ld32(t_s + 32, sr[1]);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(s_free);
-      // key column j (of this half) is visible iff kpos0 + 64*half + j <= qpos0 + row
-      const int thr = qpos0 + row - kpos0 - half * 64;
-      float pr[64];
+    int w;
+    for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+      const DqItem it = decode(w);
+      const float2 nl2 = make_float2(p.lse2[it.qrow + row], p.lse2[it.qrow + row]);  // -LSE log2e
+      const float2 ndl = make_float2(p.delta[it.qrow + row], p.delta[it.qrow + row]);  // -Delta
+      int cnt = 0;  // tiles of this item
+      TileWalk wk;
+      for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
+        const int kpos0 = wk.pos();
+        const int cls = classify(it.qpos0, kpos0);
+        if (!(ok = warp_wait(s_full, g & 1, abort, p.status))) break;
+        tc_fence_after();
+        uint32_t sr[2][32];
+        tmem_ld32(t_s, sr[0]);
+        tmem_ld32(t_s + 32, sr[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_free);
+        // key column j (of this half) is visible iff kpos0 + 64*half + j <= qpos0 + row
+        const int thr = it.qpos0 + row - kpos0 - half * 64;
+        float pr[64];
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int jj = 0; jj < 32; jj += 2) {
-          const int j0 = c * 32 + jj;
-          const float2 x = fma2(make_float2(__uint_as_float(sr[c][jj]), __uint_as_float(sr[c][jj + 1])),
-                                sl2v, nl2);
-          float p0 = ex2(x.x), p1 = ex2(x.y);
-          if (cls == kDiag) {
-            if (j0 > thr) p0 = 0.f;
-            if (j0 + 1 > thr) p1 = 0.f;
+          for (int jj = 0; jj < 32; jj += 2) {
+            const int j0 = c * 32 + jj;
+            const float2 x = fma2(make_float2(__uint_as_float(sr[c][jj]), __uint_as_float(sr[c][jj + 1])),
+                                  sl2v, nl2);
+            float p0 = ex2(x.x), p1 = ex2(x.y);
+            if (cls == kDiag) {
+              if (j0 > thr) p0 = 0.f;
+              if (j0 + 1 > thr) p1 = 0.f;
+            }
+            pr[j0] = p0;
+            pr[j0 + 1] = p1;
           }
-          pr[j0] = p0;
-          pr[j0 + 1] = p1;
-        }
-      if (!(ok = warp_wait(dp_full(j & 1), (j >> 1) & 1, abort, p.status))) break;
-      tc_fence_after();
-      const uint32_t t_dp = tmem + lane_off + 128 + 128 * (j & 1) + half * 64;
-      tmem_ld32(t_dp, sr[0]);
-      tmem_ld32(t_dp + 32, sr[1]);
-      tmem_wait_ld();
+        if (!(ok = warp_wait(dp_full(g & 1), (g >> 1) & 1, abort, p.status))) break;
+        tc_fence_after();
+        const uint32_t t_dp = tmem + lane_off + 128 + 128 * (g & 1) + half * 64;
+        tmem_ld32(t_dp, sr[0]);
+        tmem_ld32(t_dp + 32, sr[1]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int jj = 0; jj < 32; jj += 2) {
-          const int j0 = c * 32 + jj;
-          const float2 d = mul2(make_float2(pr[j0], pr[j0 + 1]),
-                                add2(make_float2(__uint_as_float(sr[c][jj]),
-                                                 __uint_as_float(sr[c][jj + 1])), ndl));
-          pk[jj >> 1] = pack_bf16(d.x, d.y);
+          for (int jj = 0; jj < 32; jj += 2) {
+            const int j0 = c * 32 + jj;
+            const float2 d = mul2(make_float2(pr[j0], pr[j0 + 1]),
+                                  add2(make_float2(__uint_as_float(sr[c][jj]),
+                                                   __uint_as_float(sr[c][jj + 1])), ndl));
+            pk[jj >> 1] = pack_bf16(d.x, d.y);
+          }
+          tmem_st16(t_dp + c * 16, pk);
         }
-        tmem_st16(t_dp + c * 16, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(ds_full(g & 1));
+        ++cnt;
+        ++g;
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(ds_full(j & 1));
-      ++j;
-    }
-    if (ok && j > 0) ok = warp_wait(dq_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.status);
-    if (ok) {
+      if (!ok) break;
+      if (cnt > 0 &&
+          !(ok = warp_wait(dq_done((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.status)))
+        break;
       tc_fence_after();
-      __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(p.out0) + (qrow + row) * D + half * (D / 2);
+      __nv_bfloat16* dq =
+          static_cast<__nv_bfloat16*>(p.out0) + (it.qrow + row) * D + half * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v32[32];
-        if (j > 0) {
+        if (cnt > 0) {
           tmem_ld32(tmem + lane_off + kDqCol + half * (D / 2) + c * 32, v32);
           tmem_wait_ld();
         } else {
@@ -714,6 +766,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         store_row32_bf16(dq + c * 32, v32, p.scale);
       }
+      // the accumulator has been read: the next item's first dQ may overwrite it
+      tc_fence_before();
+      mbar_arrive(dq_free);
     }
   }
 
@@ -760,8 +815,13 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   e = prep(dq_kernel<D>, DqSmem<D>::kBytes);
   if (e != cudaSuccess) return e;
   const int q_items = R.B * R.Hq * (R.T / kTile);
+  // persistent: at most one resident CTA per SM, each walking its share of the items
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
   timing_begin("tc_bwd_dq", st);
-  dq_kernel<D><<<q_items, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
+  dq_kernel<D><<<q_items < sms ? q_items : sms, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
   e = cudaGetLastError();
   timing_end(st);
   return e;

@@ -123,15 +123,6 @@ __device__ __forceinline__ Item decode(const Params& p, int w) {
   return it;
 }
 
-// The k-th work item of this CTA, or -1: the CTAs stay resident and walk the
-// heaviest-first item list in a snake (rounds of gridDim.x items, every other
-// round reversed), which evens out the per-CTA totals.
-__device__ __forceinline__ int item_of(int k, int n_items) {
-  const int G = gridDim.x;
-  const int w = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-  return w < n_items ? w : -1;
-}
-
 __device__ __forceinline__ int classify(int qpos0, int kpos0) {
   if (kpos0 + kTile - 1 <= qpos0) return kFull;
   if (kpos0 > qpos0 + kTile - 1) return kEmpty;
