@@ -89,21 +89,27 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
 // ===========================================================================
 template <int D>
 struct DkdvSmem {
-  static constexpr int kStages = 2;
+  // K and V stationary.  Q and dO in rings of their own, each stage with its
+  // per-query statistics (-LSE log2e with Q, -Delta with dO): Q has the extra stage
+  // because S^T, its first reader, runs a tile ahead of everything else.  No
+  // alignment slack: the kernel declares its dynamic shared memory 1024-byte
+  // aligned and checks it.
+  static constexpr int kQStages = 3;
+  static constexpr int kDOStages = 2;
   static constexpr int kTB = kTile * D * 2;
   static constexpr int kK = 0;
   static constexpr int kV = kTB;
   static constexpr int kQ = 2 * kTB;
-  static constexpr int kDO = kQ + kStages * kTB;
-  static constexpr int kLse = kDO + kStages * kTB;
-  static constexpr int kDelta = kLse + kStages * 512;
-  static constexpr int kBar = kDelta + kStages * 512;
-  // kv_full, q_full[S], do_full[S], qdo_empty[S], s_full, dp_full, p_full,
-  // ds_full, dv_done, dk_done, final (gradient issuer), final_s (S^T issuer),
-  // final_p (dP^T issuer)
-  static constexpr int kNumBars = 1 + 3 * kStages + 9;
+  static constexpr int kDO = kQ + kQStages * kTB;
+  static constexpr int kLse = kDO + kDOStages * kTB;
+  static constexpr int kDelta = kLse + kQStages * 512;
+  static constexpr int kBar = kDelta + kDOStages * 512;
+  // kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], s_full, s_free,
+  // dp_full, p_full, ds_full, dk_done, final (gradient issuer), final_s (S^T
+  // issuer), final_p (dP^T issuer)
+  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16 + 1024;
+  static constexpr int kBytes = kMisc + 16;
 };
 
 template <int D>
@@ -112,22 +118,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const Params p) {
   using L = DkdvSmem<D>;
-  constexpr int S = L::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  constexpr int QS = L::kQStages, DS = L::kDOStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the layout has no alignment slack
+    if (threadIdx.x == 0) latch_status(p.status, kStatusLaunch);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::kBar;
   const uint32_t kv_full = bars;
   auto q_full = [&](int s) { return bars + 8 * (1 + s); };
-  auto do_full = [&](int s) { return bars + 8 * (1 + S + s); };
-  auto qdo_empty = [&](int s) { return bars + 8 * (1 + 2 * S + s); };
-  const uint32_t s_full = bars + 8 * (1 + 3 * S);
-  const uint32_t dp_full = s_full + 8;
-  const uint32_t p_full = s_full + 16;
-  const uint32_t ds_full = s_full + 24;
-  const uint32_t dv_done = s_full + 32;
-  const uint32_t dk_done = s_full + 40;
+  auto q_empty = [&](int s) { return bars + 8 * (1 + QS + s); };
+  auto do_full = [&](int s) { return bars + 8 * (1 + 2 * QS + s); };
+  auto do_empty = [&](int s) { return bars + 8 * (1 + 2 * QS + DS + s); };
+  const uint32_t s_full = bars + 8 * (1 + 2 * QS + 2 * DS);
+  const uint32_t s_free = s_full + 8;
+  const uint32_t dp_full = s_full + 16;
+  const uint32_t p_full = s_full + 24;
+  const uint32_t ds_full = s_full + 32;
+  const uint32_t dk_done = s_full + 40;  // dV and dK of the tile done: the dP region is free
   const uint32_t final_bar = s_full + 48;
   const uint32_t final_s = s_full + 56;
   const uint32_t final_p = s_full + 64;
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t b = bars + 8 * i;
-      mbar_init(b, (b == p_full || b == ds_full) ? 256 : 1);
+      mbar_init(b, (b == s_free || b == p_full || b == ds_full) ? 256 : 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -161,8 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kslot0 = p.m.slot(kpos0);
   const int s_own = kslot0 / p.m.c;
   // query tiles in the order the chunk's gradient travels the ring back to its
-  // owner: ranks s, s+1, ..., s-1; every query head of the group per rank
-  auto walk_start = [&](TileWalk& w) { w.start(p.m, s_own, p.m.cp, +1, p.n_rep); };
+  // owner: ranks s, s+1, ..., s-1; every query head of the group per rank; tiles
+  // that cannot see this K/V tile are skipped by every role alike
+  auto walk_start = [&](TileWalk& w) {
+    w.start(p.m, s_own, p.m.cp, +1, p.n_rep);
+    while (!w.done() && classify(w.pos(), kpos0) == kEmpty) w.next();
+  };
+  auto walk_next = [&](TileWalk& w) {
+    do w.next(); while (!w.done() && classify(w.pos(), kpos0) == kEmpty);
+  };
 
   if (warp < 4) {
   regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2, 3)
@@ -178,33 +195,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sbase + L::kK + kb * (kTile * 128), &tm_k, kb * 64, krow, kv_full);
         tma_load_2d(sbase + L::kV + kb * (kTile * 128), &tm_v, kb * 64, krow, kv_full);
       }
-      int stage = 0, par = 0;
-      uint32_t issued = 0, ipar = 0;  // bit s: stage s loaded / its phase parity
+      StageRing<QS> qr;
+      StageRing<DS> dr;
       TileWalk wk;
-      for (walk_start(wk); !wk.done(); wk.next()) {
-        if (classify(wk.pos(), kpos0) == kEmpty) continue;
-        if (!mbar_wait(qdo_empty(stage), par ^ 1, abort, p.status, kTimeoutNs)) break;
+      for (walk_start(wk); !wk.done(); walk_next(wk)) {
         const int qrow = (b * p.Hq + g * p.n_rep + wk.rep) * p.T + wk.slot();
-        mbar_expect_tx(q_full(stage), L::kTB + 1024);
+        if (!mbar_wait(q_empty(qr.stage), qr.par ^ 1, abort, p.status, kTimeoutNs)) break;
+        mbar_expect_tx(q_full(qr.stage), L::kTB + 512);
         for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kQ + stage * L::kTB + kb * (kTile * 128), &tm_q, kb * 64, qrow,
-                      q_full(stage));
-        bulk_load(sbase + L::kLse + stage * 512, p.lse2 + qrow, 512, q_full(stage));
-        bulk_load(sbase + L::kDelta + stage * 512, p.delta + qrow, 512, q_full(stage));
-        mbar_expect_tx(do_full(stage), L::kTB);
+          tma_load_2d(sbase + L::kQ + qr.stage * L::kTB + kb * (kTile * 128), &tm_q, kb * 64, qrow,
+                      q_full(qr.stage));
+        bulk_load(sbase + L::kLse + qr.stage * 512, p.lse2 + qrow, 512, q_full(qr.stage));
+        qr.mark_issued();
+        if (!mbar_wait(do_empty(dr.stage), dr.par ^ 1, abort, p.status, kTimeoutNs)) break;
+        mbar_expect_tx(do_full(dr.stage), L::kTB + 512);
         for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kDO + stage * L::kTB + kb * (kTile * 128), &tm_do, kb * 64, qrow,
-                      do_full(stage));
-        issued |= 1u << stage;
-        ipar = (ipar & ~(1u << stage)) | ((uint32_t)par << stage);
-        if (++stage == S) stage = 0, par ^= 1;
+          tma_load_2d(sbase + L::kDO + dr.stage * L::kTB + kb * (kTile * 128), &tm_do, kb * 64,
+                      qrow, do_full(dr.stage));
+        bulk_load(sbase + L::kDelta + dr.stage * 512, p.delta + qrow, 512, do_full(dr.stage));
+        dr.mark_issued();
+        qr.advance();
+        dr.advance();
       }
       drain_wait(kv_full, 0);
-      for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u) {
-          drain_wait(q_full(s), (ipar >> s) & 1u);
-          drain_wait(do_full(s), (ipar >> s) & 1u);
-        }
+      for (int s = 0; s < QS; ++s)
+        if (qr.was_issued(s)) drain_wait(q_full(s), qr.issued_parity(s));
+      for (int s = 0; s < DS; ++s)
+        if (dr.was_issued(s)) drain_wait(do_full(s), dr.issued_parity(s));
     }
   } else if (warp == 1 || warp == 3) {
     if (lane == 0) {
@@ -222,20 +239,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ad = sdesc_sw128(sbase + (is_s ? L::kK : L::kV), 16, 1024);
       const uint64_t bd0 = sdesc_sw128(sbase + (is_s ? L::kQ : L::kDO), 16, 1024);
       const uint32_t dst = tmem + (is_s ? 0 : 128);
-      int stage = 0, par = 0, cnt = 0;
+      StageRing<QS> qr;
+      StageRing<DS> dr;
+      int cnt = 0;
       TileWalk wk;
-      for (walk_start(wk); !wk.done() && ok; wk.next()) {
-        if (classify(wk.pos(), kpos0) == kEmpty) continue;
-        // S^T: the S region is free once the previous dV has read P^T;
-        // dP^T: the dP region is free once the previous dK has read dS^T
-        if (!(ok = mbar_wait(is_s ? q_full(stage) : do_full(stage), par, abort, p.status,
-                             kTimeoutNs)))
+      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
+        const int st = is_s ? qr.stage : dr.stage;
+        // S^T: the S region is free once the compute warps have loaded the previous
+        // S^T; dP^T: the dP region is free once dV and dK of the previous tile have
+        // read the P^T and dS^T stored there
+        if (!(ok = mbar_wait(is_s ? q_full(st) : do_full(st), is_s ? qr.par : dr.par, abort,
+                             p.status, kTimeoutNs)))
           break;
-        if (cnt > 0 && !(ok = mbar_wait(is_s ? dv_done : dk_done, (cnt - 1) & 1, abort, p.status,
+        if (cnt > 0 && !(ok = mbar_wait(is_s ? s_free : dk_done, (cnt - 1) & 1, abort, p.status,
                                         kTimeoutNs)))
           break;
         tc_fence_after();
-        const uint64_t bd = bd0 + (uint64_t)(stage * kTD);
+        const uint64_t bd = bd0 + (uint64_t)(st * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
@@ -243,51 +263,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(is_s ? s_full : dp_full);
         ++cnt;
-        if (++stage == S) stage = 0, par ^= 1;
+        qr.advance();
+        dr.advance();
       }
       mma_commit(is_s ? final_s : final_p);
       drain_wait(is_s ? final_s : final_p, 0);
     }
   } else if (warp == 2) {
     if (lane == 0) {
-      // Gradient issuer: dV += P^T dO and dK += dS^T Q (TS, P^T / dS^T in TMEM,
-      // Q / dO MN-major from shared memory)
+      // Gradient issuer: dV += P^T dO and dK += dS^T Q (TS: P^T and dS^T in the dP
+      // region of TMEM, Q / dO MN-major from shared memory)
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQ, kTile * 128, 1024);
       const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
+      StageRing<QS> qr;
+      StageRing<DS> dr;
       bool ok = true;
-      int stage = 0, par = 0, cnt = 0;
+      int cnt = 0;
       TileWalk wk;
-      for (walk_start(wk); !wk.done() && ok; wk.next()) {
-        if (classify(wk.pos(), kpos0) == kEmpty) continue;
-        const uint64_t soff = (uint64_t)(stage * kTD);
+      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
         // dV += P^T dO  (dO of this stage has landed: its copy completed do_full)
         if (!(ok = mbar_wait(p_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
-        if (!(ok = mbar_wait(do_full(stage), par, abort, p.status, kTimeoutNs))) break;
+        if (!(ok = mbar_wait(do_full(dr.stage), dr.par, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acol = (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + 256, tmem + acol, dod_mn0 + soff + kk * 128, kIdTS,
-                 (cnt > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(dv_done);
-        // dK += dS^T Q  (Q landed before S^T of this tile was issued)
-        if (!(ok = mbar_wait(ds_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
-        tc_fence_after();
+        const uint64_t dod = dod_mn0 + (uint64_t)(dr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t acol = 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + 256 + D, tmem + acol, qd_mn0 + soff + kk * 128, kIdTS,
-                 (cnt > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + 256, tmem + acol, dod + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dK += dS^T Q  (Q landed before S^T of this tile was issued)
+        if (!(ok = mbar_wait(ds_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
+        tc_fence_after();
+        const uint64_t qd = qd_mn0 + (uint64_t)(qr.stage * kTD);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acol = 128 + 32 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tmem + 256 + D, tmem + acol, qd + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(dk_done);
-        // both issuers' reads of this Q/dO stage are over: S^T and dP^T completed
-        // before the compute warps released p_full / ds_full
-        mma_commit(qdo_empty(stage));
+        // every read of this tile's Q and dO stages is over: S^T and dP^T completed
+        // before the compute warps released p_full / ds_full, which also read the
+        // stages' statistics
+        mma_commit(q_empty(qr.stage));
+        mma_commit(do_empty(dr.stage));
         ++cnt;
-        if (++stage == S) stage = 0, par ^= 1;
+        qr.advance();
+        dr.advance();
       }
       mma_commit(final_bar);
       drain_wait(final_bar, 0);
@@ -302,16 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_dp = tmem + lane_off + 128 + half * 64;
     const float* lse_s = reinterpret_cast<const float*>(smem + L::kLse);
     const float* del_s = reinterpret_cast<const float*>(smem + L::kDelta);
-    int stage = 0, par = 0, cnt = 0;
+    StageRing<QS> qr;
+    StageRing<DS> dr;
+    int cnt = 0;
     bool ok = true;
     TileWalk wk;
-    for (walk_start(wk); !wk.done(); wk.next()) {
+    for (walk_start(wk); !wk.done(); walk_next(wk)) {
       const int qpos0 = wk.pos();
       const int cls = classify(qpos0, kpos0);
-      if (cls == kEmpty) continue;
-      if (!(ok = warp_wait(q_full(stage), par, abort, p.status))) break;  // LSE, Delta landed
-      const float* lse_t = lse_s + stage * 128 + half * 64;
-      const float* del_t = del_s + stage * 128 + half * 64;
+      if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status))) break;  // -LSE log2e landed
+      const float* lse_t = lse_s + qr.stage * 128 + half * 64;
+      const float* del_t = del_s + dr.stage * 128 + half * 64;
       // this half's 64 per-query LSE values, fetched while S^T is still being computed
       float4 nl4[16];
 #pragma unroll
@@ -322,13 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(t_s, sr[0]);
       tmem_ld32(t_s + 32, sr[1]);
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free);  // S^T is in registers: the S region may take the next S^T
       // query column j (of this half) sees this key row iff kpos0 + row <= qpos0 + 64*half + j
       const int thr = kpos0 + row - qpos0 - half * 64;
       float pr[64];
       const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const int j0 = c * 32 + j;
@@ -344,21 +369,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pr[j0] = p0;
           pr[j0 + 1] = p1;
-          pk[j >> 1] = pack_bf16(p0, p1);
         }
-        tmem_st16(t_s + c * 16, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full);
-      float4 nd4[16];  // -Delta of this half's 64 queries, fetched before dP^T is ready
+      // -Delta of this half's 64 queries (it travels with dO), fetched before dP^T is ready
+      if (!(ok = warp_wait(do_full(dr.stage), dr.par, abort, p.status))) break;
+      float4 nd4[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) nd4[i] = reinterpret_cast<const float4*>(del_t)[i];
+      for (int k = 0; k < 16; ++k) nd4[k] = reinterpret_cast<const float4*>(del_t)[k];
       if (!(ok = warp_wait(dp_full, cnt & 1, abort, p.status))) break;
       tc_fence_after();
       tmem_ld32(t_dp, sr[0]);
       tmem_ld32(t_dp + 32, sr[1]);
       tmem_wait_ld();
+      // P^T (bf16) over the first 32 columns of this half's dP^T, already in
+      // registers, so the dV product can start while dS is formed
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) pk[j >> 1] = pack_bf16(pr[c * 32 + j], pr[c * 32 + j + 1]);
+        tmem_st16(t_dp + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
@@ -373,13 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  __uint_as_float(sr[c][j + 1])), nd));
           pk[j >> 1] = pack_bf16(d.x, d.y);
         }
-        tmem_st16(t_dp + c * 16, pk);
+        // dS^T (bf16) over the next 32 columns of this half's dP^T
+        tmem_st16(t_dp + 32 + c * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(ds_full);
       ++cnt;
-      if (++stage == S) stage = 0, par ^= 1;
+      qr.advance();
+      dr.advance();
     }
     if (ok && cnt > 0) ok = warp_wait(dk_done, (cnt - 1) & 1, abort, p.status);
     if (ok) {
