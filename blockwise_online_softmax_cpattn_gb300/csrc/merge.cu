@@ -116,6 +116,53 @@ __global__ void __launch_bounds__(256) delta_kernel(int64_t rows, int D, const T
   }
 }
 
+// bf16 rows of V int4 vectors (D = 8V): four lanes per row, each holding its V/4
+// vector loads of o and dO in flight at once, so a warp covers 8 rows per pass
+// and the loads of many rows overlap (the one-warp-per-row form above keeps only
+// two loads of one row in flight and is latency-bound at these sizes).
+template <int V>
+__global__ void __launch_bounds__(256) delta_rows4_kernel(int64_t rows,
+                                                          const __nv_bfloat16* __restrict__ o,
+                                                          const __nv_bfloat16* __restrict__ dO,
+                                                          const float* __restrict__ lse,
+                                                          float* __restrict__ delta,
+                                                          float* __restrict__ lse2) {
+  constexpr int kPer = V / 4;  // vectors per lane
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 3;
+  const int64_t groups = (int64_t)gridDim.x * (blockDim.x >> 2);
+  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 2; row < rows;
+       row += groups) {
+    const int4* a4 = reinterpret_cast<const int4*>(o) + row * V + sub * kPer;
+    const int4* b4 = reinterpret_cast<const int4*>(dO) + row * V + sub * kPer;
+    int4 a[kPer], b[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      a[k] = __ldcs(a4 + k);
+      b[k] = __ldcs(b4 + k);
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b[k]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    }
+    // the four lanes of a row are consecutive; the loop bound is uniform per group
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if (sub == 0) {
+      delta[row] = -acc;
+      lse2[row] = -lse[row] * 1.44269504088896340736f;
+    }
+  }
+}
+
 cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const void* dO,
                          const float* lse, float* delta, float* lse2, cudaStream_t st) {
   int dev = 0, sms = 148;
@@ -125,7 +172,19 @@ cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const voi
   if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
   if (blocks < 1) blocks = 1;
   timing_begin("bwd_prepass", st);
-  if (bf16)
+  const bool aligned = (((uintptr_t)o | (uintptr_t)dO) & 15) == 0;
+  if (bf16 && lse2 && aligned && (D == 128 || D == 64) && rows % 8 == 0) {
+    // 64 rows per block, every SM covered several times over
+    int64_t g = rows / 64;
+    if (g > (int64_t)sms * 8) g = (int64_t)sms * 8;
+    if (g < 1) g = 1;
+    if (D == 128)
+      delta_rows4_kernel<16><<<(unsigned)g, 256, 0, st>>>(rows, (const __nv_bfloat16*)o,
+                                                          (const __nv_bfloat16*)dO, lse, delta, lse2);
+    else
+      delta_rows4_kernel<8><<<(unsigned)g, 256, 0, st>>>(rows, (const __nv_bfloat16*)o,
+                                                         (const __nv_bfloat16*)dO, lse, delta, lse2);
+  } else if (bf16)
     delta_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
         rows, D, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dO, lse, delta, lse2);
   else
