@@ -106,8 +106,8 @@ struct DkdvSmem {
   static constexpr int kBar = kDelta + kDOStages * 512;
   // kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], s_full, s_free,
   // dp_full, p_full, ds_full, dk_done, final (gradient issuer), final_s (S^T
-  // issuer), final_p (dP^T issuer)
-  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 9;
+  // issuer), final_p (dP^T issuer), s_issued, dp_issued
+  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 11;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
 };
@@ -141,6 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t final_bar = s_full + 48;
   const uint32_t final_s = s_full + 56;
   const uint32_t final_p = s_full + 64;
+  // issue order of the score products (plain arrivals once a product's MMAs are
+  // queued): S^T(t+1) goes in behind dP^T(t)
+  const uint32_t s_issued = s_full + 72;
+  const uint32_t dp_issued = s_full + 80;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -245,6 +249,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileWalk wk;
       for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
         const int st = is_s ? qr.stage : dr.stage;
+        // The tensor pipe runs MMAs in the order they are queued.  dP^T(t) heads the
+        // chain dP^T(t) -> P^T(t) -> dV(t) -> dK(t) -> dP^T(t+1) (the P^T and dS^T
+        // that dV and dK read are stored over dP^T), so S^T(t+1) is queued behind
+        // dP^T(t), where it runs while the compute warps store P^T(t), instead of
+        // ahead of it.  Each issuer waits for the other's previous product to be
+        // queued (dP^T(t) after S^T(t), S^T(t+1) after dP^T(t)), which keeps the two
+        // arrival barriers in lockstep.
+        if (is_s && cnt > 0 &&
+            !(ok = mbar_wait(dp_issued, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
+          break;
+        if (!is_s && !(ok = mbar_wait(s_issued, cnt & 1, abort, p.status, kTimeoutNs))) break;
         // S^T: the S region is free once the compute warps have loaded the previous
         // S^T; dP^T: the dP region is free once dV and dK of the previous tile have
         // read the P^T and dS^T stored there
@@ -261,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
           mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
         }
+        mbar_arrive(is_s ? s_issued : dp_issued);  // before the commit, so it does not wait
         mma_commit(is_s ? s_full : dp_full);
         ++cnt;
         qr.advance();
@@ -293,6 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acol = 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
           mma_ts(tmem + 256, tmem + acol, dod + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
         }
+        // dV was the last reader of this dO stage (dP^T completed before p_full, by
+        // which the compute warps also hold its -Delta in registers): release it now,
+        // a product earlier than Q, at the price of the wait below waiting for dV
+        mma_commit(do_empty(dr.stage));
         // dK += dS^T Q  (Q landed before S^T of this tile was issued)
         if (!(ok = mbar_wait(ds_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
         tc_fence_after();
@@ -303,11 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + 256 + D, tmem + acol, qd + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(dk_done);
-        // every read of this tile's Q and dO stages is over: S^T and dP^T completed
-        // before the compute warps released p_full / ds_full, which also read the
-        // stages' statistics
+        // every read of this tile's Q stage is over: S^T completed before the compute
+        // warps released ds_full, which also read the stage's statistics
         mma_commit(q_empty(qr.stage));
-        mma_commit(do_empty(dr.stage));
         ++cnt;
         qr.advance();
         dr.advance();
