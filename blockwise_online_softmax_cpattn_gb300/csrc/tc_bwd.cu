@@ -228,15 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (dr.was_issued(s)) drain_wait(do_full(s), dr.issued_parity(s));
     }
   } else if (warp == 1 || warp == 3) {
-    if (lane == 0) {
+    {
       // Score issuers: warp 1 S^T = K Q^T, warp 3 dP^T = V dO^T (SS, K-major); warp 2
-      // issues the gradient products.  A thread takes about 35-50 cycles to issue a
-      // tcgen05.mma that runs 64 cycles at N = 128, and its next memory access after
-      // a tcgen05.commit waits for the committed MMAs, so a thread per product keeps
-      // each product's waits from holding up the others.
+      // issues the gradient products.  Issuing a tcgen05.mma that runs 64 cycles at
+      // N = 128 takes its thread tens of cycles, and the thread's next memory access
+      // after a tcgen05.commit waits for the committed MMAs, so a warp per product
+      // keeps each product's waits from holding up the others.  The whole warp runs
+      // the loop (warp-uniform descriptors); one elected lane issues.
       const bool is_s = warp == 1;
+      const bool leader = elect_one();
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
-      bool ok = mbar_wait(kv_full, 0, abort, p.status, kTimeoutNs);
+      bool ok = warp_wait(kv_full, 0, abort, p.status);
       tc_fence_after();
       // descriptor bases (16-byte units), K-major
       constexpr uint32_t kTD = L::kTB >> 4;
@@ -256,39 +258,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ahead of it.  Each issuer waits for the other's previous product to be
         // queued (dP^T(t) after S^T(t), S^T(t+1) after dP^T(t)), which keeps the two
         // arrival barriers in lockstep.
-        if (is_s && cnt > 0 &&
-            !(ok = mbar_wait(dp_issued, (cnt - 1) & 1, abort, p.status, kTimeoutNs)))
+        if (is_s && cnt > 0 && !(ok = warp_wait(dp_issued, (cnt - 1) & 1, abort, p.status)))
           break;
-        if (!is_s && !(ok = mbar_wait(s_issued, cnt & 1, abort, p.status, kTimeoutNs))) break;
+        if (!is_s && !(ok = warp_wait(s_issued, cnt & 1, abort, p.status))) break;
         // S^T: the S region is free once the compute warps have loaded the previous
         // S^T; dP^T: the dP region is free once dV and dK of the previous tile have
         // read the P^T and dS^T stored there
-        if (!(ok = mbar_wait(is_s ? q_full(st) : do_full(st), is_s ? qr.par : dr.par, abort,
-                             p.status, kTimeoutNs)))
+        if (!(ok = warp_wait(is_s ? q_full(st) : do_full(st), is_s ? qr.par : dr.par, abort,
+                             p.status)))
           break;
-        if (cnt > 0 && !(ok = mbar_wait(is_s ? s_free : dk_done, (cnt - 1) & 1, abort, p.status,
-                                        kTimeoutNs)))
+        if (cnt > 0 &&
+            !(ok = warp_wait(is_s ? s_free : dk_done, (cnt - 1) & 1, abort, p.status)))
           break;
         tc_fence_after();
         const uint64_t bd = bd0 + (uint64_t)(st * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
+          if (leader) mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
         }
-        mbar_arrive(is_s ? s_issued : dp_issued);  // before the commit, so it does not wait
-        mma_commit(is_s ? s_full : dp_full);
+        if (leader) {
+          mbar_arrive(is_s ? s_issued : dp_issued);  // before the commit, so it does not wait
+          mma_commit(is_s ? s_full : dp_full);
+        }
+        __syncwarp();
         ++cnt;
         qr.advance();
         dr.advance();
       }
-      mma_commit(is_s ? final_s : final_p);
+      if (leader) mma_commit(is_s ? final_s : final_p);
+      __syncwarp();
       drain_wait(is_s ? final_s : final_p, 0);
     }
   } else if (warp == 2) {
-    if (lane == 0) {
+    {
       // Gradient issuer: dV += P^T dO and dK += dS^T Q (TS: P^T and dS^T in the dP
-      // region of TMEM, Q / dO MN-major from shared memory)
+      // region of TMEM, Q / dO MN-major from shared memory); whole warp, one lane issues
+      const bool leader = elect_one();
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQ, kTile * 128, 1024);
@@ -300,37 +306,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileWalk wk;
       for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
         // dV += P^T dO  (dO of this stage has landed: its copy completed do_full)
-        if (!(ok = mbar_wait(p_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
-        if (!(ok = mbar_wait(do_full(dr.stage), dr.par, abort, p.status, kTimeoutNs))) break;
+        if (!(ok = warp_wait(p_full, cnt & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(do_full(dr.stage), dr.par, abort, p.status))) break;
         tc_fence_after();
         const uint64_t dod = dod_mn0 + (uint64_t)(dr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t acol = 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + 256, tmem + acol, dod + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
+          if (leader)
+            mma_ts(tmem + 256, tmem + acol, dod + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
         }
         // dV was the last reader of this dO stage (dP^T completed before p_full, by
         // which the compute warps also hold its -Delta in registers): release it now,
         // a product earlier than Q, at the price of the wait below waiting for dV
-        mma_commit(do_empty(dr.stage));
+        if (leader) mma_commit(do_empty(dr.stage));
+        __syncwarp();
         // dK += dS^T Q  (Q landed before S^T of this tile was issued)
-        if (!(ok = mbar_wait(ds_full, cnt & 1, abort, p.status, kTimeoutNs))) break;
+        if (!(ok = warp_wait(ds_full, cnt & 1, abort, p.status))) break;
         tc_fence_after();
         const uint64_t qd = qd_mn0 + (uint64_t)(qr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t acol = 128 + 32 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + 256 + D, tmem + acol, qd + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
+          if (leader)
+            mma_ts(tmem + 256 + D, tmem + acol, qd + kk * 128, kIdTS,
+                   (cnt > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(dk_done);
-        // every read of this tile's Q stage is over: S^T completed before the compute
-        // warps released ds_full, which also read the stage's statistics
-        mma_commit(q_empty(qr.stage));
+        if (leader) {
+          mma_commit(dk_done);
+          // every read of this tile's Q stage is over: S^T completed before the
+          // compute warps released ds_full, which also read the stage's statistics
+          mma_commit(q_empty(qr.stage));
+        }
+        __syncwarp();
         ++cnt;
         qr.advance();
         dr.advance();
       }
-      mma_commit(final_bar);
+      if (leader) mma_commit(final_bar);
+      __syncwarp();
       drain_wait(final_bar, 0);
     }
   }
