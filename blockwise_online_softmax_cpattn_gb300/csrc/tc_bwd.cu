@@ -644,12 +644,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (vr.was_issued(s)) drain_wait(v_full(s), vr.issued_parity(s));
     }
   } else if (warp == 1 || warp == 3) {
-    // One issuer per product: warp 1 S = Q K^T, warp 3 dP = dO V^T, warp 2 dQ.  A
-    // thread takes about 35-50 cycles to issue a tcgen05.mma that runs 64 cycles at
-    // N = 128, and its next memory access after a tcgen05.commit waits for the
+    // One issuer per product: warp 1 S = Q K^T, warp 3 dP = dO V^T, warp 2 dQ.  An
+    // issuing thread's next memory access after a tcgen05.commit waits for the
     // committed MMAs, so one thread alternating products would keep a single group
-    // in flight and wait on each product's consumers in turn.
-    if (lane == 0) {
+    // in flight and wait on each product's consumers in turn.  Each issuer runs as a
+    // whole warp (warp-uniform descriptors) and issues from one elected lane.
+    {
+      const bool leader = elect_one();
       const bool is_s = warp == 1;
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
       // descriptor bases (16-byte units), K-major
@@ -663,23 +664,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int w;
       for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
         const DqItem it = decode(w);
-        if (!(ok = mbar_wait(qdo_full, k & 1, abort, p.status, kTimeoutNs))) break;
+        if (!(ok = warp_wait(qdo_full, k & 1, abort, p.status))) break;
         TileWalk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           uint32_t dst;
           uint64_t bd;
           if (is_s) {
             // S(g): the S region is free once the compute warps have read S(g-1)
-            if (g > 0 && !(ok = mbar_wait(s_free, (g - 1) & 1, abort, p.status, kTimeoutNs))) break;
-            if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, kTimeoutNs))) break;
+            if (g > 0 && !(ok = warp_wait(s_free, (g - 1) & 1, abort, p.status))) break;
+            if (!(ok = warp_wait(k_full(kr.stage), kr.par, abort, p.status))) break;
             dst = tmem;
             bd = bd0 + (uint64_t)(kr.stage * kTD);
           } else {
             // dP(g) into buffer g&1: free once dQ(g-2) has read the dS stored there
-            if (g >= 2 && !(ok = mbar_wait(dq_done(g & 1), ((g - 2) >> 1) & 1, abort, p.status,
-                                           kTimeoutNs)))
+            if (g >= 2 && !(ok = warp_wait(dq_done(g & 1), ((g - 2) >> 1) & 1, abort, p.status)))
               break;
-            if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, kTimeoutNs))) break;
+            if (!(ok = warp_wait(v_full(vr.stage), vr.par, abort, p.status))) break;
             dst = tmem + 128 + 128 * (g & 1);
             bd = bd0 + (uint64_t)(vr.stage * kTD);
           }
@@ -687,27 +687,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-            mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
+            if (leader) mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
           }
-          if (is_s) {
-            mma_commit(s_full);
-          } else {
-            mma_commit(dp_full(g & 1));
-            mma_commit(v_empty(vr.stage));  // V of this tile is not read again
+          if (leader) {
+            if (is_s) {
+              mma_commit(s_full);
+            } else {
+              mma_commit(dp_full(g & 1));
+              mma_commit(v_empty(vr.stage));  // V of this tile is not read again
+            }
           }
+          __syncwarp();
           kr.advance();
           vr.advance();
           ++g;
         }
         if (!ok) break;
-        mma_commit(qdo_empty);  // this issuer is done with the item's Q (or dO)
+        if (leader) mma_commit(qdo_empty);  // this issuer is done with the item's Q (or dO)
+        __syncwarp();
       }
-      mma_commit(is_s ? final_s : final_p);
+      if (leader) mma_commit(is_s ? final_s : final_p);
+      __syncwarp();
       drain_wait(is_s ? final_s : final_p, 0);
     }
   } else if (warp == 2) {
-    if (lane == 0) {
-      // Gradient issuer: dQ += dS K (TS: dS in TMEM, K MN-major from shared memory)
+    {
+      // Gradient issuer: dQ += dS K (TS: dS in TMEM, K MN-major from shared memory);
+      // whole warp, one elected lane issues
+      const bool leader = elect_one();
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t kd_mn0 = sdesc_sw128(sbase + L::kK, kTile * 128, 1024);
@@ -720,27 +727,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         int t = 0;  // tile of this item
         TileWalk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
-          if (!(ok = mbar_wait(ds_full(g & 1), (g >> 1) & 1, abort, p.status, kTimeoutNs))) break;
+          if (!(ok = warp_wait(ds_full(g & 1), (g >> 1) & 1, abort, p.status))) break;
           // the item's first dQ overwrites the accumulator the previous epilogue read
-          if (t == 0 && k > 0 && !(ok = mbar_wait(dq_free, (k - 1) & 1, abort, p.status, kTimeoutNs)))
-            break;
+          if (t == 0 && k > 0 && !(ok = warp_wait(dq_free, (k - 1) & 1, abort, p.status))) break;
           tc_fence_after();
           // K(g) landed before S(g), which the compute warps read before storing dS(g)
           const uint64_t kd_mn = kd_mn0 + (uint64_t)(kr.stage * kTD);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t acol = 128 + 128 * (g & 1) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-            mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS, (t > 0 || kk > 0) ? 1u : 0u);
+            if (leader)
+              mma_ts(tmem + kDqCol, tmem + acol, kd_mn + kk * 128, kIdTS,
+                     (t > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(dq_done(g & 1));  // the dS buffer may take dP(g+2)
-          // both S(g) and dQ(g) have read K(g) once dQ(g) completes
-          mma_commit(k_empty(kr.stage));
+          if (leader) {
+            mma_commit(dq_done(g & 1));  // the dS buffer may take dP(g+2)
+            // both S(g) and dQ(g) have read K(g) once dQ(g) completes
+            mma_commit(k_empty(kr.stage));
+          }
+          __syncwarp();
           kr.advance();
           ++g;
           ++t;
         }
       }
-      mma_commit(final_q);
+      if (leader) mma_commit(final_q);
+      __syncwarp();
       drain_wait(final_q, 0);
     }
   }

@@ -261,7 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
-    if (lane == 0) {
+    // (whole warp, warp-uniform descriptors; one elected lane issues)
+    {
+      const bool leader = elect_one();
       constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
       // descriptor bases; per k-step offsets are compile-time constants (16-byte units)
@@ -273,36 +275,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       int w;
       for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
         const Item it = decode(p, w);
-        if (!(ok = mbar_wait(q_full, k & 1, abort, p.status, tmo))) break;
+        if (!(ok = warp_wait(q_full, k & 1, abort, p.status, tmo))) break;
         TileWalk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           const int b = g & 1;
-          if (!(ok = mbar_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
+          if (!(ok = warp_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
           // buffer b is free once PV of tile g-2 has read the P stored there
-          if (g >= 2 && !(ok = mbar_wait(pv_done(b), ((g - 2) >> 1) & 1, abort, p.status, tmo)))
+          if (g >= 2 && !(ok = warp_wait(pv_done(b), ((g - 2) >> 1) & 1, abort, p.status, tmo)))
             break;
           tc_fence_after();
           const uint64_t kd = kd0 + (uint64_t)(kr.stage * kTileDesc);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;  // 16 KiB blocks, 32 B steps
-            mma_ss(tmem + b * 128, qd + off, kd + off, kIdescS, kk > 0);
+            if (leader) mma_ss(tmem + b * 128, qd + off, kd + off, kIdescS, kk > 0);
           }
-          mma_commit(s_full(b));
-          mma_commit(k_empty(kr.stage));
+          if (leader) {
+            mma_commit(s_full(b));
+            mma_commit(k_empty(kr.stage));
+          }
+          __syncwarp();
           kr.advance();
           ++g;
         }
         if (!ok) break;
-        mma_commit(q_empty);  // the Q buffer may take the next item's tile
+        if (leader) mma_commit(q_empty);  // the Q buffer may take the next item's tile
+        __syncwarp();
       }
-      // every MMA this thread issued has finished before TMEM can be freed
-      mma_commit(final_s);
+      // every MMA this warp issued has finished before TMEM can be freed
+      if (leader) mma_commit(final_s);
+      __syncwarp();
       drain_wait(final_s, 0);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ PV issuer
-    if (lane == 0) {
+    // (whole warp, one elected lane issues)
+    {
+      const bool leader = elect_one();
       constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
       constexpr uint32_t kTileDesc = L::kTileBytes >> 4;
       const uint64_t vd0 = sdesc_sw128(sbase + L::kV, kTile * 128, 1024);
@@ -316,29 +325,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileWalk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           const int b = g & 1;
-          if (!(ok = mbar_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
+          if (!(ok = warp_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
           // the first PV of an item overwrites O: the previous item's epilogue has read it
-          if (t == 0 && k > 0 && !(ok = mbar_wait(o_free, (k - 1) & 1, abort, p.status, tmo)))
+          if (t == 0 && k > 0 && !(ok = warp_wait(o_free, (k - 1) & 1, abort, p.status, tmo)))
             break;
           const uint64_t vd = vd0 + (uint64_t)(vr.stage * kTileDesc);
           for (int h = 0; h < 2 && ok; ++h) {
             // O_h += P_h V_h: keys [64h, 64h+64), 16 key rows = 2048 B per k-step
-            if (!(ok = mbar_wait(p_full(b, h), (g >> 1) & 1, abort, p.status, tmo))) break;
+            if (!(ok = warp_wait(p_full(b, h), (g >> 1) & 1, abort, p.status, tmo))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + 256 + h * D, tmem + b * 128 + h * 64 + kk * 8,
-                     vd + (uint64_t)((h * 4 + kk) * 128), kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+              if (leader)
+                mma_ts(tmem + 256 + h * D, tmem + b * 128 + h * 64 + kk * 8,
+                       vd + (uint64_t)((h * 4 + kk) * 128), kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+            __syncwarp();
           }
           if (!ok) break;
-          mma_commit(pv_done(b));
-          mma_commit(v_empty(vr.stage));
+          if (leader) {
+            mma_commit(pv_done(b));
+            mma_commit(v_empty(vr.stage));
+          }
+          __syncwarp();
           vr.advance();
           ++g;
           ++t;
         }
       }
-      mma_commit(final_pv);
+      if (leader) mma_commit(final_pv);
+      __syncwarp();
       drain_wait(final_pv, 0);
     }
   }
