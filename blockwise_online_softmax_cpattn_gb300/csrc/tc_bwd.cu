@@ -105,9 +105,9 @@ struct DkdvSmem {
   static constexpr int kDelta = kLse + kQStages * 512;
   static constexpr int kBar = kDelta + kDOStages * 512;
   // kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], s_full, s_free,
-  // dp_full, p_full, ds_full, dk_done, final (gradient issuer), final_s (S^T
-  // issuer), final_p (dP^T issuer), s_issued, dp_issued
-  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 11;
+  // dp_full, p_full, ds_full, final (gradient issuer), final_s (S^T issuer),
+  // s_issued, dp_issued
+  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
 };
@@ -137,14 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t dp_full = s_full + 16;
   const uint32_t p_full = s_full + 24;
   const uint32_t ds_full = s_full + 32;
-  const uint32_t dk_done = s_full + 40;  // dV and dK of the tile done: the dP region is free
-  const uint32_t final_bar = s_full + 48;
-  const uint32_t final_s = s_full + 56;
-  const uint32_t final_p = s_full + 64;
-  // issue order of the score products (plain arrivals once a product's MMAs are
-  // queued): S^T(t+1) goes in behind dP^T(t)
-  const uint32_t s_issued = s_full + 72;
-  const uint32_t dp_issued = s_full + 80;
+  const uint32_t final_bar = s_full + 40;  // every MMA of the gradient issuer done
+  const uint32_t final_s = s_full + 48;
+  // issue order (plain arrivals once a product's MMAs are queued): S^T(t+1) goes in
+  // behind dP^T(t), dP^T(t+1) behind S^T(t+1)
+  const uint32_t s_issued = s_full + 56;
+  const uint32_t dp_issued = s_full + 64;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -227,102 +225,118 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < DS; ++s)
         if (dr.was_issued(s)) drain_wait(do_full(s), dr.issued_parity(s));
     }
-  } else if (warp == 1 || warp == 3) {
+  } else if (warp == 1) {
     {
-      // Score issuers: warp 1 S^T = K Q^T, warp 3 dP^T = V dO^T (SS, K-major); warp 2
-      // issues the gradient products.  Issuing a tcgen05.mma that runs 64 cycles at
-      // N = 128 takes its thread tens of cycles, and the thread's next memory access
-      // after a tcgen05.commit waits for the committed MMAs, so a warp per product
-      // keeps each product's waits from holding up the others.  The whole warp runs
-      // the loop (warp-uniform descriptors); one elected lane issues.
-      const bool is_s = warp == 1;
+      // S^T = K Q^T issuer (SS, K-major).  Issuing a tcgen05.mma that runs 64
+      // cycles at N = 128 takes its thread tens of cycles, and the thread's next
+      // memory access after a tcgen05.commit waits for the committed MMAs, so S^T
+      // has a warp of its own and the gradient warp (warp 2) issues dP^T, dV and dK.
+      // The whole warp runs the loop (warp-uniform descriptors); one elected lane
+      // issues.
       const bool leader = elect_one();
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
       bool ok = warp_wait(kv_full, 0, abort, p.status);
       tc_fence_after();
-      // descriptor bases (16-byte units), K-major
       constexpr uint32_t kTD = L::kTB >> 4;
-      const uint64_t ad = sdesc_sw128(sbase + (is_s ? L::kK : L::kV), 16, 1024);
-      const uint64_t bd0 = sdesc_sw128(sbase + (is_s ? L::kQ : L::kDO), 16, 1024);
-      const uint32_t dst = tmem + (is_s ? 0 : 128);
+      const uint64_t kd = sdesc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t qd0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
       StageRing<QS> qr;
-      StageRing<DS> dr;
       int cnt = 0;
       TileWalk wk;
       for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        const int st = is_s ? qr.stage : dr.stage;
-        // The tensor pipe runs MMAs in the order they are queued.  dP^T(t) heads the
-        // chain dP^T(t) -> P^T(t) -> dV(t) -> dK(t) -> dP^T(t+1) (the P^T and dS^T
-        // that dV and dK read are stored over dP^T), so S^T(t+1) is queued behind
-        // dP^T(t), where it runs while the compute warps store P^T(t), instead of
-        // ahead of it.  Each issuer waits for the other's previous product to be
-        // queued (dP^T(t) after S^T(t), S^T(t+1) after dP^T(t)), which keeps the two
+        // The tensor pipe runs MMAs in the order they are queued.  The gradient warp
+        // queues ... dV(t-1), dK(t-1), dP^T(t) back to back; S^T(t+1) goes in behind
+        // dP^T(t), where it runs while the compute warps turn dP^T(t) into P^T(t).
+        // The two warps wait for each other's previous product to be queued
+        // (S^T(t+1) after dP^T(t), dP^T(t+1) after S^T(t+1)), which keeps the two
         // arrival barriers in lockstep.
-        if (is_s && cnt > 0 && !(ok = warp_wait(dp_issued, (cnt - 1) & 1, abort, p.status)))
-          break;
-        if (!is_s && !(ok = warp_wait(s_issued, cnt & 1, abort, p.status))) break;
-        // S^T: the S region is free once the compute warps have loaded the previous
-        // S^T; dP^T: the dP region is free once dV and dK of the previous tile have
-        // read the P^T and dS^T stored there
-        if (!(ok = warp_wait(is_s ? q_full(st) : do_full(st), is_s ? qr.par : dr.par, abort,
-                             p.status)))
-          break;
-        if (cnt > 0 &&
-            !(ok = warp_wait(is_s ? s_free : dk_done, (cnt - 1) & 1, abort, p.status)))
-          break;
+        if (cnt > 0 && !(ok = warp_wait(dp_issued, (cnt - 1) & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status))) break;
+        // the S region is free once the compute warps have loaded the previous S^T
+        if (cnt > 0 && !(ok = warp_wait(s_free, (cnt - 1) & 1, abort, p.status))) break;
         tc_fence_after();
-        const uint64_t bd = bd0 + (uint64_t)(st * kTD);
+        const uint64_t qd = qd0 + (uint64_t)(qr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
-          if (leader) mma_ss(dst, ad + off, bd + off, kIdSS, kk > 0);
+          if (leader) mma_ss(tmem, kd + off, qd + off, kIdSS, kk > 0);
         }
         if (leader) {
-          mbar_arrive(is_s ? s_issued : dp_issued);  // before the commit, so it does not wait
-          mma_commit(is_s ? s_full : dp_full);
+          mbar_arrive(s_issued);  // before the commit, so it does not wait
+          mma_commit(s_full);
         }
         __syncwarp();
         ++cnt;
         qr.advance();
-        dr.advance();
       }
-      if (leader) mma_commit(is_s ? final_s : final_p);
+      if (leader) mma_commit(final_s);
       __syncwarp();
-      drain_wait(is_s ? final_s : final_p, 0);
+      drain_wait(final_s, 0);
     }
   } else if (warp == 2) {
     {
-      // Gradient issuer: dV += P^T dO and dK += dS^T Q (TS: P^T and dS^T in the dP
-      // region of TMEM, Q / dO MN-major from shared memory); whole warp, one lane issues
+      // Gradient warp: dP^T = V dO^T (SS, K-major) into the dP region, then
+      // dV += P^T dO and dK += dS^T Q (TS: P^T and dS^T stored over dP^T, Q / dO
+      // MN-major), queued per tile as dV(t), dK(t), dP^T(t+1).  dP^T(t+1)
+      // overwrites what dV(t) and dK(t) read, which is safe because one thread's
+      // MMAs run in issue order, so it follows dK(t) without a round trip through
+      // an mbarrier.  The operands of dK(t) and dP^T(t+1) are waited for before the
+      // commits of tile t: a thread's first mbarrier access after a commit waits for
+      // the committed MMAs.
       const bool leader = elect_one();
+      constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);
       constexpr uint32_t kTD = L::kTB >> 4;
+      const uint64_t vd = sdesc_sw128(sbase + L::kV, 16, 1024);
+      const uint64_t dod_k0 = sdesc_sw128(sbase + L::kDO, 16, 1024);
       const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQ, kTile * 128, 1024);
       const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
-      StageRing<QS> qr;
-      StageRing<DS> dr;
-      bool ok = true;
-      int cnt = 0;
-      TileWalk wk;
-      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
-        // dV += P^T dO  (dO of this stage has landed: its copy completed do_full)
-        if (!(ok = warp_wait(p_full, cnt & 1, abort, p.status))) break;
-        if (!(ok = warp_wait(do_full(dr.stage), dr.par, abort, p.status))) break;
+      // every query tile at or after this K/V tile's position sees it, once per
+      // query head of the group (the walk of the other roles skips the rest)
+      const int n_tiles = p.n_rep * ((p.T - kpos0) >> 7);
+      bool ok = warp_wait(kv_full, 0, abort, p.status);
+      tc_fence_after();
+      StageRing<QS> qr;   // Q stage of tile t
+      StageRing<DS> dr;   // dO stage of tile t
+      StageRing<DS> dpr;  // dO stage of the next dP^T
+      auto issue_dp = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 2;
+          if (leader)
+            mma_ss(tmem + 128, vd + off, dod_k0 + (uint64_t)(dpr.stage * kTD) + off, kIdSS,
+                   kk > 0);
+        }
+        if (leader) {
+          mbar_arrive(dp_issued);
+          mma_commit(dp_full);
+        }
+        __syncwarp();
+        dpr.advance();
+      };
+      // dP^T(0), behind S^T(0)
+      if (ok && n_tiles > 0 && (ok = warp_wait(do_full(dpr.stage), dpr.par, abort, p.status)) &&
+          (ok = warp_wait(s_issued, 0, abort, p.status))) {
+        tc_fence_after();
+        issue_dp();
+      }
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        // dV(t) += P^T(t) dO(t)  (dO landed before dP^T(t) was issued)
+        if (!(ok = warp_wait(p_full, t & 1, abort, p.status))) break;
         tc_fence_after();
         const uint64_t dod = dod_mn0 + (uint64_t)(dr.stage * kTD);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t acol = 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
           if (leader)
-            mma_ts(tmem + 256, tmem + acol, dod + kk * 128, kIdTS, (cnt > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + 256, tmem + acol, dod + kk * 128, kIdTS, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        // dV was the last reader of this dO stage (dP^T completed before p_full, by
-        // which the compute warps also hold its -Delta in registers): release it now,
-        // a product earlier than Q, at the price of the wait below waiting for dV
-        if (leader) mma_commit(do_empty(dr.stage));
-        __syncwarp();
-        // dK += dS^T Q  (Q landed before S^T of this tile was issued)
-        if (!(ok = warp_wait(ds_full, cnt & 1, abort, p.status))) break;
+        // dK(t) += dS^T(t) Q(t) (Q landed before S^T(t)); dO(t+1) landed and S^T(t+1)
+        // queued for dP^T(t+1)
+        const bool more = t + 1 < n_tiles;
+        if (!(ok = warp_wait(ds_full, t & 1, abort, p.status))) break;
+        if (more && !(ok = warp_wait(do_full(dpr.stage), dpr.par, abort, p.status))) break;
+        if (more && !(ok = warp_wait(s_issued, (t + 1) & 1, abort, p.status))) break;
         tc_fence_after();
         const uint64_t qd = qd_mn0 + (uint64_t)(qr.stage * kTD);
 #pragma unroll
@@ -330,16 +344,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acol = 128 + 32 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
           if (leader)
             mma_ts(tmem + 256 + D, tmem + acol, qd + kk * 128, kIdTS,
-                   (cnt > 0 || kk > 0) ? 1u : 0u);
+                   (t > 0 || kk > 0) ? 1u : 0u);
         }
         if (leader) {
-          mma_commit(dk_done);
-          // every read of this tile's Q stage is over: S^T completed before the
-          // compute warps released ds_full, which also read the stage's statistics
+          // every read of tile t's Q and dO stages is issued: S^T(t) and dP^T(t)
+          // completed before the compute warps released p_full / ds_full, by which
+          // they also hold the stages' statistics
+          mma_commit(do_empty(dr.stage));
           mma_commit(q_empty(qr.stage));
         }
         __syncwarp();
-        ++cnt;
+        if (more) issue_dp();
         qr.advance();
         dr.advance();
       }
@@ -448,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       qr.advance();
       dr.advance();
     }
-    if (ok && cnt > 0) ok = warp_wait(dk_done, (cnt - 1) & 1, abort, p.status);
+    if (ok && cnt > 0) ok = warp_wait(final_bar, 0, abort, p.status);
     if (ok) {
       tc_fence_after();
       const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
