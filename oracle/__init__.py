@@ -12,7 +12,9 @@ What it computes, in plain numpy float64, following the pages' definitions:
   softmax equations and the per-chunk partial ``Softmax(Q K^T / sqrt(d)) V``; the
   InfiniTrain pull request "Feat: Context Parallel" #181, mode table row "p2p":
   single-pass online-softmax merge, backward by recomputing the probabilities),
-  plus the (O, LSE) merge of two partial results.
+  plus the (O, LSE) merge of two partial results, and one rank's share of the
+  all-gather mode (pull request #181, mode table row "all_gather": local queries
+  over the gathered K/V; K/V gradients summed over ranks by a ReduceScatter).
 * ``layouts``: the contiguous and zigzag (head-tail paired) token-to-rank maps
   (tutorial, section "Zig-Zag Ring Attention") and the all-to-all
   head<->sequence re-layout of the hierarchical a2a+p2p mode (pull request #181,

@@ -216,3 +216,68 @@ def dkdv_rows(q_heads, k_g, v_g, do_heads, kv_rows, scale, rows_per_block=512):
             dk += scale * (dS[:, kv_rows].T @ q_heads[h, rows])
             dv += P[:, kv_rows].T @ dO
     return dk, dv
+
+
+# ----------------------------------------------------------------------------
+# All-gather mode (pull request "Feat: Context Parallel" #181, mode table row
+# "all_gather": every rank gathers the whole sequence's K/V and runs attention of
+# its own query chunk over it; the backward sums the K/V gradients of all ranks
+# with a ReduceScatter.  Tutorial "上下文并行", section "Zig-Zag Ring Attention 的
+# 通信与计算重叠", bullet "all-gather": one all-gather gives every GPU the complete
+# K/V at once).  A rank's result is the definition above restricted to its query
+# rows; its K/V gradient is the part of the sums over i that runs over its rows.
+# ----------------------------------------------------------------------------
+
+def allgather_fwd(q, k, v, scale, q_pos):
+    """(O, LSE) of the query rows at natural positions ``q_pos`` over all keys.
+
+    q [B, H_q, T, D], k/v [B, H_kv, T, D] in natural order; ``q_pos`` lists the
+    rank's query positions (in the order its rows are stored).  Returns
+    O [B, H_q, n, D] and LSE [B, H_q, n] with n = len(q_pos).
+    """
+    q_pos = np.asarray(q_pos)
+    B, H_q, T, D = q.shape
+    n_rep = _group(H_q, k.shape[1])
+    o = np.empty((B, H_q, len(q_pos), D))
+    lse = np.empty((B, H_q, len(q_pos)))
+    pos = np.arange(T)
+    for b in range(B):
+        for h in range(H_q):
+            g = h // n_rep
+            S = scores(q[b, h, q_pos], k[b, g], scale)
+            P, m, l = safe_softmax_rows(S, causal_visible(q_pos, pos))
+            o[b, h] = P @ v[b, g]
+            lse[b, h] = m + np.log(l)
+    return o, lse
+
+
+def allgather_bwd(q, k, v, do, scale, q_pos):
+    """One rank's backward in all-gather mode.
+
+    ``q_pos`` are the rank's query positions (natural order indices) and
+    ``do`` [B, H_q, T, D] the upstream gradient in natural order (only the rows
+    at ``q_pos`` are read).  Returns (dQ [B, H_q, n, D] of the rank's rows,
+    dK_part, dV_part [B, H_kv, T, D]): the K/V gradient sums of the definition
+    with i running over the rank's rows only, which the ReduceScatter adds up over
+    the ranks.
+    """
+    q_pos = np.asarray(q_pos)
+    B, H_q, T, D = q.shape
+    n_rep = _group(H_q, k.shape[1])
+    dq = np.zeros((B, H_q, len(q_pos), D))
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    pos = np.arange(T)
+    for b in range(B):
+        for h in range(H_q):
+            g = h // n_rep
+            S = scores(q[b, h, q_pos], k[b, g], scale)
+            P, _, _ = safe_softmax_rows(S, causal_visible(q_pos, pos))
+            O = P @ v[b, g]
+            dO = do[b, h, q_pos]
+            delta = np.sum(dO * O, axis=1)
+            dS = P * (dO @ v[b, g].T - delta[:, None])
+            dq[b, h] = scale * (dS @ k[b, g])
+            dk[b, g] += scale * (dS.T @ q[b, h, q_pos])
+            dv[b, g] += P.T @ dO
+    return dq, dk, dv

@@ -238,3 +238,60 @@ def test_empty_partial_is_merge_identity(rng):
     q = rng.standard_normal((4, 3)); k = rng.standard_normal((5, 3)); v = rng.standard_normal((5, 3))
     o, l = A.partial_attention(q, k, v, np.arange(4), np.arange(10, 15), 1.0)
     assert np.all(o == 0) and np.all(l == -np.inf)
+
+
+# ---------------------------------------------------------------------------
+# All-gather mode (pull request #181, mode table row "all_gather": local queries
+# over the gathered K/V, K/V gradients summed over ranks by a ReduceScatter).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout,cp,T", [("zigzag", 4, 32), ("contiguous", 2, 24),
+                                         ("zigzag", 2, 20)])
+def test_allgather_rows_match_torch(rng, layout, cp, T):
+    """Every rank's rows equal the library's full causal attention at its positions,
+    its dQ rows the autograd dQ there, and the ranks' K/V gradients add up to the
+    autograd dK/dV (the ReduceScatter sum)."""
+    q, k, v, do = _rand(rng, 1, 4, 2, T, 8)
+    scale = 0.4
+    ro, rlse, rdq, rdk, rdv = _torch_reference(q, k, v, do, scale)
+    dk_sum = np.zeros_like(k)
+    dv_sum = np.zeros_like(v)
+    for r in range(cp):
+        pos = L.rank_positions(T, cp, layout, r)
+        o, lse = A.allgather_fwd(q, k, v, scale, pos)
+        assert rel_err(o, ro[:, :, pos]) < 1e-13
+        assert rel_err(lse, rlse[:, :, pos]) < 1e-13
+        dq, dk, dv = A.allgather_bwd(q, k, v, do, scale, pos)
+        assert rel_err(dq, rdq[:, :, pos]) < 1e-12
+        dk_sum += dk
+        dv_sum += dv
+    assert rel_err(dk_sum, rdk) < 1e-12
+    assert rel_err(dv_sum, rdv) < 1e-12
+
+
+def test_allgather_rank_share_finite_differences(rng):
+    """A rank's K/V gradient is the gradient of its own rows' share of the loss,
+    L_r = sum over its rows i of dO_i . O_i (central differences)."""
+    T, cp, layout = 8, 2, "zigzag"
+    q, k, v, do = _rand(rng, 1, 2, 1, T, 3)
+    scale = 0.6
+    pos = L.rank_positions(T, cp, layout, 1)
+    _, dk, dv = A.allgather_bwd(q, k, v, do, scale, pos)
+
+    def loss(k_, v_):
+        o, _ = A.attention_fwd(q, k_, v_, scale)
+        return float(np.sum(do[:, :, pos] * o[:, :, pos]))
+
+    eps = 1e-5
+    for x, g, which in ((k, dk, 0), (v, dv, 1)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp = x.copy(); xp[idx] += eps
+            xm = x.copy(); xm[idx] -= eps
+            args_p = [k, v]; args_p[which] = xp
+            args_m = [k, v]; args_m[which] = xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        assert rel_err(g, num) < 1e-8, which
+    # keys after the rank's last query position get nothing from it
+    later = np.arange(T) > pos.max()
+    assert np.all(dk[:, :, later] == 0) and np.all(dv[:, :, later] == 0)
