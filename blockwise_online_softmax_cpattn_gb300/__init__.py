@@ -66,6 +66,12 @@ _sigs = {
                               _vp, _vp, ctypes.c_size_t, _vp]),
     "cpattn_ring_bwd_noalloc": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _vp]),
+    "cpattn_allgather_fwd": (_st, [ctypes.POINTER(CpattnDesc), ctypes.c_int, _vp, _vp, _vp, _vp,
+                                   _vp, _vp]),
+    "cpattn_allgather_bwd_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
+    "cpattn_allgather_bwd": (_st, [ctypes.POINTER(CpattnDesc), ctypes.c_int, _vp, _vp, _vp, _vp,
+                                   _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t,
+                                   _vp]),
     "cpattn_layout": (_st, [ctypes.c_int, ctypes.POINTER(CpattnDesc), _vp, _vp, ctypes.c_int, _vp]),
     "cpattn_check": (_st, [_vp]),
     "cpattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -142,6 +148,24 @@ def cpattn_ring_bwd_noalloc(desc, q, k, v, o, lse, dO, dq, dk, dv, stream=None) 
     return _lib.cpattn_ring_bwd_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                         _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
                                         _stream(stream))
+
+
+def cpattn_allgather_fwd(desc, q_rank, q, k, v, o, lse, stream=None) -> int:
+    return _lib.cpattn_allgather_fwd(ctypes.byref(desc), q_rank, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                     _ptr(lse), _stream(stream))
+
+
+def cpattn_allgather_bwd_workspace(desc) -> int:
+    return _lib.cpattn_allgather_bwd_workspace(ctypes.byref(desc))
+
+
+def cpattn_allgather_bwd(desc, q_rank, q, k, v, o, lse, dO, dq, dk_sum, dv_sum, accumulate,
+                         workspace, ws_bytes=None, stream=None) -> int:
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    return _lib.cpattn_allgather_bwd(ctypes.byref(desc), q_rank, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                     _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk_sum), _ptr(dv_sum),
+                                     int(accumulate), _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def cpattn_layout(permute, desc, src, dst, n_heads, stream=None) -> int:

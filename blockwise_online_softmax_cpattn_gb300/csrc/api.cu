@@ -242,6 +242,68 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
   return from_cuda(launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st));
 }
 
+// ---------------------------------------------------------------------------
+// all-gather mode
+// ---------------------------------------------------------------------------
+cpattn_status cpattn_allgather_fwd(const cpattn_desc* desc, int q_rank, const void* q,
+                                   const void* k, const void* v, void* o, float* lse,
+                                   void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if (q_rank < 0 || q_rank >= R.cp) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  if (R.bf16 && tc_supported(R))
+    return from_cuda(launch_tc_fwd(R, q_rank, -1, q, k, v, o, lse, status_ptr(), st));
+  return from_cuda(launch_simt_fwd(R, q_rank, -1, q, k, v, o, lse, st));
+}
+
+// Workspace: Delta, then the LSE in base 2, of the rank's rows (float32 each),
+// each section 256-byte aligned.
+static size_t ag_section(const Ring& R) {
+  const size_t rows = (size_t)R.B * R.Hq * (R.T / R.cp);
+  return (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+size_t cpattn_allgather_bwd_workspace(const cpattn_desc* desc) {
+  Ring R;
+  if (validate(desc, &R) != CPATTN_OK) return 0;
+  return 2 * ag_section(R);
+}
+
+cpattn_status cpattn_allgather_bwd(const cpattn_desc* desc, int q_rank, const void* q,
+                                   const void* k, const void* v, const void* o,
+                                   const float* lse, const void* dO, void* dq, float* dk_sum,
+                                   float* dv_sum, int accumulate, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if (q_rank < 0 || q_rank >= R.cp || (accumulate != 0 && accumulate != 1))
+    return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk_sum) || !aligned16(dv_sum) ||
+      !aligned16(workspace))
+    return CPATTN_ERR_INVALID_ARG;
+  if (ws_bytes < cpattn_allgather_bwd_workspace(desc)) return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  float* delta = static_cast<float*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ag_section(R));
+  const int64_t rows = (int64_t)R.B * R.Hq * (R.T / R.cp);
+  const bool tc = R.bf16 && tc_supported(R);
+  cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  if (tc)
+    return from_cuda(launch_tc_allgather_bwd(R, q_rank, q, k, v, lse2, delta, dO, dq, dk_sum,
+                                             dv_sum, accumulate, status_ptr(), st));
+  return from_cuda(launch_simt_allgather_bwd(R, q_rank, q, k, v, lse, delta, dO, dq, dk_sum,
+                                             dv_sum, accumulate, st));
+}
+
 cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* src, void* dst,
                             int n_heads, void* stream) {
   cpattn_status s = validate(desc, nullptr);

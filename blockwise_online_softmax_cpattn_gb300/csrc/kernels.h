@@ -38,8 +38,9 @@ cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const voi
 
 // ---- simt_attn.cu (exact float32 / any-D path) ------------------------------
 // partial: q_rank >= 0 selects one rank's queries against kv_rank's chunk and
-// writes float32 o/lse of c rows per (b, h); q_rank < 0 runs the whole ring and
-// writes o in the tensor dtype.
+// writes float32 o/lse of c rows per (b, h); q_rank >= 0 with kv_rank < 0 is the
+// all-gather mode (that rank's c rows per (b, h) over every chunk, o in the tensor
+// dtype); q_rank < 0 runs the whole ring and writes o in the tensor dtype.
 cudaError_t launch_simt_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
                             const void* v, void* o, float* lse, cudaStream_t st);
 cudaError_t launch_simt_bwd_dq(const Ring& R, const void* q, const void* k, const void* v,
@@ -48,6 +49,13 @@ cudaError_t launch_simt_bwd_dq(const Ring& R, const void* q, const void* k, cons
 cudaError_t launch_simt_bwd_dkdv(const Ring& R, const void* q, const void* k, const void* v,
                                  const float* lse, const float* delta, const void* dO, void* dk,
                                  void* dv, cudaStream_t st);
+// All-gather mode backward of rank q_rank: lse/delta/dO/dq hold the rank's c rows
+// per (b, h), q the whole sequence; dk_sum/dv_sum (float32, all T rows) receive
+// the rank's share (added when `accumulate`).
+cudaError_t launch_simt_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,
+                                      const void* v, const float* lse, const float* delta,
+                                      const void* dO, void* dq, float* dk_sum, float* dv_sum,
+                                      int accumulate, cudaStream_t st);
 
 // ---- tc_fwd.cu / tc_bwd.cu (bf16 tcgen05 path, D in {64, 128}) --------------
 bool tc_supported(const Ring& R);
@@ -56,6 +64,12 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st);
+// All-gather mode backward of rank q_rank (see launch_simt_allgather_bwd); lse2 /
+// delta are the pre-pass statistics of the rank's rows.
+cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,
+                                    const void* v, const float* lse2, const float* delta,
+                                    const void* dO, void* dq, float* dk_sum, float* dv_sum,
+                                    int accumulate, int* status, cudaStream_t st);
 
 // The register split of the tensor-core kernels (3 warpgroups: one control, two
 // math) must fit in what a launch of `kern` allocates; a split that does not fit

@@ -55,6 +55,7 @@ struct SimtFwd {
   float scale;
   int q_slot0, n_q_slots;  // queries: slots [q_slot0, q_slot0 + n_q_slots)
   int kv_fixed;            // < 0: whole ring; else only this rank's chunk
+  int local_rows;          // o/lse hold n_q_slots rows per (b, h) instead of T
 };
 
 template <typename TI, typename TO>
@@ -110,8 +111,7 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtFwd p, const TI* __re
       mrun = mn;
     }
   }
-  const int64_t orow = bh * (int64_t)(p.kv_fixed >= 0 ? p.n_q_slots : p.T) +
-                       (p.kv_fixed >= 0 ? i_loc : slot);
+  const int64_t orow = p.local_rows ? bh * (int64_t)p.n_q_slots + i_loc : bh * (int64_t)p.T + slot;
   const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -126,6 +126,12 @@ struct SimtBwd {
   int B, Hq, Hkv, T, D, n_rep;
   SeqMap m;
   float scale;
+  // All-gather mode (ag_rank >= 0): only rank ag_rank's query rows take part; its
+  // o/lse/dO/Delta/dQ hold c = T/cp rows per (b, h) (local rows) while q holds
+  // the whole sequence, and dK/dV (float32) receive the rank's share, added to
+  // what they hold when `accumulate` is set.
+  int ag_rank;
+  int accumulate;
 };
 
 template <typename T>
@@ -138,13 +144,15 @@ __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(SimtBwd p, const T* __
                                                           T* __restrict__ dq) {
   const int lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (w >= (int64_t)p.B * p.Hq * p.T) return;
-  const int64_t bh = w / p.T;
-  const int slot = (int)(w - bh * p.T);
+  // w indexes the rows of dO / lse / Delta / dQ: all T slots, or the rank's c
+  const int n_slots = p.ag_rank >= 0 ? p.m.c : p.T;
+  if (w >= (int64_t)p.B * p.Hq * n_slots) return;
+  const int64_t bh = w / n_slots;
+  const int slot = (int)(w - bh * n_slots) + (p.ag_rank >= 0 ? p.ag_rank * p.m.c : 0);
   const int b = (int)(bh / p.Hq), h = (int)(bh % p.Hq), g = h / p.n_rep;
   const int D = p.D;
   float qv[4], dov[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
-  load_row(q + w * D, D, lane, qv);
+  load_row(q + (bh * p.T + slot) * D, D, lane, qv);
   load_row(dO + w * D, D, lane, dov);
   const float L = lse[w], Dl = delta[w];
   const int qpos = p.m.pos(slot);
@@ -174,11 +182,11 @@ __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(SimtBwd p, const T* __
 // dK_j = scale * sum_{group heads, i} dS_ij q_i,  dV_j = sum P_ij dO_i, one warp
 // per key row; the query ranks are visited in the order the chunk's gradient
 // travels the ring back to its owner s: ranks s, s+1, ..., s-1.
-template <typename T>
+template <typename T, typename TO>
 __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(
     SimtBwd p, const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ lse, const float* __restrict__ delta, const T* __restrict__ dO,
-    T* __restrict__ dk, T* __restrict__ dv) {
+    TO* __restrict__ dk, TO* __restrict__ dv) {
   const int lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (w >= (int64_t)p.B * p.Hkv * p.T) return;
@@ -191,17 +199,19 @@ __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(
   load_row(v + w * D, D, lane, vv);
   const int kpos = p.m.pos(slot);
   const int s = slot / p.m.c;
-  for (int i = 0; i < p.m.cp; ++i) {
-    const int r = (s + i) % p.m.cp;
+  const bool ag = p.ag_rank >= 0;
+  for (int i = 0; i < (ag ? 1 : p.m.cp); ++i) {
+    const int r = ag ? p.ag_rank : (s + i) % p.m.cp;
     for (int hh = 0; hh < p.n_rep; ++hh) {
       const int64_t qbh = (int64_t)b * p.Hq + g * p.n_rep + hh;
       for (int t = r * p.m.c; t < (r + 1) * p.m.c; ++t) {
         if (kpos > p.m.pos(t)) continue;
         const int64_t qrow = qbh * p.T + t;
+        const int64_t srow = ag ? qbh * p.m.c + (t - r * p.m.c) : qrow;  // dO / statistics
         const T* qr = q + qrow * D;
-        const T* dor = dO + qrow * D;
-        const float pr = expf(dot_row(kv_, qr, D, lane) * p.scale - lse[qrow]);
-        const float ds = pr * (dot_row(vv, dor, D, lane) - delta[qrow]);
+        const T* dor = dO + srow * D;
+        const float pr = expf(dot_row(kv_, qr, D, lane) * p.scale - lse[srow]);
+        const float ds = pr * (dot_row(vv, dor, D, lane) - delta[srow]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           int d = lane + 32 * j;
@@ -217,8 +227,13 @@ __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(
   for (int j = 0; j < 4; ++j) {
     int d = lane + 32 * j;
     if (d < D) {
-      dk[w * D + d] = from_f<T>(ak[j] * p.scale);
-      dv[w * D + d] = from_f<T>(av[j]);
+      float ok = ak[j] * p.scale, ov = av[j];
+      if (p.accumulate) {
+        ok += to_f(dk[w * D + d]);
+        ov += to_f(dv[w * D + d]);
+      }
+      dk[w * D + d] = from_f<TO>(ok);
+      dv[w * D + d] = from_f<TO>(ov);
     }
   }
 }
@@ -236,13 +251,17 @@ cudaError_t launch_simt_fwd(const Ring& R, int q_rank, int kv_rank, const void* 
   p.n_rep = R.Hq / R.Hkv;
   p.m = SeqMap::make(R.T, R.cp, R.zz);
   p.scale = R.scale;
-  const bool partial = q_rank >= 0;
-  p.q_slot0 = partial ? q_rank * p.m.c : 0;
-  p.n_q_slots = partial ? p.m.c : R.T;
+  // q_rank >= 0 with kv_rank >= 0: one ring step (float32 out); with kv_rank < 0:
+  // the all-gather mode (that rank's rows over every chunk, output dtype)
+  const bool local = q_rank >= 0;
+  const bool partial = local && kv_rank >= 0;
+  p.q_slot0 = local ? q_rank * p.m.c : 0;
+  p.n_q_slots = local ? p.m.c : R.T;
   p.kv_fixed = partial ? kv_rank : -1;
+  p.local_rows = local ? 1 : 0;
   const int64_t warps = (int64_t)p.B * p.Hq * p.n_q_slots;
   if (warps == 0) return cudaSuccess;
-  timing_begin(partial ? "simt_partial_fwd" : "simt_ring_fwd", st);
+  timing_begin(partial ? "simt_partial_fwd" : local ? "simt_allgather_fwd" : "simt_ring_fwd", st);
   if (R.bf16) {
     if (partial)
       simt_fwd_kernel<__nv_bfloat16, float><<<blocks_for(warps), 256, 0, st>>>(
@@ -271,6 +290,8 @@ static SimtBwd make_bwd(const Ring& R) {
   p.n_rep = R.Hq / R.Hkv;
   p.m = SeqMap::make(R.T, R.cp, R.zz);
   p.scale = R.scale;
+  p.ag_rank = -1;
+  p.accumulate = 0;
   return p;
 }
 
@@ -300,13 +321,43 @@ cudaError_t launch_simt_bwd_dkdv(const Ring& R, const void* q, const void* k, co
   const int64_t warps = (int64_t)p.B * p.Hkv * p.T;
   timing_begin("simt_bwd_dkdv", st);
   if (R.bf16)
-    simt_bwd_dkdv_kernel<__nv_bfloat16><<<blocks_for(warps), 256, 0, st>>>(
+    simt_bwd_dkdv_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks_for(warps), 256, 0, st>>>(
         p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
         (const __nv_bfloat16*)dO, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv);
   else
-    simt_bwd_dkdv_kernel<float><<<blocks_for(warps), 256, 0, st>>>(
+    simt_bwd_dkdv_kernel<float, float><<<blocks_for(warps), 256, 0, st>>>(
         p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
         (float*)dk, (float*)dv);
+  cudaError_t e = cudaGetLastError();
+  timing_end(st);
+  return e;
+}
+
+cudaError_t launch_simt_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,
+                                      const void* v, const float* lse, const float* delta,
+                                      const void* dO, void* dq, float* dk_sum, float* dv_sum,
+                                      int accumulate, cudaStream_t st) {
+  SimtBwd p = make_bwd(R);
+  p.ag_rank = q_rank;
+  p.accumulate = accumulate ? 1 : 0;
+  const int64_t q_warps = (int64_t)p.B * p.Hq * p.m.c;
+  const int64_t kv_warps = (int64_t)p.B * p.Hkv * p.T;
+  timing_begin("simt_allgather_bwd", st);
+  if (R.bf16) {
+    simt_bwd_dq_kernel<__nv_bfloat16><<<blocks_for(q_warps), 256, 0, st>>>(
+        p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
+        (const __nv_bfloat16*)dO, (__nv_bfloat16*)dq);
+    simt_bwd_dkdv_kernel<__nv_bfloat16, float><<<blocks_for(kv_warps), 256, 0, st>>>(
+        p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
+        (const __nv_bfloat16*)dO, dk_sum, dv_sum);
+  } else {
+    simt_bwd_dq_kernel<float><<<blocks_for(q_warps), 256, 0, st>>>(
+        p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
+        (float*)dq);
+    simt_bwd_dkdv_kernel<float, float><<<blocks_for(kv_warps), 256, 0, st>>>(
+        p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
+        dk_sum, dv_sum);
+  }
   cudaError_t e = cudaGetLastError();
   timing_end(st);
   return e;

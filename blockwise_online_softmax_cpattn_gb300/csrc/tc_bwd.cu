@@ -50,7 +50,24 @@ struct Params {
   void* out0;  // dkdv: dK ; dq: dQ
   void* out1;  // dkdv: dV
   int* status;
+  // All-gather mode (ag_rank >= 0): only rank ag_rank's query rows take part.  q
+  // holds the whole sequence; dO, the statistics and dQ hold the rank's c rows per
+  // (b, h); dK/dV are float32 and receive the rank's share, added to what they
+  // hold when `accumulate` is set.
+  int ag_rank;
+  int accumulate;
 };
+
+// Query tiles of rank r at positions >= kpos0 (chunk bounds and kpos0 lie on the
+// 128-token grid).
+__device__ __forceinline__ int rank_tiles_from(const SeqMap& m, int r, int kpos0) {
+  auto part = [&](int p0, int len) {
+    const int lo = p0 > kpos0 ? p0 : kpos0;
+    return lo < p0 + len ? (p0 + len - lo) >> 7 : 0;
+  };
+  if (!m.zz) return part(r * m.c, m.c);
+  return part(r * m.h, m.h) + part((2 * m.cp - 1 - r) * m.h, m.h);
+}
 
 __device__ __forceinline__ int classify(int qpos0, int kpos0) {
   if (kpos0 + kTile - 1 <= qpos0) return kFull;
@@ -112,7 +129,7 @@ struct DkdvSmem {
   static constexpr int kBytes = kMisc + 16;
 };
 
-template <int D>
+template <int D, bool AG>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -176,7 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // owner: ranks s, s+1, ..., s-1; every query head of the group per rank; tiles
   // that cannot see this K/V tile are skipped by every role alike
   auto walk_start = [&](TileWalk& w) {
-    w.start(p.m, s_own, p.m.cp, +1, p.n_rep);
+    if (AG) w.start(p.m, p.ag_rank, 1, +1, p.n_rep);  // all-gather: one rank's queries
+    else w.start(p.m, s_own, p.m.cp, +1, p.n_rep);
     while (!w.done() && classify(w.pos(), kpos0) == kEmpty) w.next();
   };
   auto walk_next = [&](TileWalk& w) {
@@ -201,20 +219,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       StageRing<DS> dr;
       TileWalk wk;
       for (walk_start(wk); !wk.done(); walk_next(wk)) {
-        const int qrow = (b * p.Hq + g * p.n_rep + wk.rep) * p.T + wk.slot();
+        const int qbh = b * p.Hq + g * p.n_rep + wk.rep;
+        const int qrow = qbh * p.T + wk.slot();
+        // rows of dO and of the statistics (the rank's own rows in all-gather mode)
+        const int srow = AG ? qbh * p.m.c + (wk.slot() - p.ag_rank * p.m.c) : qrow;
         if (!mbar_wait(q_empty(qr.stage), qr.par ^ 1, abort, p.status, kTimeoutNs)) break;
         mbar_expect_tx(q_full(qr.stage), L::kTB + 512);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kQ + qr.stage * L::kTB + kb * (kTile * 128), &tm_q, kb * 64, qrow,
                       q_full(qr.stage));
-        bulk_load(sbase + L::kLse + qr.stage * 512, p.lse2 + qrow, 512, q_full(qr.stage));
+        bulk_load(sbase + L::kLse + qr.stage * 512, p.lse2 + srow, 512, q_full(qr.stage));
         qr.mark_issued();
         if (!mbar_wait(do_empty(dr.stage), dr.par ^ 1, abort, p.status, kTimeoutNs)) break;
         mbar_expect_tx(do_full(dr.stage), L::kTB + 512);
         for (int kb = 0; kb < D / 64; ++kb)
           tma_load_2d(sbase + L::kDO + dr.stage * L::kTB + kb * (kTile * 128), &tm_do, kb * 64,
-                      qrow, do_full(dr.stage));
-        bulk_load(sbase + L::kDelta + dr.stage * 512, p.delta + qrow, 512, do_full(dr.stage));
+                      srow, do_full(dr.stage));
+        bulk_load(sbase + L::kDelta + dr.stage * 512, p.delta + srow, 512, do_full(dr.stage));
         dr.mark_issued();
         qr.advance();
         dr.advance();
@@ -293,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
       // every query tile at or after this K/V tile's position sees it, once per
       // query head of the group (the walk of the other roles skips the rest)
-      const int n_tiles = p.n_rep * ((p.T - kpos0) >> 7);
+      const int n_tiles = p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0)
+                                         : (p.T - kpos0) >> 7);
       bool ok = warp_wait(kv_full, 0, abort, p.status);
       tc_fence_after();
       StageRing<QS> qr;   // Q stage of tile t
@@ -464,7 +486,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       dr.advance();
     }
     if (ok && cnt > 0) ok = warp_wait(final_bar, 0, abort, p.status);
-    if (ok) {
+    if (ok && AG) {
+      // all-gather: float32 share of this rank's queries, added to the sum so far
+      tc_fence_after();
+      const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
+      float* dkf = static_cast<float*>(p.out0) + orow * D + half * (D / 2);
+      float* dvf = static_cast<float*>(p.out1) + orow * D + half * (D / 2);
+      if (cnt > 0 || !p.accumulate) {
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          for (int which = 0; which < 2; ++which) {
+            uint32_t v32[32];
+            if (cnt > 0) {
+              tmem_ld32(tmem + lane_off + 256 + which * D + half * (D / 2) + c * 32, v32);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v32[j] = 0u;
+            }
+            const float mul = which ? p.scale : 1.f;
+            float4* dst = reinterpret_cast<float4*>((which ? dkf : dvf) + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float4 x = make_float4(__uint_as_float(v32[4 * j]) * mul,
+                                     __uint_as_float(v32[4 * j + 1]) * mul,
+                                     __uint_as_float(v32[4 * j + 2]) * mul,
+                                     __uint_as_float(v32[4 * j + 3]) * mul);
+              if (p.accumulate) {
+                const float4 y = dst[j];
+                x.x += y.x;
+                x.y += y.y;
+                x.z += y.z;
+                x.w += y.w;
+              }
+              dst[j] = x;
+            }
+          }
+        }
+      }
+    } else if (ok) {
       tc_fence_after();
       const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
       __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(p.out0) + orow * D + half * (D / 2);
@@ -526,7 +586,8 @@ struct DqSmem {
 // latest query positions (the most keys) first.
 struct DqItem {
   int b, h, g, qpos0, qslot0, r_own;
-  int64_t qrow;
+  int64_t qrow;  // row of q
+  int64_t srow;  // row of dO, the statistics and dQ (the rank's own rows in all-gather mode)
   int kv_row_base;
 };
 
@@ -584,7 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Persistent: the CTAs stay resident and walk the items (latest query positions
   // first) in the order item_of gives; every pipeline keeps running across items.
-  const int n_q_tiles = p.T / kTile;
+  // all-gather mode: the rank's c/128 query tiles per (b, h); else all T/128
+  const bool ag = p.ag_rank >= 0;
+  const int n_q_tiles = (ag ? p.m.c : p.T) / kTile;
   const int n_items = p.B * p.Hq * n_q_tiles;
   auto decode = [&](int w) {
     DqItem it;
@@ -594,10 +657,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     it.b = rem / p.Hq;
     it.h = rem - it.b * p.Hq;
     it.g = it.h / p.n_rep;
-    it.qpos0 = (n_q_tiles - 1 - ti) * kTile;
-    it.qslot0 = p.m.slot(it.qpos0);
+    const int64_t bh = (int64_t)it.b * p.Hq + it.h;
+    if (ag) {
+      // the rank's later slots hold its later positions: heaviest first
+      it.qslot0 = p.ag_rank * p.m.c + (n_q_tiles - 1 - ti) * kTile;
+      it.qpos0 = p.m.pos(it.qslot0);
+      it.srow = bh * p.m.c + (it.qslot0 - p.ag_rank * p.m.c);
+    } else {
+      it.qpos0 = (n_q_tiles - 1 - ti) * kTile;
+      it.qslot0 = p.m.slot(it.qpos0);
+      it.srow = bh * p.T + it.qslot0;
+    }
     it.r_own = it.qslot0 / p.m.c;
-    it.qrow = ((int64_t)it.b * p.Hq + it.h) * p.T + it.qslot0;
+    it.qrow = bh * p.T + it.qslot0;
     it.kv_row_base = (it.b * p.Hkv + it.g) * p.T;
     return it;
   };
@@ -630,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(qdo_full, 2 * L::kTB);
         for (int kb = 0; kb < D / 64; ++kb) {
           tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)it.qrow, qdo_full);
-          tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)it.qrow, qdo_full);
+          tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)it.srow, qdo_full);
         }
         q_last = k;
         TileWalk wk;
@@ -783,8 +855,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int w;
     for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
       const DqItem it = decode(w);
-      const float2 nl2 = make_float2(p.lse2[it.qrow + row], p.lse2[it.qrow + row]);  // -LSE log2e
-      const float2 ndl = make_float2(p.delta[it.qrow + row], p.delta[it.qrow + row]);  // -Delta
+      const float2 nl2 = make_float2(p.lse2[it.srow + row], p.lse2[it.srow + row]);  // -LSE log2e
+      const float2 ndl = make_float2(p.delta[it.srow + row], p.delta[it.srow + row]);  // -Delta
       int cnt = 0;  // tiles of this item
       TileWalk wk;
       for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
@@ -847,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       tc_fence_after();
       __nv_bfloat16* dq =
-          static_cast<__nv_bfloat16*>(p.out0) + (it.qrow + row) * D + half * (D / 2);
+          static_cast<__nv_bfloat16*>(p.out0) + (it.srow + row) * D + half * (D / 2);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v32[32];
@@ -885,21 +957,24 @@ template <int D>
 static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, const void* k,
                            const void* v, const void* dO, void* dq, void* dk, void* dv,
                            cudaStream_t st) {
+  const bool ag = base.ag_rank >= 0;
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t qrows = (uint64_t)R.B * R.Hq * R.T, krows = (uint64_t)R.B * R.Hkv * R.T;
+  const uint64_t dorows = ag ? (uint64_t)R.B * R.Hq * (R.T / R.cp) : qrows;
   if (encode_tmap_2d_bf16(&tq, q, D, qrows, 64, kTile) != CUDA_SUCCESS ||
-      encode_tmap_2d_bf16(&tdo, dO, D, qrows, 64, kTile) != CUDA_SUCCESS ||
+      encode_tmap_2d_bf16(&tdo, dO, D, dorows, 64, kTile) != CUDA_SUCCESS ||
       encode_tmap_2d_bf16(&tk, k, D, krows, 64, kTile) != CUDA_SUCCESS ||
       encode_tmap_2d_bf16(&tv, v, D, krows, 64, kTile) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   Params pk = base;
   pk.out0 = dk;
   pk.out1 = dv;
-  cudaError_t e = prep(dkdv_kernel<D>, DkdvSmem<D>::kBytes);
+  auto kdkdv = ag ? dkdv_kernel<D, true> : dkdv_kernel<D, false>;
+  cudaError_t e = prep(kdkdv, DkdvSmem<D>::kBytes);
   if (e != cudaSuccess) return e;
   const int kv_items = R.B * R.Hkv * (R.T / kTile);
-  timing_begin("tc_bwd_dkdv", st);
-  dkdv_kernel<D><<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pk);
+  timing_begin(ag ? "tc_allgather_dkdv" : "tc_bwd_dkdv", st);
+  kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pk);
   e = cudaGetLastError();
   timing_end(st);
   if (e != cudaSuccess) return e;
@@ -908,13 +983,13 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   pq.out1 = nullptr;
   e = prep(dq_kernel<D>, DqSmem<D>::kBytes);
   if (e != cudaSuccess) return e;
-  const int q_items = R.B * R.Hq * (R.T / kTile);
+  const int q_items = R.B * R.Hq * ((ag ? R.T / R.cp : R.T) / kTile);
   // persistent: at most one resident CTA per SM, each walking its share of the items
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  timing_begin("tc_bwd_dq", st);
+  timing_begin(ag ? "tc_allgather_dq" : "tc_bwd_dq", st);
   dq_kernel<D><<<q_items < sms ? q_items : sms, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
   e = cudaGetLastError();
   timing_end(st);
@@ -923,9 +998,8 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
 
 }  // namespace tcbwd
 
-cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
-                          const float* lse2, const float* delta, const void* dO, void* dq,
-                          void* dk, void* dv, int* status, cudaStream_t st) {
+static tcbwd::Params bwd_params(const Ring& R, const float* lse2, const float* delta,
+                                int* status) {
   tcbwd::Params p;
   p.B = R.B;
   p.Hq = R.Hq;
@@ -938,8 +1012,28 @@ cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const voi
   p.lse2 = lse2;
   p.delta = delta;
   p.status = status;
+  p.ag_rank = -1;
+  p.accumulate = 0;
+  return p;
+}
+
+cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
+                          const float* lse2, const float* delta, const void* dO, void* dq,
+                          void* dk, void* dv, int* status, cudaStream_t st) {
+  const tcbwd::Params p = bwd_params(R, lse2, delta, status);
   if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st);
   return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st);
+}
+
+cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,
+                                    const void* v, const float* lse2, const float* delta,
+                                    const void* dO, void* dq, float* dk_sum, float* dv_sum,
+                                    int accumulate, int* status, cudaStream_t st) {
+  tcbwd::Params p = bwd_params(R, lse2, delta, status);
+  p.ag_rank = q_rank;
+  p.accumulate = accumulate ? 1 : 0;
+  if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk_sum, dv_sum, st);
+  return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk_sum, dv_sum, st);
 }
 
 }  // namespace cpattn

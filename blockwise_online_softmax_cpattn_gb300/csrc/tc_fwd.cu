@@ -70,7 +70,10 @@ struct Params {
   float scale_log2;
   int q_tiles;          // 128-row query tiles per (batch, head) in the launch
   int n_items;          // work items (B * Hq * q_tiles), walked by resident CTAs
-  int q_rank, kv_rank;  // partial mode when q_rank >= 0
+  // q_rank >= 0: only that rank's query rows, written as c rows per (b, h); with
+  // kv_rank >= 0 against that one chunk (a ring step), with kv_rank < 0 against
+  // every chunk (the all-gather mode)
+  int q_rank, kv_rank;
   void* o;
   float* lse;
   int* status;
@@ -112,7 +115,9 @@ __device__ __forceinline__ Item decode(const Params& p, int w) {
   it.h = rem - it.b * p.Hq;
   it.g = it.h / p.n_rep;
   if (p.q_rank >= 0) {
-    it.slot0 = p.q_rank * p.m.c + ti * kTile;
+    // the rank's later slots hold its later positions (its second zigzag half):
+    // heaviest first
+    it.slot0 = p.q_rank * p.m.c + (p.q_tiles - 1 - ti) * kTile;
     it.pos0 = p.m.pos(it.slot0);
   } else {
     // heaviest (latest) query positions first: causal work grows with position
@@ -201,8 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // K/V tiles of an item in ring order: chunks r, r-1, ..., r-cp+1 (mod cp), or one
   // chunk; every role walks the same list and skips the tiles the causal mask hides
+  const bool one_chunk = p.q_rank >= 0 && p.kv_rank >= 0;
   auto walk_start = [&](TileWalk& w, const Item& it) {
-    w.start(p.m, p.q_rank >= 0 ? p.kv_rank : it.rank, p.q_rank >= 0 ? 1 : p.m.cp, -1, 1);
+    w.start(p.m, one_chunk ? p.kv_rank : it.rank, one_chunk ? 1 : p.m.cp, -1, 1);
     while (!w.done() && classify(it.pos0, w.pos()) == kEmpty) w.next();
   };
   auto walk_next = [&](TileWalk& w, const Item& it) {
@@ -485,10 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lsum = w0 * l0 + w1 * l1;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const float a0 = w0 * inv, a1 = w1 * inv;
-      const bool partial = p.q_rank >= 0;
+      const bool local = p.q_rank >= 0;
       const int64_t bh = (int64_t)it.b * p.Hq + it.h;
-      const int64_t orow = partial ? bh * p.m.c + (it.slot0 - p.q_rank * p.m.c) + row
-                                   : bh * p.T + it.slot0 + row;
+      const int64_t orow = local ? bh * p.m.c + (it.slot0 - p.q_rank * p.m.c) + row
+                                 : bh * p.T + it.slot0 + row;
       // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
@@ -580,9 +586,12 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
   p.n_rep = R.Hq / R.Hkv;
   p.m = SeqMap::make(R.T, R.cp, R.zz);
   p.scale_log2 = R.scale * 1.44269504088896340736f;
-  const bool partial = q_rank >= 0;
-  p.q_tiles = (partial ? p.m.c : R.T) / tcfwd::kTile;
-  p.q_rank = partial ? q_rank : -1;
+  // q_rank >= 0: one rank's rows; with kv_rank >= 0 one ring step (float32 out),
+  // with kv_rank < 0 the all-gather mode (output dtype)
+  const bool local = q_rank >= 0;
+  const bool partial = local && kv_rank >= 0;
+  p.q_tiles = (local ? p.m.c : R.T) / tcfwd::kTile;
+  p.q_rank = local ? q_rank : -1;
   p.kv_rank = partial ? kv_rank : -1;
   p.o = o;
   p.lse = lse;
@@ -591,7 +600,7 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
   const int items = R.B * R.Hq * p.q_tiles;
   if (items == 0) return cudaSuccess;
   p.n_items = items;
-  timing_begin(partial ? "tc_partial_fwd" : "tc_ring_fwd", st);
+  timing_begin(partial ? "tc_partial_fwd" : local ? "tc_allgather_fwd" : "tc_ring_fwd", st);
   cudaError_t e;
   if (R.D == 128)
     e = partial ? run_fwd<128, true>(R, p, items, q, k, v, st)

@@ -179,6 +179,55 @@ cpattn_status cpattn_ring_bwd_noalloc(const cpattn_desc* desc, const void* q, co
                                       void* stream);
 
 /*
+ * All-gather mode, forward (pull request #181, mode table row "all_gather": the
+ * K/V of every rank is gathered and the rank's own queries attend to it; tutorial
+ * "上下文并行", section "Zig-Zag Ring Attention 的通信与计算重叠", bullet
+ * "all-gather": each GPU receives the complete K/V in one collective).  Rank
+ * q_rank's query rows attend to every key at or before their global position in
+ * one pass: no ring steps and no merge.
+ *   q, k, v : full layout-order tensors (the rank's rows are q's slots
+ *             [q_rank*c, (q_rank+1)*c); k and v are the gathered sequence)
+ *   o       : [B', H_q', c, D], dtype desc->dtype (the rank's rows, slot order)
+ *   lse     : [B', H_q', c] float32, natural logarithm
+ * (B', H_q', c as for cpattn_partial_fwd.)
+ * Errors: q_rank outside [0, cp/a2a) -> CPATTN_ERR_INVALID_ARG.
+ */
+cpattn_status cpattn_allgather_fwd(const cpattn_desc* desc, int q_rank, const void* q,
+                                   const void* k, const void* v, void* o, float* lse,
+                                   void* stream);
+
+/* Bytes of device workspace cpattn_allgather_bwd needs (float32 row statistics of
+ * one rank's rows). */
+size_t cpattn_allgather_bwd_workspace(const cpattn_desc* desc);
+
+/*
+ * All-gather mode, backward (pull request #181, mode table row "all_gather": the
+ * K/V gradients of all ranks are summed by a ReduceScatter).  Computes rank
+ * q_rank's dQ and its share of the K/V gradient of the whole sequence, and adds
+ * that share into float32 sums, which is the ReduceScatter's addition:
+ *   q, k, v          : full layout-order tensors
+ *   o, lse, dO       : the rank's rows, as cpattn_allgather_fwd returns them
+ *                      ([B', H_q', c, D], [B', H_q', c] float32, [B', H_q', c, D])
+ *   dq               : [B', H_q', c, D], dtype desc->dtype
+ *   dk_sum, dv_sum   : [B', H_kv', T, D] float32, layout order.  accumulate = 0
+ *                      overwrites them with the rank's share, 1 adds the share to
+ *                      what they hold.  Calling q_rank = 0 (accumulate 0), then
+ *                      1, ..., cp/a2a - 1 (accumulate 1) in order on one stream
+ *                      leaves the full dK, dV: rank s's slice [s*c, (s+1)*c) is
+ *                      what s receives from the ReduceScatter.
+ *   workspace        : at least cpattn_allgather_bwd_workspace(desc) bytes
+ *                      (smaller -> CPATTN_ERR_INVALID_ARG); contents on entry do
+ *                      not matter.
+ * Errors: q_rank outside [0, cp/a2a) or accumulate not 0/1 -> CPATTN_ERR_INVALID_ARG;
+ * others as cpattn_ring_bwd.
+ */
+cpattn_status cpattn_allgather_bwd(const cpattn_desc* desc, int q_rank, const void* q,
+                                   const void* k, const void* v, const void* o,
+                                   const float* lse, const void* dO, void* dq, float* dk_sum,
+                                   float* dv_sum, int accumulate, void* workspace,
+                                   size_t ws_bytes, void* stream);
+
+/*
  * Permutes one tensor of n_heads heads (H_q or H_kv) between orders:
  *  CPATTN_ZIGZAG_FWD / _INV : [B][n_heads][T][D] natural <-> layout order of
  *      desc->layout over the ring's cp/a2a ranks (tutorial, section "Zig-Zag Ring

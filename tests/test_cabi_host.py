@@ -64,6 +64,10 @@ def test_invalid_descriptors_are_rejected(cp, kw, code):
                               1 << 30, 0) == code
     assert cp.cpattn_partial_fwd(d, 0, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == code
     assert cp.cpattn_ring_bwd_workspace(d) == 0
+    assert cp.cpattn_allgather_fwd(d, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == code
+    assert cp.cpattn_allgather_bwd(d, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0,
+                                   FAKE, 1 << 30, 0) == code
+    assert cp.cpattn_allgather_bwd_workspace(d) == 0
 
 
 def test_null_and_misaligned_pointers(cp):
@@ -99,3 +103,19 @@ def test_timing_table_host_side(cp):
     assert cp.cpattn_timing_enable(False) == 0
     assert cp.cpattn_timing_collect() == 0
     assert cp.cpattn_timing_table() == {}
+
+
+def test_allgather_ranks_flags_and_workspace_are_checked(cp):
+    d = _desc(cp)  # cp = 2: ranks 0 and 1
+    assert cp.cpattn_allgather_fwd(d, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert cp.cpattn_allgather_fwd(d, -1, FAKE, FAKE, FAKE, FAKE, FAKE, 0) == 1
+    assert cp.cpattn_allgather_fwd(d, 0, FAKE, FAKE, FAKE, FAKE + 8, FAKE, 0) == 1
+    need = cp.cpattn_allgather_bwd_workspace(d)
+    # Delta and the base-2 LSE of one rank's rows: B * H_q * T / cp floats each
+    assert need >= 2 * 1 * 4 * 256 * 4 and need % 256 == 0
+    assert need < cp.cpattn_ring_bwd_workspace(d)
+    args = [FAKE] * 8
+    assert cp.cpattn_allgather_bwd(d, 2, *args, 0, FAKE, need, 0) == 1
+    assert cp.cpattn_allgather_bwd(d, 0, *args, 2, FAKE, need, 0) == 1      # accumulate: 0 or 1
+    assert cp.cpattn_allgather_bwd(d, 0, *args, 1, FAKE, need - 1, 0) == 1  # workspace too small
+    assert cp.cpattn_allgather_bwd(d, 0, *args[:7], 0, 1, FAKE, need, 0) == 1  # null dv_sum
