@@ -13,6 +13,12 @@ before every timed step.
 --impl reference times the FP64 CPU oracle (the only reference there is) on the
 host cores, each step a bounded sample of the same workload.
 
+--mode allgather times the all-gather mode instead (pull request #181, mode table
+row "all_gather"): one step = cpattn_allgather_fwd and cpattn_allgather_bwd for
+every emulated rank, with the layout-order q, k, v and each rank's dO rows already
+in HBM; the ranks' K/V gradient shares are summed in float32 (the mode's
+ReduceScatter).  Same FLOP count as the ring.
+
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl cpattn|reference]
         [--workload NAME]; for N > 1 under torch.distributed.run, one independent
 replica of the workload per GPU (no data exchange; weak scaling).
@@ -50,6 +56,7 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="ring", choices=["ring", "allgather"])
     return ap.parse_args()
 
 
@@ -146,6 +153,13 @@ def kernel_flops_or_bytes(name, w):
         return "tensor", 8.0 * w.D * pairs
     if name in ("tc_bwd_dq", "simt_bwd_dq"):         # the dQ product only
         return "tensor", 2.0 * w.D * pairs
+    # all-gather mode: one launch covers one rank's rows (1/cp of the pairs on average)
+    if name == "tc_allgather_fwd":
+        return "tensor", 4.0 * w.D * pairs / w.cp
+    if name == "tc_allgather_dkdv":
+        return "tensor", 8.0 * w.D * pairs / w.cp
+    if name == "tc_allgather_dq":
+        return "tensor", 2.0 * w.D * pairs / w.cp
     if name == "bwd_prepass":
         return "hbm", 2.0 * rows_q * w.D * elt + 12.0 * rows_q
     if name.startswith("layout"):                    # per launch: one tensor read + written
@@ -375,6 +389,145 @@ def run_cpattn(args, rank, world):
     return out
 
 
+def run_allgather(args, rank, world):
+    """The all-gather mode: every emulated rank's forward and backward per step."""
+    import torch
+    import blockwise_online_softmax_cpattn_gb300 as cp
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.ALL[args.workload]
+    if w.a2a != 1:
+        raise SystemExit("--mode allgather takes a plain ring workload (a2a = 1)")
+    stream = torch.cuda.current_stream()
+    desc = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, w.D, w.cp, w.layout, w.dtype)
+    dt = W.torch_dtype(w)
+    c = w.T // w.cp
+    nat = W.draw_cast(w)
+    # inputs as the ranks hold them: the gathered q, k, v in layout order, and each
+    # rank's own dO rows; prepared once, outside the timed region
+    H = [w.H_q, w.H_kv, w.H_kv, w.H_q]
+    lay = []
+    for x, h in zip(nat, H):
+        y = torch.empty(w.B, h, w.T, w.D, dtype=dt, device=dev)
+        cp.check(cp.cpattn_layout(cp.ZIGZAG_FWD, desc, x.to(dev), y, h))
+        lay.append(y)
+    ql, kl, vl, dol = lay
+    do_r = [dol[:, :, r * c:(r + 1) * c].contiguous() for r in range(w.cp)]
+    o_r = [torch.empty(w.B, w.H_q, c, w.D, dtype=dt, device=dev) for _ in range(w.cp)]
+    lse_r = [torch.empty(w.B, w.H_q, c, dtype=torch.float32, device=dev) for _ in range(w.cp)]
+    dq_r = [torch.empty_like(o) for o in o_r]
+    dk_sum = torch.empty(w.B, w.H_kv, w.T, w.D, dtype=torch.float32, device=dev)
+    dv_sum = torch.empty_like(dk_sum)
+    ws = torch.empty(cp.cpattn_allgather_bwd_workspace(desc), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        for r in range(w.cp):
+            cp.check(cp.cpattn_allgather_fwd(desc, r, ql, kl, vl, o_r[r], lse_r[r]))
+        for r in range(w.cp):
+            cp.check(cp.cpattn_allgather_bwd(desc, r, ql, kl, vl, o_r[r], lse_r[r], do_r[r],
+                                             dq_r[r], dk_sum, dv_sum, r > 0, ws))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cp.check(cp.cpattn_check())
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    cp.check(cp.cpattn_check())
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, dev)
+    flops = w.fwd_flops + w.bwd_flops
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    cp.cpattn_timing_reset()
+    cp.cpattn_timing_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    cp.check(cp.cpattn_timing_collect())
+    cp.cpattn_timing_enable(False)
+    table = cp.cpattn_timing_table()
+    cp.cpattn_timing_reset()
+    launches_per_step = sum(n for _, n in table.values()) / args.steps
+    kernels = {name: {"avg_ms": tot / n, "launches": n, "share": tot / sum(t for t, _ in table.values())}
+               for name, (tot, n) in table.items()}
+    dom = max(table, key=lambda n: table[n][0])
+    pk, src_pk = peaks()
+    bound, work = kernel_flops_or_bytes(dom, w)
+    avg_ms = table[dom][0] / table[dom][1]
+    if bound == "tensor":
+        achieved = work / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                "peak_source": f"{src_pk} bf16 dense burst (cuBLAS)",
+                "work_per_launch": work, "avg_launch_ms": avg_ms,
+                "note": "work per launch is the average over the ranks (pairs / cp)"}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": None}
+    roof["traffic"] = None
+
+    # end to end: the ranks' inputs uploaded from pinned host memory and their
+    # outputs (o, dq rows, float32 dK/dV sums) read back, inside each step's events
+    h_in = [x.cpu().pin_memory() for x in (ql, kl, vl)] + [x.cpu().pin_memory() for x in do_r]
+    d_in = [ql, kl, vl] + do_r
+    d_out = o_r + dq_r + [dk_sum, dv_sum]
+    h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in d_out]
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_e2e)]
+    torch.cuda.synchronize()
+    for a, b in ev2:
+        flush.zero_()
+        a.record(stream)
+        for d_, h_ in zip(d_in, h_in):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(h_out, d_out):
+            h_.copy_(d_, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(cp.cpattn_check())
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev2), world, dev)
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "transfers": "pinned host buffers, on the step's stream"}
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": config_of(w, {
+                "mode": "all_gather",
+                "parallelism": "replicas" if world > 1 else "single GPU, cp ranks emulated",
+                "l2": "flushed before every timed step (256 MiB device write, outside the events)",
+                "step": "for every rank: cpattn_allgather_fwd, then for every rank: "
+                        "cpattn_allgather_bwd (K/V gradient shares summed in float32)",
+                "pct_of_bf16_peak": value / world / pk["bf16_tflops"], "peak_source": src_pk}),
+            "roofline": roof, "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clocks, "e2e": e2e, "kernels": kernels}
+
+
 # ---------------------------------------------------------------------------
 # the oracle (CPU) legs
 # ---------------------------------------------------------------------------
@@ -459,7 +612,7 @@ def main():
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend)
-    out = run_cpattn(args, rank, world)
+    out = run_allgather(args, rank, world) if args.mode == "allgather" else run_cpattn(args, rank, world)
     if rank == 0:
         w = W.ALL[args.workload]
         if world == 1 and not args.no_cpu_baseline:

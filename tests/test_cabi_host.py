@@ -53,6 +53,7 @@ FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
     (dict(cp=0), 1),
     (dict(a2a=3, cp=2), 1),                  # a2a must divide cp
     (dict(a2a=2, cp=4, H_kv=1, H_q=4), 1),   # heads must split over a2a
+    (dict(a2a=4, cp=4, H_kv=2, H_q=8), 1),   # full Ulysses (a2a = cp): H_kv % cp != 0
     (dict(layout=7), 1),
     (dict(dtype=5), 1),
     (dict(B=0), 1),

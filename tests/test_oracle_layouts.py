@@ -103,7 +103,9 @@ def test_chunk_pair_flops_match_the_page():
 
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 @pytest.mark.parametrize("B,H,T,cp,a2a", [(1, 8, 64, 8, 2), (2, 4, 32, 4, 2), (1, 6, 48, 6, 3),
-                                          (1, 4, 16, 2, 2), (1, 4, 32, 4, 1)])
+                                          (1, 4, 16, 2, 2), (1, 4, 32, 4, 1),
+                                          # full Ulysses (a2a = cp, p2p = 1)
+                                          (1, 8, 64, 4, 4), (2, 8, 64, 8, 8)])
 def test_a2a_round_trip_and_structure(rng, B, H, T, cp, a2a, layout):
     D = 3
     nat = rng.standard_normal((B, H, T, D))

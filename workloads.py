@@ -70,14 +70,18 @@ LLAMA = Workload("llama_gqa_T8192_cp8_zigzag", 1, 32, 8, 8192, 128, 8, "zigzag",
 QWEN3 = Workload("qwen3_gqa_T32768_a2a2_p2p4_zigzag", 1, 32, 4, 32768, 128, 8, "zigzag",
                  "bf16", a2a=2)
 LONG = Workload("long_T131072_zigzag", 1, 8, 8, 131072, 128, 8, "zigzag", "bf16")
+# the full Ulysses mode (a2a = cp, so the ring has one rank): the LLaMA shape with the
+# all-to-all over all 8 ranks, each then holding 4 query heads and 1 K/V head of the
+# whole sequence
+ULYSSES = Workload("llama_gqa_T8192_ulysses8", 1, 32, 8, 8192, 128, 8, "zigzag", "bf16", a2a=8)
 
 GPT2_VARIANTS = [GPT2.replace(cp=cp, layout=lay, name=f"gpt2_small_T1024_cp{cp}_{lay}")
                  for cp in (2, 4) for lay in ("contiguous", "zigzag")]
 GPT2_STRESS = GPT2.replace(seed=1, q_scale=4.0, name="gpt2_small_T1024_q4")
 LONG_SWEEP = [LONG.replace(cp=cp, name=f"long_T131072_cp{cp}_zigzag") for cp in (4, 8, 16, 32)]
 
-ALL = {w.name: w for w in [TINY, GPT2, LLAMA, QWEN3, LONG, GPT2_STRESS, *GPT2_VARIANTS,
-                           *LONG_SWEEP]}
+ALL = {w.name: w for w in [TINY, GPT2, LLAMA, QWEN3, LONG, ULYSSES, GPT2_STRESS,
+                           *GPT2_VARIANTS, *LONG_SWEEP]}
 
 
 def draw(w: Workload, seed: Optional[int] = None):
