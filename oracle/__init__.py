@@ -15,6 +15,9 @@ What it computes, in plain numpy float64, following the pages' definitions:
   plus the (O, LSE) merge of two partial results, and one rank's share of the
   all-gather mode (pull request #181, mode table row "all_gather": local queries
   over the gathered K/V; K/V gradients summed over ranks by a ReduceScatter).
+  Packed sequences: causal attention inside each document of a packed row
+  (transformers pull request #50497: position ids restart mid-sequence and the
+  mask is rebuilt for the packed documents).
 * ``layouts``: the contiguous and zigzag (head-tail paired) token-to-rank maps
   (tutorial, section "Zig-Zag Ring Attention") and the all-to-all
   head<->sequence re-layout of the hierarchical a2a+p2p mode (pull request #181,

@@ -281,3 +281,65 @@ def allgather_bwd(q, k, v, do, scale, q_pos):
             dk[b, g] += scale * (dS.T @ q[b, h, q_pos])
             dv[b, g] += P.T @ dO
     return dq, dk, dv
+
+
+# ----------------------------------------------------------------------------
+# Packed sequences (transformers pull request #50497, the packed variant of the
+# context-parallel tests: position_ids restart mid-sequence, and the mask has to
+# be rebuilt for the packed documents; InfiniTrain pull request #181 lists packed /
+# variable-length sequences as not covered).  Every batch row holds n_docs
+# documents back to back, document d at natural positions [starts[b, d],
+# starts[b, d + 1]); a token attends to the keys of its own document at or before
+# it: causal attention with the position restarting at every document.
+# ----------------------------------------------------------------------------
+
+def doc_of(starts_row, pos):
+    """Document index of each natural position (starts_row: [n_docs + 1])."""
+    return np.searchsorted(np.asarray(starts_row), np.asarray(pos), side="right") - 1
+
+
+def packed_visible(q_pos, k_pos, starts_row):
+    """Boolean [len(q_pos), len(k_pos)]: causal and in the same document."""
+    dq = doc_of(starts_row, q_pos)
+    dk = doc_of(starts_row, k_pos)
+    return causal_visible(q_pos, k_pos) & (dk[None, :] == dq[:, None])
+
+
+def packed_attention_fwd(q, k, v, scale, starts):
+    """Forward of packed causal attention in natural order; starts [B, n_docs + 1]."""
+    B, H_q, T, D = q.shape
+    n_rep = _group(H_q, k.shape[1])
+    o = np.empty_like(q)
+    lse = np.empty((B, H_q, T))
+    pos = np.arange(T)
+    for b in range(B):
+        vis = packed_visible(pos, pos, starts[b])
+        for h in range(H_q):
+            g = h // n_rep
+            P, m, l = safe_softmax_rows(scores(q[b, h], k[b, g], scale), vis)
+            o[b, h] = P @ v[b, g]
+            lse[b, h] = m + np.log(l)
+    return o, lse
+
+
+def packed_attention_bwd(q, k, v, do, scale, starts):
+    """Analytic backward of packed causal attention (definition as above, with the
+    packed mask).  Returns (dQ, dK, dV)."""
+    B, H_q, T, D = q.shape
+    n_rep = _group(H_q, k.shape[1])
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    pos = np.arange(T)
+    for b in range(B):
+        vis = packed_visible(pos, pos, starts[b])
+        for h in range(H_q):
+            g = h // n_rep
+            P, _, _ = safe_softmax_rows(scores(q[b, h], k[b, g], scale), vis)
+            O = P @ v[b, g]
+            delta = np.sum(do[b, h] * O, axis=1)
+            dS = P * (do[b, h] @ v[b, g].T - delta[:, None])
+            dq[b, h] = scale * (dS @ k[b, g])
+            dk[b, g] += scale * (dS.T @ q[b, h])
+            dv[b, g] += P.T @ do[b, h]
+    return dq, dk, dv

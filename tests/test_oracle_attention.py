@@ -295,3 +295,67 @@ def test_allgather_rank_share_finite_differences(rng):
     # keys after the rank's last query position get nothing from it
     later = np.arange(T) > pos.max()
     assert np.all(dk[:, :, later] == 0) and np.all(dv[:, :, later] == 0)
+
+
+# ---------------------------------------------------------------------------
+# Packed sequences (position restart at every document)
+# ---------------------------------------------------------------------------
+
+def test_packed_equals_documents_alone(rng):
+    """Each document of a packed row is attended exactly as if it were a sequence
+    of its own (positions restarting at 0); the backward likewise."""
+    T, D = 40, 6
+    q, k, v, do = _rand(rng, 2, 4, 2, T, D)
+    starts = np.array([[0, 7, 7, 23, 40], [0, 1, 19, 33, 40]])   # one empty document
+    scale = 0.5
+    o, lse = A.packed_attention_fwd(q, k, v, scale, starts)
+    dq, dk, dv = A.packed_attention_bwd(q, k, v, do, scale, starts)
+    for b in range(2):
+        for d in range(starts.shape[1] - 1):
+            s0, s1 = starts[b, d], starts[b, d + 1]
+            if s1 == s0:
+                continue
+            sl = slice(s0, s1)
+            ro, rl = A.attention_fwd(q[b:b + 1, :, sl], k[b:b + 1, :, sl], v[b:b + 1, :, sl], scale)
+            rq, rk, rv = A.attention_bwd(q[b:b + 1, :, sl], k[b:b + 1, :, sl], v[b:b + 1, :, sl],
+                                         do[b:b + 1, :, sl], scale)
+            assert rel_err(o[b:b + 1, :, sl], ro) < 1e-13
+            assert rel_err(lse[b:b + 1, :, sl], rl) < 1e-13
+            assert rel_err(dq[b:b + 1, :, sl], rq) < 1e-12
+            assert rel_err(dk[b:b + 1, :, sl], rk) < 1e-12
+            assert rel_err(dv[b:b + 1, :, sl], rv) < 1e-12
+
+
+def test_packed_matches_torch_masked_sdpa(rng):
+    """The library routine with the packed boolean mask, plus autograd."""
+    T, D = 33, 5
+    q, k, v, do = _rand(rng, 1, 4, 1, T, D)
+    starts = np.array([[0, 10, 11, 33]])
+    scale = 0.45
+    o, lse = A.packed_attention_fwd(q, k, v, scale, starts)
+    dq, dk, dv = A.packed_attention_bwd(q, k, v, do, scale, starts)
+    pos = np.arange(T)
+    doc = np.searchsorted(starts[0], pos, side="right") - 1
+    mask = torch.tensor((pos[None, :] <= pos[:, None]) & (doc[None, :] == doc[:, None]))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    kr, vr = tk.repeat_interleave(4, dim=1), tv.repeat_interleave(4, dim=1)
+    to = torch.nn.functional.scaled_dot_product_attention(tq, kr, vr, attn_mask=mask, scale=scale)
+    (to * torch.tensor(do)).sum().backward()
+    s_ = (scale * tq.detach() @ kr.detach().transpose(-1, -2)).masked_fill(~mask, float("-inf"))
+    assert rel_err(o, to.detach().numpy()) < 1e-13
+    assert rel_err(lse, torch.logsumexp(s_, dim=-1).numpy()) < 1e-13
+    assert rel_err(dq, tq.grad.numpy()) < 1e-12
+    assert rel_err(dk, tk.grad.numpy()) < 1e-12
+    assert rel_err(dv, tv.grad.numpy()) < 1e-12
+
+
+def test_packed_single_document_is_causal(rng):
+    q, k, v, do = _rand(rng, 1, 2, 2, 24, 4)
+    starts = np.array([[0, 24]])
+    o, lse = A.packed_attention_fwd(q, k, v, 0.3, starts)
+    ro, rl = A.attention_fwd(q, k, v, 0.3)
+    assert rel_err(o, ro) < 1e-14 and rel_err(lse, rl) < 1e-14
+    g = A.packed_attention_bwd(q, k, v, do, 0.3, starts)
+    r = A.attention_bwd(q, k, v, do, 0.3)
+    for a_, b_ in zip(g, r):
+        assert rel_err(a_, b_) < 1e-13
