@@ -66,6 +66,11 @@ _sigs = {
                               _vp, _vp, ctypes.c_size_t, _vp]),
     "cpattn_ring_bwd_noalloc": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _vp]),
+    "cpattn_packed_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
+    "cpattn_ring_fwd_packed": (_st, [ctypes.POINTER(CpattnDesc), _vp, ctypes.c_int, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "cpattn_ring_bwd_packed": (_st, [ctypes.POINTER(CpattnDesc), _vp, ctypes.c_int, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "cpattn_allgather_fwd": (_st, [ctypes.POINTER(CpattnDesc), ctypes.c_int, _vp, _vp, _vp, _vp,
                                    _vp, _vp]),
     "cpattn_allgather_bwd_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
@@ -148,6 +153,29 @@ def cpattn_ring_bwd_noalloc(desc, q, k, v, o, lse, dO, dq, dk, dv, stream=None) 
     return _lib.cpattn_ring_bwd_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                         _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
                                         _stream(stream))
+
+
+def cpattn_packed_workspace(desc) -> int:
+    return _lib.cpattn_packed_workspace(ctypes.byref(desc))
+
+
+def _ws_bytes(workspace, ws_bytes):
+    return workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+
+
+def cpattn_ring_fwd_packed(desc, starts, n_docs, q, k, v, o, lse, workspace, ws_bytes=None,
+                           stream=None) -> int:
+    return _lib.cpattn_ring_fwd_packed(ctypes.byref(desc), _ptr(starts), n_docs, _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                       _ws_bytes(workspace, ws_bytes), _stream(stream))
+
+
+def cpattn_ring_bwd_packed(desc, starts, n_docs, q, k, v, o, lse, dO, dq, dk, dv, workspace,
+                           ws_bytes=None, stream=None) -> int:
+    return _lib.cpattn_ring_bwd_packed(ctypes.byref(desc), _ptr(starts), n_docs, _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                       _ptr(dv), _ptr(workspace), _ws_bytes(workspace, ws_bytes),
+                                       _stream(stream))
 
 
 def cpattn_allgather_fwd(desc, q_rank, q, k, v, o, lse, stream=None) -> int:

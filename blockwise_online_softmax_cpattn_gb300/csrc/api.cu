@@ -243,6 +243,81 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
 }
 
 // ---------------------------------------------------------------------------
+// packed sequences
+// ---------------------------------------------------------------------------
+// Workspace: lo, hi (int32 per batch row and position), then the backward's
+// statistics as for cpattn_ring_bwd; each section 256-byte aligned.
+static size_t doc_section(const cpattn_desc* desc) {
+  return ((size_t)desc->B * desc->T * sizeof(int) + 255) / 256 * 256;
+}
+
+size_t cpattn_packed_workspace(const cpattn_desc* desc) {
+  if (validate(desc, nullptr) != CPATTN_OK || desc->a2a != 1) return 0;
+  return 2 * doc_section(desc) + cpattn_ring_bwd_workspace(desc);
+}
+
+static cpattn_status packed_args(const cpattn_desc* desc, const int32_t* starts, int n_docs,
+                                 void* workspace, size_t ws_bytes) {
+  if (desc->a2a != 1) return CPATTN_ERR_UNSUPPORTED;
+  if (n_docs < 1 || !starts || ((uintptr_t)starts & 3u)) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || ws_bytes < cpattn_packed_workspace(desc))
+    return CPATTN_ERR_INVALID_ARG;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_ring_fwd_packed(const cpattn_desc* desc, const int32_t* starts, int n_docs,
+                                     const void* q, const void* k, const void* v, void* o,
+                                     float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if ((s = packed_args(desc, starts, n_docs, workspace, ws_bytes)) != CPATTN_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  int* lo = static_cast<int*>(workspace);
+  int* hi = reinterpret_cast<int*>(static_cast<char*>(workspace) + doc_section(desc));
+  cudaError_t e = launch_doc_bounds(R.B, R.T, n_docs, starts, lo, hi, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  if (R.bf16 && tc_supported(R))
+    return from_cuda(launch_tc_fwd(R, -1, -1, q, k, v, o, lse, status_ptr(), st, lo));
+  return from_cuda(launch_simt_fwd(R, -1, -1, q, k, v, o, lse, st, lo));
+}
+
+cpattn_status cpattn_ring_bwd_packed(const cpattn_desc* desc, const int32_t* starts, int n_docs,
+                                     const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dO, void* dq, void* dk,
+                                     void* dv, void* workspace, size_t ws_bytes, void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if ((s = packed_args(desc, starts, n_docs, workspace, ws_bytes)) != CPATTN_OK) return s;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  int* lo = static_cast<int*>(workspace);
+  int* hi = reinterpret_cast<int*>(static_cast<char*>(workspace) + doc_section(desc));
+  char* stats = static_cast<char*>(workspace) + 2 * doc_section(desc);
+  float* delta = reinterpret_cast<float*>(stats);
+  float* lse2 = reinterpret_cast<float*>(stats + ws_section(desc));
+  cudaError_t e = launch_doc_bounds(R.B, R.T, n_docs, starts, lo, hi, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  const int64_t rows = (int64_t)R.B * R.Hq * R.T;
+  const bool tc = R.bf16 && tc_supported(R);
+  e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  if (tc)
+    return from_cuda(
+        launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st, lo, hi));
+  e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st, lo);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  return from_cuda(launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st, hi));
+}
+
+// ---------------------------------------------------------------------------
 // all-gather mode
 // ---------------------------------------------------------------------------
 cpattn_status cpattn_allgather_fwd(const cpattn_desc* desc, int q_rank, const void* q,

@@ -28,6 +28,12 @@ struct PermuteArgs {
 cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cudaStream_t st);
 
 // ---- merge.cu --------------------------------------------------------------
+// Packed sequences: from the document starts [B][n_docs + 1] (natural positions,
+// starts[b][0] = 0, non-decreasing, starts[b][n_docs] = T) the first and last
+// position of every position's document, lo/hi [B][T] int32.  Positions are
+// clamped into their own document so that every query sees at least itself.
+cudaError_t launch_doc_bounds(int B, int T, int n_docs, const int* starts, int* lo, int* hi,
+                              cudaStream_t st);
 cudaError_t launch_merge(int64_t rows, int D, const float* oa, const float* la, const float* ob,
                          const float* lb, float* oo, float* lo, cudaStream_t st);
 // delta[row] = sum_d dO[row, d] * O[row, d] (float32 accumulation).  When lse2 is
@@ -42,13 +48,14 @@ cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const voi
 // all-gather mode (that rank's c rows per (b, h) over every chunk, o in the tensor
 // dtype); q_rank < 0 runs the whole ring and writes o in the tensor dtype.
 cudaError_t launch_simt_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
-                            const void* v, void* o, float* lse, cudaStream_t st);
+                            const void* v, void* o, float* lse, cudaStream_t st,
+                            const int* doc_lo = nullptr);
 cudaError_t launch_simt_bwd_dq(const Ring& R, const void* q, const void* k, const void* v,
                                const float* lse, const float* delta, const void* dO, void* dq,
-                               cudaStream_t st);
+                               cudaStream_t st, const int* doc_lo = nullptr);
 cudaError_t launch_simt_bwd_dkdv(const Ring& R, const void* q, const void* k, const void* v,
                                  const float* lse, const float* delta, const void* dO, void* dk,
-                                 void* dv, cudaStream_t st);
+                                 void* dv, cudaStream_t st, const int* doc_hi = nullptr);
 // All-gather mode backward of rank q_rank: lse/delta/dO/dq hold the rank's c rows
 // per (b, h), q the whole sequence; dk_sum/dv_sum (float32, all T rows) receive
 // the rank's share (added when `accumulate`).
@@ -59,11 +66,17 @@ cudaError_t launch_simt_allgather_bwd(const Ring& R, int q_rank, const void* q, 
 
 // ---- tc_fwd.cu / tc_bwd.cu (bf16 tcgen05 path, D in {64, 128}) --------------
 bool tc_supported(const Ring& R);
+// doc_lo (packed sequences, ring mode only): per batch row and natural position
+// the first position of its document, [B][T] int32; nullptr for plain causal.
 cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
-                          const void* v, void* o, float* lse, int* status, cudaStream_t st);
+                          const void* v, void* o, float* lse, int* status, cudaStream_t st,
+                          const int* doc_lo = nullptr);
+// doc_lo / doc_hi (packed sequences): first and last position of each position's
+// document, [B][T] int32 each; nullptr for plain causal.
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
-                          void* dk, void* dv, int* status, cudaStream_t st);
+                          void* dk, void* dv, int* status, cudaStream_t st,
+                          const int* doc_lo = nullptr, const int* doc_hi = nullptr);
 // All-gather mode backward of rank q_rank (see launch_simt_allgather_bwd); lse2 /
 // delta are the pre-pass statistics of the rank's rows.
 cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,

@@ -195,4 +195,42 @@ cudaError_t launch_delta(int64_t rows, int D, int bf16, const void* o, const voi
   return e;
 }
 
+// ---------------------------------------------------------------------------
+// Packed sequences: the document of every position (transformers pull request
+// #50497: position ids restart at every packed document, and the mask is rebuilt
+// from them).  One thread per (batch row, position): the last document whose start
+// is <= the position, found by binary search over the row's starts.
+// ---------------------------------------------------------------------------
+__global__ void doc_bounds_kernel(int B, int T, int n_docs, const int* __restrict__ starts,
+                                  int* __restrict__ lo, int* __restrict__ hi) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)B * T) return;
+  const int b = (int)(i / T), pos = (int)(i - (int64_t)b * T);
+  const int* st = starts + (int64_t)b * (n_docs + 1);
+  int a = 0, z = n_docs - 1;  // the document index lies in [a, z]
+  while (a < z) {
+    const int mid = (a + z + 1) >> 1;
+    if (st[mid] <= pos) a = mid;
+    else z = mid - 1;
+  }
+  int l = st[a], h = st[a + 1] - 1;
+  // starts that break the contract still leave every position inside its own
+  // document (each query sees at least itself)
+  l = l > pos ? pos : (l < 0 ? 0 : l);
+  h = h < pos ? pos : (h > T - 1 ? T - 1 : h);
+  lo[i] = l;
+  hi[i] = h;
+}
+
+cudaError_t launch_doc_bounds(int B, int T, int n_docs, const int* starts, int* lo, int* hi,
+                              cudaStream_t st) {
+  const int64_t n = (int64_t)B * T;
+  if (n == 0) return cudaSuccess;
+  timing_begin("doc_bounds", st);
+  doc_bounds_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(B, T, n_docs, starts, lo, hi);
+  cudaError_t e = cudaGetLastError();
+  timing_end(st);
+  return e;
+}
+
 }  // namespace cpattn

@@ -56,6 +56,7 @@ struct SimtFwd {
   int q_slot0, n_q_slots;  // queries: slots [q_slot0, q_slot0 + n_q_slots)
   int kv_fixed;            // < 0: whole ring; else only this rank's chunk
   int local_rows;          // o/lse hold n_q_slots rows per (b, h) instead of T
+  const int* doc_lo;       // packed: first position of each position's document, [B][T]
 };
 
 template <typename TI, typename TO>
@@ -82,12 +83,14 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtFwd p, const TI* __re
 
   float mrun = -INFINITY, lrun = 0.f, orun[4] = {0.f, 0.f, 0.f, 0.f};
   const int steps = p.kv_fixed >= 0 ? 1 : p.m.cp;
+  const int lo_q = p.doc_lo ? p.doc_lo[(int64_t)b * p.T + qpos] : 0;
   for (int i = 0; i < steps; ++i) {
     const int s = p.kv_fixed >= 0 ? p.kv_fixed : (r - i + p.m.cp) % p.m.cp;
     // chunk-local online softmax over the K/V held at this step
     float mc = -INFINITY, lc = 0.f, oc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int t = s * p.m.c; t < (s + 1) * p.m.c; ++t) {
-      if (p.m.pos(t) > qpos) continue;
+      const int kp = p.m.pos(t);
+      if (kp > qpos || kp < lo_q) continue;
       const float sc = dot_row(qv, kb + (int64_t)t * D, D, lane) * p.scale;
       const float mn = fmaxf(mc, sc);
       const float corr = expf(mc - mn);
@@ -132,6 +135,9 @@ struct SimtBwd {
   // what they hold when `accumulate` is set.
   int ag_rank;
   int accumulate;
+  // packed sequences: first / last position of each position's document, [B][T]
+  const int* doc_lo;
+  const int* doc_hi;
 };
 
 template <typename T>
@@ -159,10 +165,12 @@ __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(SimtBwd p, const T* __
   const int r = slot / p.m.c;
   const T* kb = k + ((int64_t)b * p.Hkv + g) * p.T * D;
   const T* vb = v + ((int64_t)b * p.Hkv + g) * p.T * D;
+  const int lo_q = p.doc_lo ? p.doc_lo[(int64_t)b * p.T + qpos] : 0;
   for (int i = 0; i < p.m.cp; ++i) {
     const int s = (r - i + p.m.cp) % p.m.cp;
     for (int t = s * p.m.c; t < (s + 1) * p.m.c; ++t) {
-      if (p.m.pos(t) > qpos) continue;
+      const int kp = p.m.pos(t);
+      if (kp > qpos || kp < lo_q) continue;
       const float pr = expf(dot_row(qv, kb + (int64_t)t * D, D, lane) * p.scale - L);
       const float ds = pr * (dot_row(dov, vb + (int64_t)t * D, D, lane) - Dl);
 #pragma unroll
@@ -199,13 +207,15 @@ __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(
   load_row(v + w * D, D, lane, vv);
   const int kpos = p.m.pos(slot);
   const int s = slot / p.m.c;
+  const int hi_k = p.doc_hi ? p.doc_hi[(int64_t)b * p.T + kpos] : p.T;
   const bool ag = p.ag_rank >= 0;
   for (int i = 0; i < (ag ? 1 : p.m.cp); ++i) {
     const int r = ag ? p.ag_rank : (s + i) % p.m.cp;
     for (int hh = 0; hh < p.n_rep; ++hh) {
       const int64_t qbh = (int64_t)b * p.Hq + g * p.n_rep + hh;
       for (int t = r * p.m.c; t < (r + 1) * p.m.c; ++t) {
-        if (kpos > p.m.pos(t)) continue;
+        const int qp = p.m.pos(t);
+        if (qp < kpos || qp > hi_k) continue;
         const int64_t qrow = qbh * p.T + t;
         const int64_t srow = ag ? qbh * p.m.c + (t - r * p.m.c) : qrow;  // dO / statistics
         const T* qr = q + qrow * D;
@@ -241,7 +251,8 @@ __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(
 static unsigned blocks_for(int64_t warps) { return (unsigned)((warps + 7) / 8); }
 
 cudaError_t launch_simt_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
-                            const void* v, void* o, float* lse, cudaStream_t st) {
+                            const void* v, void* o, float* lse, cudaStream_t st,
+                            const int* doc_lo) {
   SimtFwd p;
   p.B = R.B;
   p.Hq = R.Hq;
@@ -259,6 +270,7 @@ cudaError_t launch_simt_fwd(const Ring& R, int q_rank, int kv_rank, const void* 
   p.n_q_slots = local ? p.m.c : R.T;
   p.kv_fixed = partial ? kv_rank : -1;
   p.local_rows = local ? 1 : 0;
+  p.doc_lo = doc_lo;
   const int64_t warps = (int64_t)p.B * p.Hq * p.n_q_slots;
   if (warps == 0) return cudaSuccess;
   timing_begin(partial ? "simt_partial_fwd" : local ? "simt_allgather_fwd" : "simt_ring_fwd", st);
@@ -292,13 +304,16 @@ static SimtBwd make_bwd(const Ring& R) {
   p.scale = R.scale;
   p.ag_rank = -1;
   p.accumulate = 0;
+  p.doc_lo = nullptr;
+  p.doc_hi = nullptr;
   return p;
 }
 
 cudaError_t launch_simt_bwd_dq(const Ring& R, const void* q, const void* k, const void* v,
                                const float* lse, const float* delta, const void* dO, void* dq,
-                               cudaStream_t st) {
+                               cudaStream_t st, const int* doc_lo) {
   SimtBwd p = make_bwd(R);
+  p.doc_lo = doc_lo;
   const int64_t warps = (int64_t)p.B * p.Hq * p.T;
   timing_begin("simt_bwd_dq", st);
   if (R.bf16)
@@ -316,8 +331,9 @@ cudaError_t launch_simt_bwd_dq(const Ring& R, const void* q, const void* k, cons
 
 cudaError_t launch_simt_bwd_dkdv(const Ring& R, const void* q, const void* k, const void* v,
                                  const float* lse, const float* delta, const void* dO, void* dk,
-                                 void* dv, cudaStream_t st) {
+                                 void* dv, cudaStream_t st, const int* doc_hi) {
   SimtBwd p = make_bwd(R);
+  p.doc_hi = doc_hi;
   const int64_t warps = (int64_t)p.B * p.Hkv * p.T;
   timing_begin("simt_bwd_dkdv", st);
   if (R.bf16)

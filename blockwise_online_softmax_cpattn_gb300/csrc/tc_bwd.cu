@@ -56,6 +56,10 @@ struct Params {
   // hold when `accumulate` is set.
   int ag_rank;
   int accumulate;
+  // packed sequences (ring mode): first / last natural position of each position's
+  // document per batch row, [B][T]; nullptr for plain causal attention
+  const int* doc_lo;
+  const int* doc_hi;
 };
 
 // Query tiles of rank r at positions >= kpos0 (chunk bounds and kpos0 lie on the
@@ -69,10 +73,15 @@ __device__ __forceinline__ int rank_tiles_from(const SeqMap& m, int r, int kpos0
   return part(r * m.h, m.h) + part((2 * m.cp - 1 - r) * m.h, m.h);
 }
 
-__device__ __forceinline__ int classify(int qpos0, int kpos0) {
-  if (kpos0 + kTile - 1 <= qpos0) return kFull;
+// Tile pairs on the same 128-position grid (see the forward kernel): plain causal
+// without documents (lo_row nullptr); with packed documents also empty when every
+// key lies before the first query's document and full only when every key lies in
+// the last query's document.
+__device__ __forceinline__ int classify(int qpos0, int kpos0, const int* lo_row) {
   if (kpos0 > qpos0 + kTile - 1) return kEmpty;
-  return kDiag;
+  if (lo_row == nullptr) return kpos0 + kTile - 1 <= qpos0 ? kFull : kDiag;
+  if (kpos0 + kTile - 1 < lo_row[qpos0]) return kEmpty;
+  return kpos0 + kTile - 1 <= qpos0 && kpos0 >= lo_row[qpos0 + kTile - 1] ? kFull : kDiag;
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t par, volatile int* abort,
@@ -129,7 +138,7 @@ struct DkdvSmem {
   static constexpr int kBytes = kMisc + 16;
 };
 
-template <int D, bool AG>
+template <int D, bool AG, bool PK>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -192,13 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // query tiles in the order the chunk's gradient travels the ring back to its
   // owner: ranks s, s+1, ..., s-1; every query head of the group per rank; tiles
   // that cannot see this K/V tile are skipped by every role alike
+  // packed sequences only in the PK instantiation, so the plain path keeps its code
+  const int* lo_row = PK ? p.doc_lo + (int64_t)b * p.T : nullptr;
   auto walk_start = [&](TileWalk& w) {
     if (AG) w.start(p.m, p.ag_rank, 1, +1, p.n_rep);  // all-gather: one rank's queries
     else w.start(p.m, s_own, p.m.cp, +1, p.n_rep);
-    while (!w.done() && classify(w.pos(), kpos0) == kEmpty) w.next();
+    while (!w.done() && classify(w.pos(), kpos0, lo_row) == kEmpty) w.next();
   };
   auto walk_next = [&](TileWalk& w) {
-    do w.next(); while (!w.done() && classify(w.pos(), kpos0) == kEmpty);
+    do w.next(); while (!w.done() && classify(w.pos(), kpos0, lo_row) == kEmpty);
   };
 
   if (warp < 4) {
@@ -314,8 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
       // every query tile at or after this K/V tile's position sees it, once per
       // query head of the group (the walk of the other roles skips the rest)
-      const int n_tiles = p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0)
-                                         : (p.T - kpos0) >> 7);
+      int n_tiles;
+      if (!PK) {
+        n_tiles = p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0) : (p.T - kpos0) >> 7);
+      } else {
+        // packed: the query tiles at or after this one that reach into its keys,
+        // counted by the warp's lanes in parallel (the walk visits every query tile
+        // position once per head of the group)
+        int n = 0;
+        for (int qt = (kpos0 >> 7) + lane; qt < (p.T >> 7); qt += 32)
+          n += classify(qt << 7, kpos0, lo_row) != kEmpty;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+        n_tiles = p.n_rep * n;
+      }
       bool ok = warp_wait(kv_full, 0, abort, p.status);
       tc_fence_after();
       StageRing<QS> qr;   // Q stage of tile t
@@ -389,6 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_math();  // warpgroups 1 and 2: softmax / gradient math
     const int quad = warp & 3, half = (warp - 4) >> 2;
     const int row = quad * 32 + lane;  // key row of the tile
+    // packed: this key is seen by the queries up to its document's last position
+    const int hi_k = PK ? p.doc_hi[(int64_t)b * p.T + kpos0 + row] : p.T;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + half * 64;
     const uint32_t t_dp = tmem + lane_off + 128 + half * 64;
@@ -401,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     TileWalk wk;
     for (walk_start(wk); !wk.done(); walk_next(wk)) {
       const int qpos0 = wk.pos();
-      const int cls = classify(qpos0, kpos0);
+      const int cls = classify(qpos0, kpos0, lo_row);
       if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status))) break;  // -LSE log2e landed
       const float* lse_t = lse_s + qr.stage * 128 + half * 64;
       const float* del_t = del_s + dr.stage * 128 + half * 64;
@@ -419,6 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(s_free);  // S^T is in registers: the S region may take the next S^T
       // query column j (of this half) sees this key row iff kpos0 + row <= qpos0 + 64*half + j
       const int thr = kpos0 + row - qpos0 - half * 64;
+      // packed: query column j is also hidden past the key's document end
+      const int thr_hi = hi_k - qpos0 - half * 64;
       float pr[64];
       const float2 sl2v = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
@@ -433,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sl2v, nl);
           float p0 = ex2(x.x), p1 = ex2(x.y);
           if (cls == kDiag) {
-            if (j0 < thr) p0 = 0.f;
-            if (j0 + 1 < thr) p1 = 0.f;
+            if (j0 < thr || (PK && j0 > thr_hi)) p0 = 0.f;
+            if (j0 + 1 < thr || (PK && j0 + 1 > thr_hi)) p1 = 0.f;
           }
           pr[j0] = p0;
           pr[j0 + 1] = p1;
@@ -591,7 +618,7 @@ struct DqItem {
   int kv_row_base;
 };
 
-template <int D>
+template <int D, bool PK>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -674,12 +701,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     return it;
   };
   // K/V tiles of an item in ring order (chunks r, r-1, ...), hidden tiles skipped
+  auto doc_row = [&](const DqItem& it) -> const int* {
+    return PK ? p.doc_lo + (int64_t)it.b * p.T : nullptr;
+  };
   auto walk_start = [&](TileWalk& w, const DqItem& it) {
     w.start(p.m, it.r_own, p.m.cp, -1, 1);
-    while (!w.done() && classify(it.qpos0, w.pos()) == kEmpty) w.next();
+    while (!w.done() && classify(it.qpos0, w.pos(), doc_row(it)) == kEmpty) w.next();
   };
   auto walk_next = [&](TileWalk& w, const DqItem& it) {
-    do w.next(); while (!w.done() && classify(it.qpos0, w.pos()) == kEmpty);
+    do w.next(); while (!w.done() && classify(it.qpos0, w.pos(), doc_row(it)) == kEmpty);
   };
 
   if (warp < 4) {
@@ -855,13 +885,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int w;
     for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
       const DqItem it = decode(w);
+      const int* lo_row = doc_row(it);
+      const int lo_q = PK ? lo_row[it.qpos0 + row] : 0;  // packed: first key of the document
       const float2 nl2 = make_float2(p.lse2[it.srow + row], p.lse2[it.srow + row]);  // -LSE log2e
       const float2 ndl = make_float2(p.delta[it.srow + row], p.delta[it.srow + row]);  // -Delta
       int cnt = 0;  // tiles of this item
       TileWalk wk;
       for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
         const int kpos0 = wk.pos();
-        const int cls = classify(it.qpos0, kpos0);
+        const int cls = classify(it.qpos0, kpos0, lo_row);
         if (!(ok = warp_wait(s_full, g & 1, abort, p.status))) break;
         tc_fence_after();
         uint32_t sr[2][32];
@@ -872,6 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(s_free);
         // key column j (of this half) is visible iff kpos0 + 64*half + j <= qpos0 + row
         const int thr = it.qpos0 + row - kpos0 - half * 64;
+        const int thr_lo = lo_q - kpos0 - half * 64;
         float pr[64];
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -882,8 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   sl2v, nl2);
             float p0 = ex2(x.x), p1 = ex2(x.y);
             if (cls == kDiag) {
-              if (j0 > thr) p0 = 0.f;
-              if (j0 + 1 > thr) p1 = 0.f;
+              if (j0 > thr || (PK && j0 < thr_lo)) p0 = 0.f;
+              if (j0 + 1 > thr || (PK && j0 + 1 < thr_lo)) p1 = 0.f;
             }
             pr[j0] = p0;
             pr[j0 + 1] = p1;
@@ -969,11 +1002,13 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   Params pk = base;
   pk.out0 = dk;
   pk.out1 = dv;
-  auto kdkdv = ag ? dkdv_kernel<D, true> : dkdv_kernel<D, false>;
+  const bool packed = base.doc_lo != nullptr;  // ring mode only (checked by the caller)
+  auto kdkdv = ag ? dkdv_kernel<D, true, false>
+                  : (packed ? dkdv_kernel<D, false, true> : dkdv_kernel<D, false, false>);
   cudaError_t e = prep(kdkdv, DkdvSmem<D>::kBytes);
   if (e != cudaSuccess) return e;
   const int kv_items = R.B * R.Hkv * (R.T / kTile);
-  timing_begin(ag ? "tc_allgather_dkdv" : "tc_bwd_dkdv", st);
+  timing_begin(ag ? "tc_allgather_dkdv" : packed ? "tc_packed_dkdv" : "tc_bwd_dkdv", st);
   kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pk);
   e = cudaGetLastError();
   timing_end(st);
@@ -981,7 +1016,8 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   Params pq = base;
   pq.out0 = dq;
   pq.out1 = nullptr;
-  e = prep(dq_kernel<D>, DqSmem<D>::kBytes);
+  auto kdq = packed ? dq_kernel<D, true> : dq_kernel<D, false>;
+  e = prep(kdq, DqSmem<D>::kBytes);
   if (e != cudaSuccess) return e;
   const int q_items = R.B * R.Hq * ((ag ? R.T / R.cp : R.T) / kTile);
   // persistent: at most one resident CTA per SM, each walking its share of the items
@@ -989,8 +1025,8 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  timing_begin(ag ? "tc_allgather_dq" : "tc_bwd_dq", st);
-  dq_kernel<D><<<q_items < sms ? q_items : sms, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
+  timing_begin(ag ? "tc_allgather_dq" : packed ? "tc_packed_dq" : "tc_bwd_dq", st);
+  kdq<<<q_items < sms ? q_items : sms, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
   e = cudaGetLastError();
   timing_end(st);
   return e;
@@ -1014,13 +1050,18 @@ static tcbwd::Params bwd_params(const Ring& R, const float* lse2, const float* d
   p.status = status;
   p.ag_rank = -1;
   p.accumulate = 0;
+  p.doc_lo = nullptr;
+  p.doc_hi = nullptr;
   return p;
 }
 
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
-                          void* dk, void* dv, int* status, cudaStream_t st) {
-  const tcbwd::Params p = bwd_params(R, lse2, delta, status);
+                          void* dk, void* dv, int* status, cudaStream_t st, const int* doc_lo,
+                          const int* doc_hi) {
+  tcbwd::Params p = bwd_params(R, lse2, delta, status);
+  p.doc_lo = doc_lo;
+  p.doc_hi = doc_hi;
   if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st);
   return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st);
 }

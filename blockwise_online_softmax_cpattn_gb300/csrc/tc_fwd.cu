@@ -78,6 +78,9 @@ struct Params {
   float* lse;
   int* status;
   int debug_fault;
+  // packed sequences: lo[b * T + p] = first natural position of p's document in
+  // batch row b (nullptr: one document per row, plain causal attention)
+  const int* doc_lo;
 };
 
 template <int D>
@@ -128,10 +131,16 @@ __device__ __forceinline__ Item decode(const Params& p, int w) {
   return it;
 }
 
-__device__ __forceinline__ int classify(int qpos0, int kpos0) {
-  if (kpos0 + kTile - 1 <= qpos0) return kFull;
+// Tile pairs on the same 128-position grid.  Plain causal: full below the
+// diagonal, empty above it, masked on it.  Packed sequences (lo_row = the batch
+// row's document starts per position): also empty when every key lies before
+// the first query's document, and full only when every key lies in the last
+// query's document; any other pair is masked per element.
+__device__ __forceinline__ int classify(int qpos0, int kpos0, const int* lo_row) {
   if (kpos0 > qpos0 + kTile - 1) return kEmpty;
-  return kDiag;  // tiles are aligned on the same 128-position grid: kpos0 == qpos0
+  if (lo_row == nullptr) return kpos0 + kTile - 1 <= qpos0 ? kFull : kDiag;
+  if (kpos0 + kTile - 1 < lo_row[qpos0]) return kEmpty;
+  return kpos0 + kTile - 1 <= qpos0 && kpos0 >= lo_row[qpos0 + kTile - 1] ? kFull : kDiag;
 }
 
 // Wait in which every lane of the warp takes part; all lanes agree on the result.
@@ -147,7 +156,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t par) {
   return mbar_wait(bar, par, &never, nullptr, kDrainTimeoutNs);
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool PK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -207,12 +216,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // K/V tiles of an item in ring order: chunks r, r-1, ..., r-cp+1 (mod cp), or one
   // chunk; every role walks the same list and skips the tiles the causal mask hides
   const bool one_chunk = p.q_rank >= 0 && p.kv_rank >= 0;
+  // packed sequences only in the PK instantiation, so the plain path keeps its code
+  auto doc_row = [&](const Item& it) -> const int* {
+    return PK ? p.doc_lo + (int64_t)it.b * p.T : nullptr;
+  };
   auto walk_start = [&](TileWalk& w, const Item& it) {
     w.start(p.m, one_chunk ? p.kv_rank : it.rank, one_chunk ? 1 : p.m.cp, -1, 1);
-    while (!w.done() && classify(it.pos0, w.pos()) == kEmpty) w.next();
+    while (!w.done() && classify(it.pos0, w.pos(), doc_row(it)) == kEmpty) w.next();
   };
   auto walk_next = [&](TileWalk& w, const Item& it) {
-    do w.next(); while (!w.done() && classify(it.pos0, w.pos()) == kEmpty);
+    do w.next(); while (!w.done() && classify(it.pos0, w.pos(), doc_row(it)) == kEmpty);
   };
 
   if (warp < 4) {
@@ -377,12 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int w;
     for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
       const Item it = decode(p, w);
+      const int* lo_row = doc_row(it);
+      // packed: this row's keys start at its document's first position
+      const int lo_q = PK ? lo_row[it.pos0 + row] : 0;
       float m_run = -INFINITY, l_run = 0.f;
       int cnt = 0;  // tiles of this item
       TileWalk wk;
       for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
         const int kpos = wk.pos();
-        const int cls = classify(it.pos0, kpos);
+        const int cls = classify(it.pos0, kpos, lo_row);
         const int b = g & 1;
         const uint32_t t_s = tmem + lane_off + b * 128 + half * 64;
         if (!(ok = warp_wait(s_full(b), (g >> 1) & 1, abort, p.status, tmo))) break;
@@ -392,13 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(t_s + 32, r[1]);
         tmem_wait_ld();
         if (cls == kDiag) {
-          // key column j of this half is visible iff kpos + 64 half + j <= qpos + row
+          // key column j of this half is visible iff lo_q <= kpos + 64 half + j <= qpos + row
           const int thr = row + it.pos0 - kpos - half * 64;
+          const int thr_lo = lo_q - kpos - half * 64;
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (c * 32 + j > thr) r[c][j] = __float_as_uint(-INFINITY);
+              if (c * 32 + j > thr || (PK && c * 32 + j < thr_lo))
+                r[c][j] = __float_as_uint(-INFINITY);
         }
         float mx;
         {
@@ -553,7 +571,7 @@ bool tc_supported(const Ring& R) {
   return true;
 }
 
-template <int D, bool F32>
+template <int D, bool F32, bool PK = false>
 static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, const void* q,
                            const void* k, const void* v, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
@@ -562,7 +580,7 @@ static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, con
       encode_tmap_2d_bf16(&tv, v, D, (uint64_t)R.B * R.Hkv * R.T, 64, tcfwd::kTile) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   constexpr int kSmem = tcfwd::Smem<D>::kBytes;
-  auto kern = tcfwd::fwd_kernel<D, F32>;
+  auto kern = tcfwd::fwd_kernel<D, F32, PK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   if ((e = check_register_split(kern, tcfwd::kThreads)) != cudaSuccess) return e;
@@ -577,7 +595,8 @@ static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, con
 }
 
 cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
-                          const void* v, void* o, float* lse, int* status, cudaStream_t st) {
+                          const void* v, void* o, float* lse, int* status, cudaStream_t st,
+                          const int* doc_lo) {
   tcfwd::Params p;
   p.B = R.B;
   p.Hq = R.Hq;
@@ -597,17 +616,25 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
   p.lse = lse;
   p.status = status;
   p.debug_fault = R.debug_fault;
+  p.doc_lo = doc_lo;
   const int items = R.B * R.Hq * p.q_tiles;
   if (items == 0) return cudaSuccess;
   p.n_items = items;
-  timing_begin(partial ? "tc_partial_fwd" : local ? "tc_allgather_fwd" : "tc_ring_fwd", st);
+  const bool packed = doc_lo != nullptr;  // ring mode only (checked by the caller)
+  timing_begin(partial  ? "tc_partial_fwd"
+               : local  ? "tc_allgather_fwd"
+               : packed ? "tc_packed_fwd"
+                        : "tc_ring_fwd",
+               st);
   cudaError_t e;
   if (R.D == 128)
-    e = partial ? run_fwd<128, true>(R, p, items, q, k, v, st)
-                : run_fwd<128, false>(R, p, items, q, k, v, st);
+    e = partial  ? run_fwd<128, true>(R, p, items, q, k, v, st)
+        : packed ? run_fwd<128, false, true>(R, p, items, q, k, v, st)
+                 : run_fwd<128, false>(R, p, items, q, k, v, st);
   else
-    e = partial ? run_fwd<64, true>(R, p, items, q, k, v, st)
-                : run_fwd<64, false>(R, p, items, q, k, v, st);
+    e = partial  ? run_fwd<64, true>(R, p, items, q, k, v, st)
+        : packed ? run_fwd<64, false, true>(R, p, items, q, k, v, st)
+                 : run_fwd<64, false>(R, p, items, q, k, v, st);
   timing_end(st);
   return e;
 }

@@ -179,6 +179,33 @@ cpattn_status cpattn_ring_bwd_noalloc(const cpattn_desc* desc, const void* q, co
                                       void* stream);
 
 /*
+ * Packed sequences (transformers pull request #50497: the packed variant restarts
+ * the position ids mid-sequence and the mask is rebuilt for the documents; the
+ * InfiniTrain pull request #181 leaves packed / variable-length sequences out).
+ * Every batch row holds n_docs documents back to back: document d of row b is
+ * natural positions [starts[b][d], starts[b][d+1]), and a token attends to the
+ * keys of its own document at or before it (causal attention with the position
+ * restarting at every document).  Otherwise as cpattn_ring_fwd / cpattn_ring_bwd.
+ *   starts    : device int32 [B][n_docs + 1], natural positions, starts[b][0] = 0,
+ *               non-decreasing (empty documents allowed), starts[b][n_docs] = T;
+ *               4-byte aligned.  Starts that break this contract give unspecified
+ *               (but finite, in-bounds) results.
+ *   workspace : at least cpattn_packed_workspace(desc) bytes (the documents of
+ *               every position, and for the backward the row statistics)
+ * Errors: n_docs < 1, null or misaligned starts, workspace too small ->
+ * CPATTN_ERR_INVALID_ARG; desc->a2a != 1 -> CPATTN_ERR_UNSUPPORTED; others as
+ * cpattn_ring_fwd / cpattn_ring_bwd.
+ */
+size_t cpattn_packed_workspace(const cpattn_desc* desc);
+cpattn_status cpattn_ring_fwd_packed(const cpattn_desc* desc, const int32_t* starts, int n_docs,
+                                     const void* q, const void* k, const void* v, void* o,
+                                     float* lse, void* workspace, size_t ws_bytes, void* stream);
+cpattn_status cpattn_ring_bwd_packed(const cpattn_desc* desc, const int32_t* starts, int n_docs,
+                                     const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dO, void* dq, void* dk,
+                                     void* dv, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * All-gather mode, forward (pull request #181, mode table row "all_gather": the
  * K/V of every rank is gathered and the rank's own queries attend to it; tutorial
  * "上下文并行", section "Zig-Zag Ring Attention 的通信与计算重叠", bullet

@@ -120,3 +120,22 @@ def test_allgather_ranks_flags_and_workspace_are_checked(cp):
     assert cp.cpattn_allgather_bwd(d, 0, *args, 2, FAKE, need, 0) == 1      # accumulate: 0 or 1
     assert cp.cpattn_allgather_bwd(d, 0, *args, 1, FAKE, need - 1, 0) == 1  # workspace too small
     assert cp.cpattn_allgather_bwd(d, 0, *args[:7], 0, 1, FAKE, need, 0) == 1  # null dv_sum
+
+
+def test_packed_arguments_are_checked(cp):
+    d = _desc(cp)
+    need = cp.cpattn_packed_workspace(d)
+    # documents of every position (lo, hi: int32 each) plus the backward statistics
+    assert need >= 2 * 512 * 4 + cp.cpattn_ring_bwd_workspace(d) and need % 256 == 0
+    assert cp.cpattn_packed_workspace(_desc(cp, a2a=2, cp=4, T=512)) == 0
+    f = [FAKE] * 5
+    assert cp.cpattn_ring_fwd_packed(d, FAKE, 0, *f, FAKE, need, 0) == 1      # n_docs < 1
+    assert cp.cpattn_ring_fwd_packed(d, 0, 2, *f, FAKE, need, 0) == 1         # null starts
+    assert cp.cpattn_ring_fwd_packed(d, FAKE + 2, 2, *f, FAKE, need, 0) == 1  # misaligned starts
+    assert cp.cpattn_ring_fwd_packed(d, FAKE, 2, *f, FAKE, need - 1, 0) == 1  # workspace
+    assert cp.cpattn_ring_fwd_packed(_desc(cp, a2a=2, cp=4, T=512), FAKE, 2, *f, FAKE, need,
+                                     0) == 2
+    b = [FAKE] * 9
+    assert cp.cpattn_ring_bwd_packed(d, FAKE, 0, *b, FAKE, need, 0) == 1
+    assert cp.cpattn_ring_bwd_packed(d, FAKE, 2, *b, FAKE, need - 1, 0) == 1
+    assert cp.cpattn_ring_bwd_packed(_desc(cp, causal=0), FAKE, 2, *b, FAKE, need, 0) == 2

@@ -1,0 +1,76 @@
+"""GPU: packed sequences (transformers pull request #50497: position ids restart
+at every packed document and the mask is rebuilt for the documents) through
+cpattn_ring_fwd_packed / cpattn_ring_bwd_packed, against the oracle's packed
+attention.  Document boundaries fall inside tiles, on tile edges, inside zigzag
+halves and between ranks; empty documents are included.  With one document per
+row the packed calls reproduce the plain ring bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_helpers import LSE_ABS_TOL, TOL, cp_mod, desc_of, dev, rel, ring_inputs, run_ring, to_nat
+from oracle import attention as OA
+
+pytestmark = pytest.mark.gpu
+
+
+def _random_starts(rng, B, T, n_docs):
+    rows = []
+    for _ in range(B):
+        cuts = np.sort(rng.integers(0, T + 1, n_docs - 1))
+        rows.append(np.concatenate([[0], cuts, [T]]))
+    return np.stack(rows).astype(np.int32)
+
+
+CASES = [
+    (W.Workload("pk_tc_T2048_cp4_zz_gqa4_B2", 2, 8, 2, 2048, 128, 4, "zigzag", "bf16"),
+     np.array([[0, 300, 301, 1200, 1200, 2048], [0, 128, 1024, 1025, 1919, 2048]], np.int32)),
+    (W.Workload("pk_tc_T1024_cp2_contig_D64", 1, 4, 4, 1024, 64, 2, "contiguous", "bf16"), 37),
+    (W.Workload("pk_tc_T1024_cp4_zz_gqa3", 1, 3, 1, 1024, 128, 4, "zigzag", "bf16"), 5),
+    (W.Workload("pk_simt_f32_T96_cp3_zz", 2, 2, 1, 96, 20, 3, "zigzag", "f32"), 4),
+    (W.Workload("pk_simt_bf16_T128_cp2_D32", 1, 2, 2, 128, 32, 2, "zigzag", "bf16"), 3),
+]
+
+
+def _run_packed(w, lay, starts_dev, n_docs):
+    cp = cp_mod()
+    ql, kl, vl, dol = lay
+    desc = desc_of(w)
+    ws = torch.empty(cp.cpattn_packed_workspace(desc), dtype=torch.uint8, device=dev())
+    o = torch.empty_like(ql)
+    lse = torch.empty(w.B, w.H_q, w.T, dtype=torch.float32, device=dev())
+    cp.check(cp.cpattn_ring_fwd_packed(desc, starts_dev, n_docs, ql, kl, vl, o, lse, ws))
+    dq, dk, dv = torch.empty_like(ql), torch.empty_like(kl), torch.empty_like(vl)
+    cp.check(cp.cpattn_ring_bwd_packed(desc, starts_dev, n_docs, ql, kl, vl, o, lse, dol, dq, dk,
+                                       dv, ws))
+    cp.check(cp.cpattn_check())
+    return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+
+@pytest.mark.parametrize("w,starts", CASES, ids=lambda x: getattr(x, "name", ""))
+def test_packed_matches_oracle(w, starts):
+    if isinstance(starts, int):
+        starts = _random_starts(np.random.default_rng(w.T + starts), w.B, w.T, starts)
+    n_docs = starts.shape[1] - 1
+    nat, lay = ring_inputs(w)
+    got = _run_packed(w, lay, torch.from_numpy(starts).to(dev()), n_docs)
+    q, k, v, do = (W.as_f64(x) for x in nat)
+    ro, rlse = OA.packed_attention_fwd(q, k, v, w.scale, starts)
+    rdq, rdk, rdv = OA.packed_attention_bwd(q, k, v, do, w.scale, starts)
+    tol = TOL[w.dtype]
+    assert rel(to_nat(got["o"], w), ro) <= tol["o"]
+    lse = to_nat(got["lse"].unsqueeze(-1), w)[..., 0]
+    assert float(np.max(np.abs(lse - rlse))) <= LSE_ABS_TOL[w.dtype]
+    for key, ref in (("dq", rdq), ("dk", rdk), ("dv", rdv)):
+        assert rel(to_nat(got[key], w), ref) <= tol["grad"], key
+
+
+@pytest.mark.parametrize("w", [CASES[0][0], CASES[3][0]], ids=lambda w: w.name)
+def test_one_document_is_the_plain_ring(w):
+    nat, lay = ring_inputs(w)
+    starts = np.tile(np.array([[0, w.T]], np.int32), (w.B, 1))
+    got = _run_packed(w, lay, torch.from_numpy(starts).to(dev()), 1)
+    ref = run_ring(w, lay)
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(got[key], ref[key]), key
