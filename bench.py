@@ -13,6 +13,10 @@ before every timed step.
 --impl reference times the FP64 CPU oracle (the only reference there is) on the
 host cores, each step a bounded sample of the same workload.
 
+--packed-docs N times the ring over packed sequences instead: every row holds N
+documents of seeded random lengths (causal attention inside each document); the
+FLOPs count the pairs the packed mask attends.
+
 --mode allgather times the all-gather mode instead (pull request #181, mode table
 row "all_gather"): one step = cpattn_allgather_fwd and cpattn_allgather_bwd for
 every emulated rank, with the layout-order q, k, v and each rank's dO rows already
@@ -36,6 +40,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -57,6 +63,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mode", default="ring", choices=["ring", "allgather"])
+    ap.add_argument("--packed-docs", type=int, default=0,
+                    help="ring mode over packed sequences: this many documents per row, "
+                         "seeded random lengths (0: one sequence per row)")
     return ap.parse_args()
 
 
@@ -141,17 +150,18 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the CUDA arm
 # ---------------------------------------------------------------------------
-def kernel_flops_or_bytes(name, w):
-    """Algorithmic work of one launch of a library kernel on this workload."""
-    pairs = w.attended_pairs
+def kernel_flops_or_bytes(name, w, pairs=None):
+    """Algorithmic work of one launch of a library kernel on this workload (pairs:
+    the attended pairs when they differ from plain causal, e.g. packed documents)."""
+    pairs = w.attended_pairs if pairs is None else pairs
     elt = 2 if w.dtype == "bf16" else 4
     rows_q = w.B * w.H_q * w.T
     rows_kv = w.B * w.H_kv * w.T
-    if name in ("tc_ring_fwd", "simt_ring_fwd"):
+    if name in ("tc_ring_fwd", "simt_ring_fwd", "tc_packed_fwd"):
         return "tensor", 4.0 * w.D * pairs
-    if name in ("tc_bwd_dkdv", "simt_bwd_dkdv"):     # S, dP recomputed + dV, dK products
+    if name in ("tc_bwd_dkdv", "simt_bwd_dkdv", "tc_packed_dkdv"):  # S, dP recomputed + dV, dK
         return "tensor", 8.0 * w.D * pairs
-    if name in ("tc_bwd_dq", "simt_bwd_dq"):         # the dQ product only
+    if name in ("tc_bwd_dq", "simt_bwd_dq", "tc_packed_dq"):        # the dQ product only
         return "tensor", 2.0 * w.D * pairs
     # all-gather mode: one launch covers one rank's rows (1/cp of the pairs on average)
     if name == "tc_allgather_fwd":
@@ -199,6 +209,17 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def packed_documents(w, n_docs, seed=1234):
+    """Seeded document starts [B][n_docs + 1] for a packed workload (every row the same
+    cut points: n_docs - 1 distinct random cuts) and the pairs the packed mask attends."""
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.choice(np.arange(1, w.T), size=n_docs - 1, replace=False))
+    row = np.concatenate([[0], cuts, [w.T]]).astype(np.int32)
+    lens = np.diff(row).astype(np.float64)
+    pairs = w.B * w.H_q * float(np.sum(lens * (lens + 1) / 2))
+    return np.tile(row, (w.B, 1)), pairs
+
+
 def run_cpattn(args, rank, world):
     import torch
     import blockwise_online_softmax_cpattn_gb300 as cp
@@ -233,14 +254,33 @@ def run_cpattn(args, rank, world):
     lse = torch.empty(w.B, w.H_q, w.T, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(lay[0]), torch.empty_like(lay[1]), torch.empty_like(lay[2])
     outs = [torch.empty_like(s) for s in (src[0], src[1], src[2], src[0])]  # o, dk, dv, dq
-    ws = torch.empty(cp.cpattn_ring_bwd_workspace(desc), dtype=torch.uint8, device=dev)
+    packed = args.packed_docs > 0
+    if packed:
+        if w.a2a != 1:
+            raise SystemExit("--packed-docs takes a plain ring workload (a2a = 1)")
+        starts_np, doc_pairs = packed_documents(w, args.packed_docs)
+        starts = torch.from_numpy(starts_np).to(dev)
+        ws = torch.empty(cp.cpattn_packed_workspace(desc), dtype=torch.uint8, device=dev)
+    else:
+        ws = torch.empty(cp.cpattn_ring_bwd_workspace(desc), dtype=torch.uint8, device=dev)
+
+    def ring_fwd(q_, k_, v_, o_, lse_):
+        if packed:
+            return cp.cpattn_ring_fwd_packed(desc, starts, args.packed_docs, q_, k_, v_, o_, lse_, ws)
+        return cp.cpattn_ring_fwd(desc, q_, k_, v_, o_, lse_)
+
+    def ring_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_):
+        if packed:
+            return cp.cpattn_ring_bwd_packed(desc, starts, args.packed_docs, q_, k_, v_, o_, lse_,
+                                             do_, dq_, dk_, dv_, ws)
+        return cp.cpattn_ring_bwd(desc, q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, ws)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step():
         for s_, l_, h in zip(src, lay, H):
             cp.check(cp.cpattn_layout(fwd_perm, desc, s_, l_, h))
-        cp.check(cp.cpattn_ring_fwd(desc, lay[0], lay[1], lay[2], o, lse))
-        cp.check(cp.cpattn_ring_bwd(desc, lay[0], lay[1], lay[2], o, lse, lay[3], dq, dk, dv, ws))
+        cp.check(ring_fwd(lay[0], lay[1], lay[2], o, lse))
+        cp.check(ring_bwd(lay[0], lay[1], lay[2], o, lse, lay[3], dq, dk, dv))
         for x, y, h in zip((o, dk, dv, dq), outs, (w.H_q, w.H_kv, w.H_kv, w.H_q)):
             cp.check(cp.cpattn_layout(inv_perm, desc, x, y, h))
 
@@ -272,7 +312,8 @@ def run_cpattn(args, rank, world):
     clocks = sampler.stop(t0, t1)
     cp.check(cp.cpattn_check())
     ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, dev)
-    flops = w.fwd_flops + w.bwd_flops
+    # 14 D FLOPs per attended pair (4 D forward, 10 D backward)
+    flops = 14.0 * w.D * doc_pairs if packed else w.fwd_flops + w.bwd_flops
     value = world * flops / (ms * 1e-3) / 1e12
 
     # ---- per-kernel durations (events on the launch stream, same steps)
@@ -290,7 +331,7 @@ def run_cpattn(args, rank, world):
                for name, (tot, n) in table.items()}
     dom = max(table, key=lambda n: table[n][0])
     pk, src_pk = peaks()
-    bound, work = kernel_flops_or_bytes(dom, w)
+    bound, work = kernel_flops_or_bytes(dom, w, doc_pairs if packed else None)
     avg_ms = table[dom][0] / table[dom][1]
     if bound == "tensor":
         achieved = work / (avg_ms * 1e-3) / 1e12
@@ -302,7 +343,7 @@ def run_cpattn(args, rank, world):
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": None}
-    traffic = traffic_for(dom, w.name)
+    traffic = None if packed else traffic_for(dom, w.name)
     roof["traffic"] = traffic
 
     # ---- end to end through the C ABI with host buffers
@@ -330,7 +371,7 @@ def run_cpattn(args, rank, world):
             dst_.copy_(hsrc, non_blocking=True)
         for s_, l_, h in zip(src[:3], lay[:3], H[:3]):
             cp.check(cp.cpattn_layout(fwd_perm, desc, s_, l_, h))
-        cp.check(cp.cpattn_ring_fwd(desc, lay[0], lay[1], lay[2], o, lse))
+        cp.check(ring_fwd(lay[0], lay[1], lay[2], o, lse))
         cp.check(cp.cpattn_layout(inv_perm, desc, o, outs[0], w.H_q))
         e_o.record(stream)
         side_out.wait_event(e_o)
@@ -338,7 +379,7 @@ def run_cpattn(args, rank, world):
             host_out[0].copy_(outs[0], non_blocking=True)
         stream.wait_event(e_do)
         cp.check(cp.cpattn_layout(fwd_perm, desc, src[3], lay[3], H[3]))
-        cp.check(cp.cpattn_ring_bwd(desc, lay[0], lay[1], lay[2], o, lse, lay[3], dq, dk, dv, ws))
+        cp.check(ring_bwd(lay[0], lay[1], lay[2], o, lse, lay[3], dq, dk, dv))
         for x, y, h in zip((dk, dv, dq), outs[1:], (w.H_kv, w.H_kv, w.H_q)):
             cp.check(cp.cpattn_layout(inv_perm, desc, x, y, h))
         for hdst, dsrc in zip(host_out[1:], outs[1:]):
@@ -383,7 +424,11 @@ def run_cpattn(args, rank, world):
                "step": ("a2a permute" if w.a2a > 1 else "zigzag permute")
                + " q,k,v,dO -> ring fwd -> ring bwd -> inverse permute o,dq,dk,dv",
                "pct_of_bf16_peak": value / world / pk["bf16_tflops"],
-               "peak_source": src_pk}),
+               "peak_source": src_pk,
+               **({"packed_docs": args.packed_docs,
+                   "doc_lengths": [int(x) for x in np.diff(starts_np[0])],
+                   "attended_pairs": doc_pairs, "flops_per_step": 14.0 * w.D * doc_pairs}
+                  if packed else {})}),
            "roofline": roof, "gpu_launches": int(round(launches_per_step * args.steps)),
            "clocks": clocks, "e2e": e2e, "kernels": kernels}
     return out
