@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace cpattn {
 
 // Device status codes (the values of cpattn_status).
@@ -86,6 +88,33 @@ struct TileWalk {
         if (s < 0) s += cp;
         else if (s >= cp) s -= cp;
       }
+    }
+  }
+};
+
+// Walk over the 128-token tiles of a range of NATURAL positions, tiles
+// [first, last] in order, `reps` passes (the query heads of a K/V group).  Packed
+// sequences use it: the tiles a tile pair can see form one contiguous natural
+// range (a document's), so nothing has to be skipped.  Same interface as TileWalk.
+struct NatWalk {
+  SeqMap m;
+  int t, first, last, rep, reps;
+  __device__ __forceinline__ void start(const SeqMap& mm, int first_tile, int last_tile,
+                                        int repeats) {
+    m = mm;
+    first = first_tile;
+    last = last_tile;
+    t = first_tile;
+    rep = 0;
+    reps = first_tile <= last_tile ? repeats : 0;
+  }
+  __device__ __forceinline__ bool done() const { return rep >= reps; }
+  __device__ __forceinline__ int pos() const { return t << 7; }
+  __device__ __forceinline__ int slot() const { return m.slot(t << 7); }
+  __device__ __forceinline__ void next() {
+    if (++t > last) {
+      t = first;
+      ++rep;
     }
   }
 };

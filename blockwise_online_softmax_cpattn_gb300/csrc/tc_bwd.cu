@@ -203,13 +203,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // that cannot see this K/V tile are skipped by every role alike
   // packed sequences only in the PK instantiation, so the plain path keeps its code
   const int* lo_row = PK ? p.doc_lo + (int64_t)b * p.T : nullptr;
-  auto walk_start = [&](TileWalk& w) {
-    if (AG) w.start(p.m, p.ag_rank, 1, +1, p.n_rep);  // all-gather: one rank's queries
-    else w.start(p.m, s_own, p.m.cp, +1, p.n_rep);
-    while (!w.done() && classify(w.pos(), kpos0, lo_row) == kEmpty) w.next();
+  // packed: the query tiles from this one up to the tile holding the end of its last
+  // key's document, in natural order (every head of the group in turn)
+  using Walk = std::conditional_t<PK, NatWalk, TileWalk>;
+  const int pk_last = PK ? p.doc_hi[(int64_t)b * p.T + kpos0 + kTile - 1] >> 7 : 0;
+  auto walk_start = [&](Walk& w) {
+    if constexpr (PK) {
+      w.start(p.m, kpos0 >> 7, pk_last, p.n_rep);
+    } else {
+      if (AG) w.start(p.m, p.ag_rank, 1, +1, p.n_rep);  // all-gather: one rank's queries
+      else w.start(p.m, s_own, p.m.cp, +1, p.n_rep);
+      while (!w.done() && classify(w.pos(), kpos0, nullptr) == kEmpty) w.next();
+    }
   };
-  auto walk_next = [&](TileWalk& w) {
-    do w.next(); while (!w.done() && classify(w.pos(), kpos0, lo_row) == kEmpty);
+  auto walk_next = [&](Walk& w) {
+    if constexpr (PK) w.next();
+    else do w.next(); while (!w.done() && classify(w.pos(), kpos0, nullptr) == kEmpty);
   };
 
   if (warp < 4) {
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       StageRing<QS> qr;
       StageRing<DS> dr;
-      TileWalk wk;
+      Walk wk;
       for (walk_start(wk); !wk.done(); walk_next(wk)) {
         const int qbh = b * p.Hq + g * p.n_rep + wk.rep;
         const int qrow = qbh * p.T + wk.slot();
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
       StageRing<QS> qr;
       int cnt = 0;
-      TileWalk wk;
+      Walk wk;
       for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
         // The tensor pipe runs MMAs in the order they are queued.  The gradient warp
         // queues ... dV(t-1), dK(t-1), dP^T(t) back to back; S^T(t+1) goes in behind
@@ -325,20 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
       // every query tile at or after this K/V tile's position sees it, once per
       // query head of the group (the walk of the other roles skips the rest)
-      int n_tiles;
-      if (!PK) {
-        n_tiles = p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0) : (p.T - kpos0) >> 7);
-      } else {
-        // packed: the query tiles at or after this one that reach into its keys,
-        // counted by the warp's lanes in parallel (the walk visits every query tile
-        // position once per head of the group)
-        int n = 0;
-        for (int qt = (kpos0 >> 7) + lane; qt < (p.T >> 7); qt += 32)
-          n += classify(qt << 7, kpos0, lo_row) != kEmpty;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-        n_tiles = p.n_rep * n;
-      }
+      // packed: the natural range the walk covers, once per head of the group
+      const int n_tiles =
+          PK ? p.n_rep * (pk_last - (kpos0 >> 7) + 1)
+             : p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0) : (p.T - kpos0) >> 7);
       bool ok = warp_wait(kv_full, 0, abort, p.status);
       tc_fence_after();
       StageRing<QS> qr;   // Q stage of tile t
@@ -423,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     StageRing<DS> dr;
     int cnt = 0;
     bool ok = true;
-    TileWalk wk;
+    Walk wk;
     for (walk_start(wk); !wk.done(); walk_next(wk)) {
       const int qpos0 = wk.pos();
       const int cls = classify(qpos0, kpos0, lo_row);
@@ -704,12 +703,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto doc_row = [&](const DqItem& it) -> const int* {
     return PK ? p.doc_lo + (int64_t)it.b * p.T : nullptr;
   };
-  auto walk_start = [&](TileWalk& w, const DqItem& it) {
-    w.start(p.m, it.r_own, p.m.cp, -1, 1);
-    while (!w.done() && classify(it.qpos0, w.pos(), doc_row(it)) == kEmpty) w.next();
+  // packed: the key tiles from the one holding the first row's document start up to
+  // the diagonal, in natural order
+  using Walk = std::conditional_t<PK, NatWalk, TileWalk>;
+  auto walk_start = [&](Walk& w, const DqItem& it) {
+    if constexpr (PK) {
+      w.start(p.m, doc_row(it)[it.qpos0] >> 7, it.qpos0 >> 7, 1);
+    } else {
+      w.start(p.m, it.r_own, p.m.cp, -1, 1);
+      while (!w.done() && classify(it.qpos0, w.pos(), nullptr) == kEmpty) w.next();
+    }
   };
-  auto walk_next = [&](TileWalk& w, const DqItem& it) {
-    do w.next(); while (!w.done() && classify(it.qpos0, w.pos(), doc_row(it)) == kEmpty);
+  auto walk_next = [&](Walk& w, const DqItem& it) {
+    if constexpr (PK) w.next();
+    else do w.next(); while (!w.done() && classify(it.qpos0, w.pos(), nullptr) == kEmpty);
   };
 
   if (warp < 4) {
@@ -735,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)it.srow, qdo_full);
         }
         q_last = k;
-        TileWalk wk;
+        Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           const int row = it.kv_row_base + wk.slot();
           if (!(ok = mbar_wait(k_empty(kr.stage), kr.par ^ 1, abort, p.status, kTimeoutNs))) break;
@@ -782,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
         const DqItem it = decode(w);
         if (!(ok = warp_wait(qdo_full, k & 1, abort, p.status))) break;
-        TileWalk wk;
+        Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           uint32_t dst;
           uint64_t bd;
@@ -842,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
         const DqItem it = decode(w);
         int t = 0;  // tile of this item
-        TileWalk wk;
+        Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           if (!(ok = warp_wait(ds_full(g & 1), (g >> 1) & 1, abort, p.status))) break;
           // the item's first dQ overwrites the accumulator the previous epilogue read
@@ -890,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 nl2 = make_float2(p.lse2[it.srow + row], p.lse2[it.srow + row]);  // -LSE log2e
       const float2 ndl = make_float2(p.delta[it.srow + row], p.delta[it.srow + row]);  // -Delta
       int cnt = 0;  // tiles of this item
-      TileWalk wk;
+      Walk wk;
       for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
         const int kpos0 = wk.pos();
         const int cls = classify(it.qpos0, kpos0, lo_row);

@@ -220,12 +220,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto doc_row = [&](const Item& it) -> const int* {
     return PK ? p.doc_lo + (int64_t)it.b * p.T : nullptr;
   };
-  auto walk_start = [&](TileWalk& w, const Item& it) {
-    w.start(p.m, one_chunk ? p.kv_rank : it.rank, one_chunk ? 1 : p.m.cp, -1, 1);
-    while (!w.done() && classify(it.pos0, w.pos(), doc_row(it)) == kEmpty) w.next();
+  // packed: the key tiles of the query tile's visible range, from the tile holding
+  // its first row's document start up to the diagonal, in natural order
+  using Walk = std::conditional_t<PK, NatWalk, TileWalk>;
+  auto walk_start = [&](Walk& w, const Item& it) {
+    if constexpr (PK) {
+      w.start(p.m, doc_row(it)[it.pos0] >> 7, it.pos0 >> 7, 1);
+    } else {
+      w.start(p.m, one_chunk ? p.kv_rank : it.rank, one_chunk ? 1 : p.m.cp, -1, 1);
+      while (!w.done() && classify(it.pos0, w.pos(), nullptr) == kEmpty) w.next();
+    }
   };
-  auto walk_next = [&](TileWalk& w, const Item& it) {
-    do w.next(); while (!w.done() && classify(it.pos0, w.pos(), doc_row(it)) == kEmpty);
+  auto walk_next = [&](Walk& w, const Item& it) {
+    if constexpr (PK) w.next();
+    else do w.next(); while (!w.done() && classify(it.pos0, w.pos(), nullptr) == kEmpty);
   };
 
   if (warp < 4) {
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             q_last = k;
           }
         }
-        TileWalk wk;
+        Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           const uint32_t empty = is_k ? k_empty(stage) : v_empty(stage);
           const uint32_t full = is_k ? k_full(stage) : v_full(stage);
@@ -295,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
         const Item it = decode(p, w);
         if (!(ok = warp_wait(q_full, k & 1, abort, p.status, tmo))) break;
-        TileWalk wk;
+        Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           const int b = g & 1;
           if (!(ok = warp_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
@@ -341,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
         const Item it = decode(p, w);
         int t = 0;  // tile of this item
-        TileWalk wk;
+        Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           const int b = g & 1;
           if (!(ok = warp_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
@@ -395,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lo_q = PK ? lo_row[it.pos0 + row] : 0;
       float m_run = -INFINITY, l_run = 0.f;
       int cnt = 0;  // tiles of this item
-      TileWalk wk;
+      Walk wk;
       for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
         const int kpos = wk.pos();
         const int cls = classify(it.pos0, kpos, lo_row);

@@ -3,7 +3,9 @@ at every packed document and the mask is rebuilt for the documents) through
 cpattn_ring_fwd_packed / cpattn_ring_bwd_packed, against the oracle's packed
 attention.  Document boundaries fall inside tiles, on tile edges, inside zigzag
 halves and between ranks; empty documents are included.  With one document per
-row the packed calls reproduce the plain ring bit for bit."""
+row the packed calls give the plain ring's result up to the order of
+accumulation (they visit the visible tiles in natural order, the ring in ring
+order)."""
 import numpy as np
 import pytest
 import torch
@@ -72,5 +74,9 @@ def test_one_document_is_the_plain_ring(w):
     starts = np.tile(np.array([[0, w.T]], np.int32), (w.B, 1))
     got = _run_packed(w, lay, torch.from_numpy(starts).to(dev()), 1)
     ref = run_ring(w, lay)
-    for key in ("o", "lse", "dq", "dk", "dv"):
-        assert torch.equal(got[key], ref[key]), key
+    # the same products over the same tiles, summed in another order
+    lim = {"f32": 1e-5, "bf16": 1e-2}[w.dtype]
+    for key in ("o", "dq", "dk", "dv"):
+        e = rel(W.as_f64(got[key]), W.as_f64(ref[key]))
+        assert e <= lim, (key, e)
+    assert float((got["lse"] - ref["lse"]).abs().max()) <= LSE_ABS_TOL[w.dtype]
