@@ -264,16 +264,16 @@ def run_cpattn(args, rank, world):
     else:
         ws = torch.empty(cp.cpattn_ring_bwd_workspace(desc), dtype=torch.uint8, device=dev)
 
-    def ring_fwd(q_, k_, v_, o_, lse_):
+    def ring_fwd(q_, k_, v_, o_, lse_, d=desc):
         if packed:
-            return cp.cpattn_ring_fwd_packed(desc, starts, args.packed_docs, q_, k_, v_, o_, lse_, ws)
-        return cp.cpattn_ring_fwd(desc, q_, k_, v_, o_, lse_)
+            return cp.cpattn_ring_fwd_packed(d, starts, args.packed_docs, q_, k_, v_, o_, lse_, ws)
+        return cp.cpattn_ring_fwd(d, q_, k_, v_, o_, lse_)
 
-    def ring_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_):
+    def ring_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, d=desc):
         if packed:
-            return cp.cpattn_ring_bwd_packed(desc, starts, args.packed_docs, q_, k_, v_, o_, lse_,
+            return cp.cpattn_ring_bwd_packed(d, starts, args.packed_docs, q_, k_, v_, o_, lse_,
                                              do_, dq_, dk_, dv_, ws)
-        return cp.cpattn_ring_bwd(desc, q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, ws)
+        return cp.cpattn_ring_bwd(d, q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, ws)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step():
@@ -386,12 +386,70 @@ def run_cpattn(args, rank, world):
             hdst.copy_(dsrc, non_blocking=True)
         stream.wait_stream(side_out)  # o's download is part of the step
 
+    # Head-chunked pipeline (one batch row, plain ring): the heads split into two
+    # halves, each a problem of its own for the library (H_q/2 query heads and their
+    # H_kv/2 K/V heads), so the second half's upload runs while the first half is
+    # computed and the first half's gradients download while the second is.
+    n_chunks = 2
+    chunked = (w.B == 1 and w.a2a == 1 and w.H_kv % n_chunks == 0 and src_dev is not None)
+    if chunked:
+        d_c = cp.make_desc(w.B, w.H_q // n_chunks, w.H_kv // n_chunks, w.T, w.D, w.cp, w.layout,
+                           w.dtype)
+
+        def hs(x, c, h):
+            n = h // n_chunks
+            return x[:, c * n:(c + 1) * n]
+
+        ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
+        ev_do = [torch.cuda.Event() for _ in range(n_chunks)]
+        ev_o = [torch.cuda.Event() for _ in range(n_chunks)]
+        ev_g = [torch.cuda.Event() for _ in range(n_chunks)]
+
+    def e2e_step_chunked(a_ev):
+        side_in.wait_event(a_ev)
+        side_out.wait_event(a_ev)
+        with torch.cuda.stream(side_in):
+            for c in range(n_chunks):
+                for dst_, hsrc, h in zip(src[:3], nat_host[:3], H[:3]):
+                    hs(dst_, c, h).copy_(hs(hsrc, c, h), non_blocking=True)
+                ev_in[c].record(side_in)
+            for c in range(n_chunks):
+                hs(src[3], c, H[3]).copy_(hs(nat_host[3], c, H[3]), non_blocking=True)
+                ev_do[c].record(side_in)
+        for c in range(n_chunks):
+            stream.wait_event(ev_in[c])
+            for s_, l_, h in zip(src[:3], lay[:3], H[:3]):
+                cp.check(cp.cpattn_layout(fwd_perm, d_c, hs(s_, c, h), hs(l_, c, h), h // n_chunks))
+            cp.check(ring_fwd(hs(lay[0], c, w.H_q), hs(lay[1], c, w.H_kv), hs(lay[2], c, w.H_kv),
+                              hs(o, c, w.H_q), hs(lse, c, w.H_q), d=d_c))
+            cp.check(cp.cpattn_layout(inv_perm, d_c, hs(o, c, w.H_q), hs(outs[0], c, w.H_q),
+                                      w.H_q // n_chunks))
+            ev_o[c].record(stream)
+            side_out.wait_event(ev_o[c])
+            with torch.cuda.stream(side_out):
+                hs(host_out[0], c, w.H_q).copy_(hs(outs[0], c, w.H_q), non_blocking=True)
+        for c in range(n_chunks):
+            stream.wait_event(ev_do[c])
+            cp.check(cp.cpattn_layout(fwd_perm, d_c, hs(src[3], c, H[3]), hs(lay[3], c, H[3]),
+                                      H[3] // n_chunks))
+            cp.check(ring_bwd(hs(lay[0], c, w.H_q), hs(lay[1], c, w.H_kv), hs(lay[2], c, w.H_kv),
+                              hs(o, c, w.H_q), hs(lse, c, w.H_q), hs(lay[3], c, w.H_q),
+                              hs(dq, c, w.H_q), hs(dk, c, w.H_kv), hs(dv, c, w.H_kv), d=d_c))
+            for x, y, h in zip((dk, dv, dq), outs[1:], (w.H_kv, w.H_kv, w.H_q)):
+                cp.check(cp.cpattn_layout(inv_perm, d_c, hs(x, c, h), hs(y, c, h), h // n_chunks))
+            ev_g[c].record(stream)
+            side_out.wait_event(ev_g[c])
+            with torch.cuda.stream(side_out):
+                for hdst, dsrc, h in zip(host_out[1:], outs[1:], (w.H_kv, w.H_kv, w.H_q)):
+                    hs(hdst, c, h).copy_(hs(dsrc, c, h), non_blocking=True)
+        stream.wait_stream(side_out)  # every download is part of the step
+
     torch.cuda.synchronize()
     for a, b in ev2:
         flush.zero_()
         a.record(stream)
         if src_dev is not None:
-            e2e_step_overlapped(a)
+            (e2e_step_chunked if chunked else e2e_step_overlapped)(a)
             b.record(stream)
             continue
         else:
@@ -409,9 +467,21 @@ def run_cpattn(args, rank, world):
     torch.cuda.synchronize()
     cp.check(cp.cpattn_check())
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev2), world, dev)
+    if chunked:
+        # the end-to-end outputs are the device step's, bit for bit (the head halves
+        # are independent problems with the same per-tile arithmetic)
+        e2e_out = [x.clone() for x in host_out]
+        step()
+        torch.cuda.synchronize()
+        if not all(torch.equal(a_, b_.cpu()) for a_, b_ in zip(e2e_out, outs)):
+            raise RuntimeError("end-to-end outputs differ from the device-resident step's")
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "transfers": ("pinned host buffers; dO upload overlaps the forward and o download "
+           "transfers": ("pinned host buffers on side streams inside each step's events; the "
+                         "heads split into two halves, each half a library call of its own, so "
+                         "uploads and downloads of one half overlap the other half's compute"
+                         if src_dev is not None and chunked else
+                         "pinned host buffers; dO upload overlaps the forward and o download "
                          "overlaps the backward on side streams inside each step's events"
                          if src_dev is not None else "pinned host buffers, on the step's stream")}
 
