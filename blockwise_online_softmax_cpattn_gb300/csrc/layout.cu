@@ -1,5 +1,6 @@
 // Layout permutes: the zigzag token map and the all-to-all head<->sequence
-// re-layout of the hierarchical mode, as row gathers with 16-byte vectors.
+// re-layout of the hierarchical mode, as chunk moves (zigzag) or row gathers with
+// 16-byte vectors.
 //
 // Every destination row (D elements) is copied from one source row; threads
 // walk the destination in order, so stores are fully coalesced and each source
@@ -66,6 +67,57 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteDev p, const V* __r
     int64_t s = permute_src_row(p, row);
     dst[i] = __ldcs(src + s * vpr + v);
   }
+}
+
+// Row gathers for rows of 8, 16 or 32 16-byte vectors: G = 8 threads share a row,
+// each copying VPT = vpr / 8 of its vectors (so a group reads and writes 128
+// contiguous bytes per instruction), and every thread keeps kRowsInFlight rows in
+// flight; the source row is worked out once per row and thread rather than once
+// per vector.
+constexpr int kRowGroup = 8;
+constexpr int kRowsInFlight = 4;
+
+template <int VPT>
+__global__ void __launch_bounds__(256) gather_rows_kernel(PermuteDev p, const int4* __restrict__ src,
+                                                          int4* __restrict__ dst, int64_t rows) {
+  constexpr int vpr = kRowGroup * VPT;
+  const int lg = threadIdx.x % kRowGroup;
+  const int64_t grp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kRowGroup;
+  const int64_t ngrp = (int64_t)gridDim.x * blockDim.x / kRowGroup;
+  for (int64_t r0 = grp; r0 < rows; r0 += ngrp * kRowsInFlight) {
+    int4 v[kRowsInFlight][VPT];
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      const int64_t row = r0 + u * ngrp;
+      if (row < rows) {
+        const int4* s = src + permute_src_row(p, row) * vpr + lg;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) v[u][i] = __ldcs(s + i * kRowGroup);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      const int64_t row = r0 + u * ngrp;
+      if (row < rows) {
+        int4* d = dst + row * vpr + lg;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) __stcs(d + i * kRowGroup, v[u][i]);
+      }
+    }
+  }
+}
+
+template <int VPT>
+static cudaError_t run_rows(const PermuteDev& p, const void* src, void* dst, int64_t rows,
+                            cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (rows * kRowGroup + 255) / 256;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  if (blocks < 1) blocks = 1;
+  gather_rows_kernel<VPT><<<(unsigned)blocks, 256, 0, st>>>(p, (const int4*)src, (int4*)dst, rows);
+  return cudaGetLastError();
 }
 
 // Zigzag permutes as chunk moves.  Each (batch, head) sequence is 2*cp chunks of
@@ -163,6 +215,12 @@ cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cud
   const int nchunk = a.zz ? 2 * (a.cp / a.a2a) : a.cp / a.a2a;
   if (a.kind <= kZigzagInv && row_bytes % 16 == 0 && al % 16 == 0 && a.T % nchunk == 0)
     e = run_chunks(a, src, dst, row_bytes, st);
+  else if (row_bytes % 16 == 0 && al % 16 == 0 && row_bytes / 16 == 16)
+    e = run_rows<2>(p, src, dst, rows, st);
+  else if (row_bytes % 16 == 0 && al % 16 == 0 && row_bytes / 16 == 8)
+    e = run_rows<1>(p, src, dst, rows, st);
+  else if (row_bytes % 16 == 0 && al % 16 == 0 && row_bytes / 16 == 32)
+    e = run_rows<4>(p, src, dst, rows, st);
   else if (row_bytes % 16 == 0 && al % 16 == 0)
     e = run<int4>(p, src, dst, rows, row_bytes / 16, st);
   else if (row_bytes % 8 == 0 && al % 8 == 0)
