@@ -245,15 +245,39 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
 // ---------------------------------------------------------------------------
 // packed sequences
 // ---------------------------------------------------------------------------
-// Workspace: lo, hi (int32 per batch row and position), then the backward's
-// statistics as for cpattn_ring_bwd; each section 256-byte aligned.
+// Workspace: lo, hi (int32 per batch row and position), the work orders of the
+// query and key tiles (int32 per batch row and 128-token tile), then the
+// backward's statistics as for cpattn_ring_bwd; each section 256-byte aligned.
 static size_t doc_section(const cpattn_desc* desc) {
   return ((size_t)desc->B * desc->T * sizeof(int) + 255) / 256 * 256;
+}
+static size_t order_section(const cpattn_desc* desc) {
+  return ((size_t)desc->B * (desc->T / 128) * sizeof(int) + 255) / 256 * 256;
+}
+static size_t packed_stats_offset(const cpattn_desc* desc) {
+  return 2 * doc_section(desc) + 2 * order_section(desc);
 }
 
 size_t cpattn_packed_workspace(const cpattn_desc* desc) {
   if (validate(desc, nullptr) != CPATTN_OK || desc->a2a != 1) return 0;
-  return 2 * doc_section(desc) + cpattn_ring_bwd_workspace(desc);
+  return packed_stats_offset(desc) + cpattn_ring_bwd_workspace(desc);
+}
+
+// lo, hi and (tensor-core path only) the tile work orders of a packed call
+struct PackedTables {
+  int *lo, *hi, *ord_q, *ord_k;
+};
+static cudaError_t packed_tables(const cpattn_desc* desc, const Ring& R, const int32_t* starts,
+                                 int n_docs, void* workspace, bool tc, cudaStream_t st,
+                                 PackedTables* t) {
+  char* w = static_cast<char*>(workspace);
+  t->lo = reinterpret_cast<int*>(w);
+  t->hi = reinterpret_cast<int*>(w + doc_section(desc));
+  t->ord_q = reinterpret_cast<int*>(w + 2 * doc_section(desc));
+  t->ord_k = reinterpret_cast<int*>(w + 2 * doc_section(desc) + order_section(desc));
+  cudaError_t e = launch_doc_bounds(R.B, R.T, n_docs, starts, t->lo, t->hi, st);
+  if (e != cudaSuccess || !tc) return e;
+  return launch_doc_order(R.B, R.T, t->lo, t->hi, t->ord_q, t->ord_k, st);
 }
 
 static cpattn_status packed_args(const cpattn_desc* desc, const int32_t* starts, int n_docs,
@@ -276,13 +300,14 @@ cpattn_status cpattn_ring_fwd_packed(const cpattn_desc* desc, const int32_t* sta
     return CPATTN_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
-  int* lo = static_cast<int*>(workspace);
-  int* hi = reinterpret_cast<int*>(static_cast<char*>(workspace) + doc_section(desc));
-  cudaError_t e = launch_doc_bounds(R.B, R.T, n_docs, starts, lo, hi, st);
-  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  if (R.bf16 && tc_supported(R))
-    return from_cuda(launch_tc_fwd(R, -1, -1, q, k, v, o, lse, status_ptr(), st, lo));
-  return from_cuda(launch_simt_fwd(R, -1, -1, q, k, v, o, lse, st, lo));
+  const bool tc = R.bf16 && tc_supported(R);
+  PackedTables t;
+  if (packed_tables(desc, R, starts, n_docs, workspace, tc, st, &t) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  if (tc)
+    return from_cuda(
+        launch_tc_fwd(R, -1, -1, q, k, v, o, lse, status_ptr(), st, t.lo, t.ord_q));
+  return from_cuda(launch_simt_fwd(R, -1, -1, q, k, v, o, lse, st, t.lo));
 }
 
 cpattn_status cpattn_ring_bwd_packed(const cpattn_desc* desc, const int32_t* starts, int n_docs,
@@ -298,20 +323,22 @@ cpattn_status cpattn_ring_bwd_packed(const cpattn_desc* desc, const int32_t* sta
     return CPATTN_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
-  int* lo = static_cast<int*>(workspace);
-  int* hi = reinterpret_cast<int*>(static_cast<char*>(workspace) + doc_section(desc));
-  char* stats = static_cast<char*>(workspace) + 2 * doc_section(desc);
+  char* stats = static_cast<char*>(workspace) + packed_stats_offset(desc);
   float* delta = reinterpret_cast<float*>(stats);
   float* lse2 = reinterpret_cast<float*>(stats + ws_section(desc));
-  cudaError_t e = launch_doc_bounds(R.B, R.T, n_docs, starts, lo, hi, st);
-  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  const int64_t rows = (int64_t)R.B * R.Hq * R.T;
   const bool tc = R.bf16 && tc_supported(R);
-  e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
+  PackedTables t;
+  if (packed_tables(desc, R, starts, n_docs, workspace, tc, st, &t) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  const int* lo = t.lo;
+  const int* hi = t.hi;
+  const int64_t rows = (int64_t)R.B * R.Hq * R.T;
+  cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   if (tc)
     return from_cuda(
-        launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st, lo, hi));
+        launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st, lo, hi, t.ord_q,
+                      t.ord_k));
   e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st, lo);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   return from_cuda(launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st, hi));

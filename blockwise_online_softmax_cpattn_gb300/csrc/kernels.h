@@ -34,6 +34,10 @@ cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cud
 // clamped into their own document so that every query sees at least itself.
 cudaError_t launch_doc_bounds(int B, int T, int n_docs, const int* starts, int* lo, int* hi,
                               cudaStream_t st);
+// Packed sequences: (batch row, 128-token tile) entries b * (T/128) + tile in order
+// of decreasing work, for query tiles (ord_q) and key tiles (ord_k), B * T/128 each.
+cudaError_t launch_doc_order(int B, int T, const int* lo, const int* hi, int* ord_q, int* ord_k,
+                             cudaStream_t st);
 cudaError_t launch_merge(int64_t rows, int D, const float* oa, const float* la, const float* ob,
                          const float* lb, float* oo, float* lo, cudaStream_t st);
 // delta[row] = sum_d dO[row, d] * O[row, d] (float32 accumulation).  When lse2 is
@@ -70,13 +74,14 @@ bool tc_supported(const Ring& R);
 // the first position of its document, [B][T] int32; nullptr for plain causal.
 cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
                           const void* v, void* o, float* lse, int* status, cudaStream_t st,
-                          const int* doc_lo = nullptr);
+                          const int* doc_lo = nullptr, const int* ord_q = nullptr);
 // doc_lo / doc_hi (packed sequences): first and last position of each position's
 // document, [B][T] int32 each; nullptr for plain causal.
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st,
-                          const int* doc_lo = nullptr, const int* doc_hi = nullptr);
+                          const int* doc_lo = nullptr, const int* doc_hi = nullptr,
+                          const int* ord_q = nullptr, const int* ord_k = nullptr);
 // All-gather mode backward of rank q_rank (see launch_simt_allgather_bwd); lse2 /
 // delta are the pre-pass statistics of the rank's rows.
 cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,

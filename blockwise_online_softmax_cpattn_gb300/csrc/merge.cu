@@ -233,4 +233,57 @@ cudaError_t launch_doc_bounds(int B, int T, int n_docs, const int* starts, int* 
   return e;
 }
 
+// Packed sequences: the (batch row, 128-token tile) entries in order of decreasing
+// work, for the query tiles (keys from the tile holding the document start up to
+// the diagonal) and for the key tiles (queries from the diagonal up to the tile
+// holding the document end), so that the kernels hand out the heaviest work first.
+// One block, a counting sort over work (capped at kOrderBuckets - 1 tiles); the
+// order inside a bucket is whatever the atomics give, which changes the
+// scheduling only, never a result.  Entry value: b * n_tiles + tile.
+constexpr int kOrderBuckets = 1024;
+
+__global__ void __launch_bounds__(1024) doc_order_kernel(int B, int T, const int* __restrict__ lo,
+                                                         const int* __restrict__ hi,
+                                                         int* __restrict__ ord_q,
+                                                         int* __restrict__ ord_k) {
+  __shared__ int count[2][kOrderBuckets];
+  const int nt = T >> 7, n = B * nt;
+  for (int i = threadIdx.x; i < 2 * kOrderBuckets; i += blockDim.x) (&count[0][0])[i] = 0;
+  __syncthreads();
+  auto work = [&](int e, int which) {
+    const int b = e / nt, t = e - b * nt;
+    const int wk = which == 0 ? t - (lo[(int64_t)b * T + (t << 7)] >> 7) + 1
+                              : (hi[(int64_t)b * T + (t << 7) + 127] >> 7) - t + 1;
+    return wk < 1 ? 1 : (wk > kOrderBuckets - 1 ? kOrderBuckets - 1 : wk);
+  };
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    atomicAdd(&count[0][work(e, 0)], 1);
+    atomicAdd(&count[1][work(e, 1)], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < 2) {  // start of each bucket, heaviest bucket first
+    int run = 0;
+    for (int v = kOrderBuckets - 1; v >= 0; --v) {
+      const int c = count[threadIdx.x][v];
+      count[threadIdx.x][v] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    ord_q[atomicAdd(&count[0][work(e, 0)], 1)] = e;
+    ord_k[atomicAdd(&count[1][work(e, 1)], 1)] = e;
+  }
+}
+
+cudaError_t launch_doc_order(int B, int T, const int* lo, const int* hi, int* ord_q, int* ord_k,
+                             cudaStream_t st) {
+  if (B <= 0 || T < 128) return cudaSuccess;
+  timing_begin("doc_order", st);
+  doc_order_kernel<<<1, 1024, 0, st>>>(B, T, lo, hi, ord_q, ord_k);
+  cudaError_t e = cudaGetLastError();
+  timing_end(st);
+  return e;
+}
+
 }  // namespace cpattn

@@ -60,6 +60,10 @@ struct Params {
   // document per batch row, [B][T]; nullptr for plain causal attention
   const int* doc_lo;
   const int* doc_hi;
+  // packed: (batch row, tile) entries b * (T/128) + tile in decreasing work, for the
+  // dQ kernel's query tiles and the dK/dV kernel's key tiles
+  const int* ord_q;
+  const int* ord_k;
 };
 
 // Query tiles of rank r at positions >= kpos0 (chunk bounds and kpos0 lie on the
@@ -191,10 +195,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // work item: kv tiles with the earliest positions (the most queries) first
-  const int units = p.B * p.Hkv;
-  const int ti = blockIdx.x / units;
-  const int rem = blockIdx.x - ti * units;
-  const int b = rem / p.Hkv, g = rem - (rem / p.Hkv) * p.Hkv;
+  int ti, b, g;
+  if constexpr (PK) {
+    // packed: key tiles in decreasing work, every K/V head of a (batch row, tile) together
+    const int nt = p.T >> 7;
+    const int ent = p.ord_k[blockIdx.x / p.Hkv];
+    g = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
+    b = ent / nt;
+    ti = ent - b * nt;
+  } else {
+    const int units = p.B * p.Hkv;
+    ti = blockIdx.x / units;
+    const int rem = blockIdx.x - ti * units;
+    b = rem / p.Hkv;
+    g = rem - (rem / p.Hkv) * p.Hkv;
+  }
   const int kpos0 = ti * kTile;
   const int kslot0 = p.m.slot(kpos0);
   const int s_own = kslot0 / p.m.c;
@@ -678,10 +693,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto decode = [&](int w) {
     DqItem it;
     const int units = p.B * p.Hq;
-    const int ti = w / units;
-    const int rem = w - ti * units;
-    it.b = rem / p.Hq;
-    it.h = rem - it.b * p.Hq;
+    int ti;
+    if constexpr (PK) {
+      // packed: items in decreasing work, every head of a (batch row, tile) together
+      const int nt = p.T >> 7;
+      const int ent = p.ord_q[w / p.Hq];
+      it.b = ent / nt;
+      it.h = w - (w / p.Hq) * p.Hq;
+      ti = n_q_tiles - 1 - (ent - it.b * nt);  // the tile below is n_q_tiles - 1 - ti
+    } else {
+      ti = w / units;
+      const int rem = w - ti * units;
+      it.b = rem / p.Hq;
+      it.h = rem - it.b * p.Hq;
+    }
     it.g = it.h / p.n_rep;
     const int64_t bh = (int64_t)it.b * p.Hq + it.h;
     if (ag) {
@@ -1059,16 +1084,20 @@ static tcbwd::Params bwd_params(const Ring& R, const float* lse2, const float* d
   p.accumulate = 0;
   p.doc_lo = nullptr;
   p.doc_hi = nullptr;
+  p.ord_q = nullptr;
+  p.ord_k = nullptr;
   return p;
 }
 
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st, const int* doc_lo,
-                          const int* doc_hi) {
+                          const int* doc_hi, const int* ord_q, const int* ord_k) {
   tcbwd::Params p = bwd_params(R, lse2, delta, status);
   p.doc_lo = doc_lo;
   p.doc_hi = doc_hi;
+  p.ord_q = ord_q;
+  p.ord_k = ord_k;
   if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st);
   return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st);
 }

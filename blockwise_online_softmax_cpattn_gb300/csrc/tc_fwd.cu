@@ -81,6 +81,9 @@ struct Params {
   // packed sequences: lo[b * T + p] = first natural position of p's document in
   // batch row b (nullptr: one document per row, plain causal attention)
   const int* doc_lo;
+  // packed sequences: (batch row, query tile) entries b * (T/128) + tile, heaviest
+  // first (the order items are handed out in)
+  const int* ord_q;
 };
 
 template <int D>
@@ -109,8 +112,21 @@ struct Item {
   int b, h, g, rank, slot0, pos0;
 };
 
+template <bool PK>
 __device__ __forceinline__ Item decode(const Params& p, int w) {
   Item it;
+  if constexpr (PK) {
+    // packed: items in decreasing work, every head of a (batch row, tile) together
+    const int nt = p.T >> 7;
+    const int ent = p.ord_q[w / p.Hq];
+    it.b = ent / nt;
+    it.h = w - (w / p.Hq) * p.Hq;
+    it.g = it.h / p.n_rep;
+    it.pos0 = (ent - it.b * nt) * kTile;
+    it.slot0 = p.m.slot(it.pos0);
+    it.rank = it.slot0 / p.m.c;
+    return it;
+  }
   const int units = p.B * p.Hq;
   const int ti = w / units;
   const int rem = w - ti * units;
@@ -253,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int w;
       for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
-        const Item it = decode(p, w);
+        const Item it = decode<PK>(p, w);
         const int kv_row_base = (it.b * p.Hkv + it.g) * p.T;
         if (is_k) {
           // the Q buffer is free once the last S of the previous item has read it
@@ -301,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int w;
       for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
-        const Item it = decode(p, w);
+        const Item it = decode<PK>(p, w);
         if (!(ok = warp_wait(q_full, k & 1, abort, p.status, tmo))) break;
         Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
@@ -347,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int w;
       for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
-        const Item it = decode(p, w);
+        const Item it = decode<PK>(p, w);
         int t = 0;  // tile of this item
         Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
@@ -397,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int w;
     for (int k = 0; ok && (w = item_of(k, p.n_items)) >= 0; ++k) {
-      const Item it = decode(p, w);
+      const Item it = decode<PK>(p, w);
       const int* lo_row = doc_row(it);
       // packed: this row's keys start at its document's first position
       const int lo_q = PK ? lo_row[it.pos0 + row] : 0;
@@ -604,7 +620,7 @@ static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, con
 
 cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
                           const void* v, void* o, float* lse, int* status, cudaStream_t st,
-                          const int* doc_lo) {
+                          const int* doc_lo, const int* ord_q) {
   tcfwd::Params p;
   p.B = R.B;
   p.Hq = R.Hq;
@@ -625,6 +641,7 @@ cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q,
   p.status = status;
   p.debug_fault = R.debug_fault;
   p.doc_lo = doc_lo;
+  p.ord_q = ord_q;
   const int items = R.B * R.Hq * p.q_tiles;
   if (items == 0) return cudaSuccess;
   p.n_items = items;

@@ -191,7 +191,8 @@ cpattn_status cpattn_ring_bwd_noalloc(const cpattn_desc* desc, const void* q, co
  *               4-byte aligned.  Starts that break this contract give unspecified
  *               (but finite, in-bounds) results.
  *   workspace : at least cpattn_packed_workspace(desc) bytes (the documents of
- *               every position, and for the backward the row statistics)
+ *               every position, the 128-token tiles in order of decreasing work,
+ *               and for the backward the row statistics)
  * Errors: n_docs < 1, null or misaligned starts, workspace too small ->
  * CPATTN_ERR_INVALID_ARG; desc->a2a != 1 -> CPATTN_ERR_UNSUPPORTED; others as
  * cpattn_ring_fwd / cpattn_ring_bwd.
