@@ -248,13 +248,15 @@ __global__ void __launch_bounds__(1024) doc_order_kernel(int B, int T, const int
                                                          int* __restrict__ ord_k) {
   __shared__ int count[2][kOrderBuckets];
   const int nt = T >> 7, n = B * nt;
+  // a tile visits at most nt tiles: buckets 0..top
+  const int top = nt < kOrderBuckets - 1 ? nt : kOrderBuckets - 1;
   for (int i = threadIdx.x; i < 2 * kOrderBuckets; i += blockDim.x) (&count[0][0])[i] = 0;
   __syncthreads();
   auto work = [&](int e, int which) {
     const int b = e / nt, t = e - b * nt;
     const int wk = which == 0 ? t - (lo[(int64_t)b * T + (t << 7)] >> 7) + 1
                               : (hi[(int64_t)b * T + (t << 7) + 127] >> 7) - t + 1;
-    return wk < 1 ? 1 : (wk > kOrderBuckets - 1 ? kOrderBuckets - 1 : wk);
+    return wk < 1 ? 1 : (wk > top ? top : wk);
   };
   for (int e = threadIdx.x; e < n; e += blockDim.x) {
     atomicAdd(&count[0][work(e, 0)], 1);
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(1024) doc_order_kernel(int B, int T, const int
   __syncthreads();
   if (threadIdx.x < 2) {  // start of each bucket, heaviest bucket first
     int run = 0;
-    for (int v = kOrderBuckets - 1; v >= 0; --v) {
+    for (int v = top; v >= 0; --v) {
       const int c = count[threadIdx.x][v];
       count[threadIdx.x][v] = run;
       run += c;
