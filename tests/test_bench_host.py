@@ -77,3 +77,13 @@ def test_max_over_ranks_gloo_world2():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert res == {0: 2.5, 1: 2.5}
+
+
+def test_tensor_peak_burst_or_sustained():
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = {"hbm_gbs": 1.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    burst, what = bench.tensor_peak(pk, "measured", 0.4)
+    assert burst == 1900.0 and "burst" in what
+    sus, what = bench.tensor_peak(pk, "measured", 1.5)
+    assert sus == 1700.0 and "sustained" in what
