@@ -221,12 +221,10 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 def packed_documents(w, n_docs, seed=1234):
     """Seeded document starts [B][n_docs + 1] for a packed workload (every row the same
     cut points: n_docs - 1 distinct random cuts) and the pairs the packed mask attends."""
-    rng = np.random.default_rng(seed)
-    cuts = np.sort(rng.choice(np.arange(1, w.T), size=n_docs - 1, replace=False))
-    row = np.concatenate([[0], cuts, [w.T]]).astype(np.int32)
-    lens = np.diff(row).astype(np.float64)
+    starts = W.packed_starts(w, n_docs, seed)
+    lens = np.diff(starts[0]).astype(np.float64)
     pairs = w.B * w.H_q * float(np.sum(lens * (lens + 1) / 2))
-    return np.tile(row, (w.B, 1)), pairs
+    return starts, pairs
 
 
 def run_cpattn(args, rank, world):

@@ -80,3 +80,28 @@ def test_one_document_is_the_plain_ring(w):
         e = rel(W.as_f64(got[key]), W.as_f64(ref[key]))
         assert e <= lim, (key, e)
     assert float((got["lse"] - ref["lse"]).abs().max()) <= LSE_ABS_TOL[w.dtype]
+
+
+def test_packed_llama_T8192_eight_documents():
+    """The packed benchmark's launch configuration: the LLaMA shape (B1, H_q 32 /
+    H_kv 8, T 8192, D 128, cp 8 zigzag, bf16) with the seeded 8-document rows
+    (documents of 20 to 4448 tokens).  The oracle computes the last K/V group in
+    full (query heads 28-31 with K/V head 7); the other heads run the same tiles."""
+    w = W.LLAMA
+    starts = W.packed_starts(w, 8)
+    nat, lay = ring_inputs(w)
+    got = _run_packed(w, lay, torch.from_numpy(starts).to(dev()), 8)
+    n_rep = w.H_q // w.H_kv
+    tol = TOL[w.dtype]
+    for g in (w.H_kv - 1,):
+        hq = slice(g * n_rep, (g + 1) * n_rep)
+        q, do = (W.as_f64(x[:, hq]) for x in (nat[0], nat[3]))
+        k, v = (W.as_f64(x[:, g:g + 1]) for x in (nat[1], nat[2]))
+        ro, rlse = OA.packed_attention_fwd(q, k, v, w.scale, starts)
+        rdq, rdk, rdv = OA.packed_attention_bwd(q, k, v, do, w.scale, starts)
+        assert rel(to_nat(got["o"][:, hq], w), ro) <= tol["o"], ("o", g)
+        lse = to_nat(got["lse"][:, hq].unsqueeze(-1), w)[..., 0]
+        assert float(np.max(np.abs(lse - rlse))) <= LSE_ABS_TOL[w.dtype], ("lse", g)
+        assert rel(to_nat(got["dq"][:, hq], w), rdq) <= tol["grad"], ("dq", g)
+        assert rel(to_nat(got["dk"][:, g:g + 1], w), rdk) <= tol["grad"], ("dk", g)
+        assert rel(to_nat(got["dv"][:, g:g + 1], w), rdv) <= tol["grad"], ("dv", g)

@@ -20,6 +20,7 @@ import dataclasses
 import math
 from typing import Optional
 
+import numpy as np
 import torch
 
 
@@ -82,6 +83,15 @@ LONG_SWEEP = [LONG.replace(cp=cp, name=f"long_T131072_cp{cp}_zigzag") for cp in 
 
 ALL = {w.name: w for w in [TINY, GPT2, LLAMA, QWEN3, LONG, ULYSSES, GPT2_STRESS,
                            *GPT2_VARIANTS, *LONG_SWEEP]}
+
+
+def packed_starts(w: Workload, n_docs: int, seed: int = 1234) -> np.ndarray:
+    """Seeded document starts int32 [B, n_docs + 1] for packed sequences: n_docs - 1
+    distinct cut points drawn uniformly from 1..T-1, the same for every batch row."""
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.choice(np.arange(1, w.T), size=n_docs - 1, replace=False))
+    row = np.concatenate([[0], cuts, [w.T]]).astype(np.int32)
+    return np.tile(row, (w.B, 1))
 
 
 def draw(w: Workload, seed: Optional[int] = None):
