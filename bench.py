@@ -354,9 +354,11 @@ def run_cpattn(args, rank, world):
 
     # ---- end to end through the C ABI with host buffers
     host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
-    h2d = sum(x.numel() * x.element_size() for x in nat_host)
+    # the host holds what the library takes: natural-order tensors for the ring, the
+    # ranks' token shards for the a2a layout (prepared once, here)
+    up_host = nat_host if w.a2a == 1 else [x.cpu().pin_memory() for x in src]
+    h2d = sum(x.numel() * x.element_size() for x in up_host)
     d2h = sum(x.numel() * x.element_size() for x in host_out)
-    src_dev = src if w.a2a == 1 else None
     n_e2e = max(1, min(args.e2e_steps, args.steps))
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_e2e)]
@@ -371,9 +373,9 @@ def run_cpattn(args, rank, world):
         side_in.wait_event(a_ev)
         side_out.wait_event(a_ev)
         with torch.cuda.stream(side_in):
-            src[3].copy_(nat_host[3], non_blocking=True)
+            src[3].copy_(up_host[3], non_blocking=True)
             e_do.record(side_in)
-        for dst_, hsrc in zip(src[:3], nat_host[:3]):
+        for dst_, hsrc in zip(src[:3], up_host[:3]):
             dst_.copy_(hsrc, non_blocking=True)
         for s_, l_, h in zip(src[:3], lay[:3], H[:3]):
             cp.check(cp.cpattn_layout(fwd_perm, desc, s_, l_, h))
@@ -397,7 +399,7 @@ def run_cpattn(args, rank, world):
     # H_kv/2 K/V heads), so the second half's upload runs while the first half is
     # computed and the first half's gradients download while the second is.
     n_chunks = 2
-    chunked = (w.B == 1 and w.a2a == 1 and w.H_kv % n_chunks == 0 and src_dev is not None)
+    chunked = w.B == 1 and w.a2a == 1 and w.H_kv % n_chunks == 0
     if chunked:
         d_c = cp.make_desc(w.B, w.H_q // n_chunks, w.H_kv // n_chunks, w.T, w.D, w.cp, w.layout,
                            w.dtype)
@@ -416,11 +418,11 @@ def run_cpattn(args, rank, world):
         side_out.wait_event(a_ev)
         with torch.cuda.stream(side_in):
             for c in range(n_chunks):
-                for dst_, hsrc, h in zip(src[:3], nat_host[:3], H[:3]):
+                for dst_, hsrc, h in zip(src[:3], up_host[:3], H[:3]):
                     hs(dst_, c, h).copy_(hs(hsrc, c, h), non_blocking=True)
                 ev_in[c].record(side_in)
             for c in range(n_chunks):
-                hs(src[3], c, H[3]).copy_(hs(nat_host[3], c, H[3]), non_blocking=True)
+                hs(src[3], c, H[3]).copy_(hs(up_host[3], c, H[3]), non_blocking=True)
                 ev_do[c].record(side_in)
         for c in range(n_chunks):
             stream.wait_event(ev_in[c])
@@ -454,42 +456,28 @@ def run_cpattn(args, rank, world):
     for a, b in ev2:
         flush.zero_()
         a.record(stream)
-        if src_dev is not None:
-            (e2e_step_chunked if chunked else e2e_step_overlapped)(a)
-            b.record(stream)
-            continue
-        else:
-            for dst_, hsrc in zip((q, k, v, do), nat_host):
-                dst_.copy_(hsrc, non_blocking=True)
-            # token shards are rebuilt from the natural-order upload
-            for x, y, h in zip((q, k, v, do), src, H):
-                tmp = torch.empty_like(x)
-                cp.check(cp.cpattn_layout(cp.ZIGZAG_FWD, d_cp, x, tmp, h))
-                y.copy_(tmp.view(w.B, h, w.cp, w.T // w.cp, w.D).permute(2, 0, 3, 1, 4))
-        step()
-        for hdst, dsrc in zip(host_out, outs):
-            hdst.copy_(dsrc, non_blocking=True)
+        (e2e_step_chunked if chunked else e2e_step_overlapped)(a)
         b.record(stream)
     torch.cuda.synchronize()
     cp.check(cp.cpattn_check())
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev2), world, dev)
-    if chunked:
-        # the end-to-end outputs are the device step's, bit for bit (the head halves
-        # are independent problems with the same per-tile arithmetic)
-        e2e_out = [x.clone() for x in host_out]
-        step()
-        torch.cuda.synchronize()
-        if not all(torch.equal(a_, b_.cpu()) for a_, b_ in zip(e2e_out, outs)):
-            raise RuntimeError("end-to-end outputs differ from the device-resident step's")
+    # the end-to-end outputs are the device step's, bit for bit (the same calls on the
+    # same inputs; with head halves, independent problems with the same per-tile
+    # arithmetic)
+    e2e_out = [x.clone() for x in host_out]
+    step()
+    torch.cuda.synchronize()
+    if not all(torch.equal(a_, b_.cpu()) for a_, b_ in zip(e2e_out, outs)):
+        raise RuntimeError("end-to-end outputs differ from the device-resident step's")
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "transfers": ("pinned host buffers on side streams inside each step's events; the "
                          "heads split into two halves, each half a library call of its own, so "
                          "uploads and downloads of one half overlap the other half's compute"
-                         if src_dev is not None and chunked else
-                         "pinned host buffers; dO upload overlaps the forward and o download "
-                         "overlaps the backward on side streams inside each step's events"
-                         if src_dev is not None else "pinned host buffers, on the step's stream")}
+                         if chunked else
+                         "pinned host buffers (the ranks' token shards for the a2a layout); dO "
+                         "upload overlaps the forward and o download overlaps the backward on "
+                         "side streams inside each step's events")}
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
