@@ -88,6 +88,19 @@ def tensor_peak(pk, src_pk, timed_s):
     return pk["bf16_tflops"], f"{src_pk} bf16 dense burst (cuBLAS)"
 
 
+def hbm_roofline(kernel, nbytes, avg_ms, pk, src_pk):
+    """Roofline object of an HBM-bound dominant kernel: algorithmic bytes per launch
+    over its average launch time, against the measured copy bandwidth."""
+    if nbytes is None:
+        return {"bound": "hbm", "kernel": kernel, "achieved": None, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": None}
+    achieved = nbytes / (avg_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+            "peak_source": f"{src_pk} copy bandwidth", "work_per_launch": nbytes,
+            "avg_launch_ms": avg_ms}
+
+
 def config_of(w, extra=None):
     cfg = {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "T": w.T, "D": w.D,
            "cp": w.cp, "a2a": w.a2a, "layout": w.layout, "causal": True, "seed": w.seed,
@@ -181,8 +194,10 @@ def kernel_flops_or_bytes(name, w, pairs=None):
         return "tensor", 2.0 * w.D * pairs / w.cp
     if name == "bwd_prepass":
         return "hbm", 2.0 * rows_q * w.D * elt + 12.0 * rows_q
-    if name.startswith("layout"):                    # per launch: one tensor read + written
-        return "hbm", None
+    if name.startswith("layout"):
+        # a step permutes q, k, v, dO and o, dk, dv, dq (each read once and written
+        # once): the average launch moves (rows_q + rows_kv) rows each way
+        return "hbm", 2.0 * (rows_q + rows_kv) * w.D * elt / 2.0
     return "hbm", None
 
 
@@ -347,8 +362,7 @@ def run_cpattn(args, rank, world):
                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_what,
                 "work_per_launch": work, "avg_launch_ms": avg_ms}
     else:
-        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": None}
+        roof = hbm_roofline(dom, work, avg_ms, pk, src_pk)
     traffic = None if packed else traffic_for(dom, w.name)
     roof["traffic"] = traffic
 
@@ -592,8 +606,7 @@ def run_allgather(args, rank, world):
                 "work_per_launch": work, "avg_launch_ms": avg_ms,
                 "note": "work per launch is the average over the ranks (pairs / cp)"}
     else:
-        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": None}
+        roof = hbm_roofline(dom, work, avg_ms, pk, src_pk)
     roof["traffic"] = None
 
     # end to end: the ranks' inputs uploaded from pinned host memory and their
