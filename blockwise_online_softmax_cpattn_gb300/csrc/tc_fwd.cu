@@ -442,50 +442,83 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (c * 32 + j > thr || (PK && c * 32 + j < thr_lo))
                 r[c][j] = __float_as_uint(-INFINITY);
         }
-        float mx;
-        {
-          // 4 independent chains of three-input max over the 64 scores
+        // P = 2^(s * scale * log2e - mu) for the 64 scores: exponent arguments and row
+        // sums two lanes per instruction (packed fp32x2), 2^x on the special-function
+        // unit, P stored as bf16 over the scores.  With with_max set, the tile's max
+        // is taken in the same pass (4 independent chains of three-input max).
+        auto form_p = [&](auto with_max, float mu, float& mx) -> float {
+          const float2 nmu = make_float2(-mu, -mu);
+          float2 l4[4];
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2)
-              m4[(c * 16 + j / 2) & 3] = max3(m4[(c * 16 + j / 2) & 3], __uint_as_float(r[c][j]),
-                                              __uint_as_float(r[c][j + 1]));
-          mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
-        }
-        const float m_new = fmaxf(m_run, mx * p.scale_log2);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float s0 = __uint_as_float(r[c][2 * j]), s1 = __uint_as_float(r[c][2 * j + 1]);
+              if (decltype(with_max)::value) m4[(c * 16 + j) & 3] = max3(m4[(c * 16 + j) & 3], s0, s1);
+              const float2 x = fma2(make_float2(s0, s1), sl2v, nmu);
+              const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+              l4[j & 3] = add2(l4[j & 3], pp);
+              pk[j] = pack_bf16(pp.x, pp.y);
+            }
+            tmem_st16(t_s + c * 16, pk);
+          }
+          if (decltype(with_max)::value) mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+          return ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+        };
         bool rescale = false;
         float factor = 1.f;
-        if (cnt == 0) {
-          m_run = m_new;
-        } else if (m_new > m_run + 8.f) {
-          factor = ex2(m_run - m_new);
-          l_run *= factor;
-          m_run = m_new;
-          rescale = true;
-        }
-        const float mu = m_run == -INFINITY ? 0.f : m_run;
-        // P = 2^(s * scale * log2e - m): exponent arguments and row sums two lanes per
-        // instruction (packed fp32x2), 2^x on the special-function unit
-        const float2 nmu = make_float2(-mu, -mu);
-        float2 l4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) l4[i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 x = fma2(make_float2(__uint_as_float(r[c][2 * j]),
-                                              __uint_as_float(r[c][2 * j + 1])), sl2v, nmu);
-            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-            l4[j & 3] = add2(l4[j & 3], pp);
-            pk[j] = pack_bf16(pp.x, pp.y);
+        float lsum;
+        // form_p's TMEM stores are warp-collective: every branch around it is taken
+        // by the whole warp
+        if (cnt > 0 && __all_sync(0xffffffffu, m_run != -INFINITY)) {
+          // Against the running max straight away, the tile's max alongside: P stays
+          // below 2^8 unless the tile's max exceeds the running max by more than 8
+          // (log2 units).  Only then (rarely after an item's first tiles) is the
+          // running max raised and the tile's P formed again over what was stored,
+          // by the whole warp (a row whose max did not move forms the same P again).
+          float mx;
+          lsum = form_p(std::true_type{}, m_run, mx);
+          const float m_tile = mx * p.scale_log2;
+          const bool jump = m_tile > m_run + 8.f;
+          if (jump) {
+            factor = ex2(m_run - m_tile);
+            l_run *= factor;
+            m_run = m_tile;
+            rescale = true;
           }
-          tmem_st16(t_s + c * 16, pk);
+          if (__any_sync(0xffffffffu, jump)) {
+            tmem_wait_st();
+            lsum = form_p(std::false_type{}, m_run, mx);
+          }
+        } else {
+          float mx;
+          {
+            // 4 independent chains of three-input max over the 64 scores
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int j = 0; j < 32; j += 2)
+                m4[(c * 16 + j / 2) & 3] = max3(m4[(c * 16 + j / 2) & 3], __uint_as_float(r[c][j]),
+                                                __uint_as_float(r[c][j + 1]));
+            mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+          }
+          const float m_new = fmaxf(m_run, mx * p.scale_log2);
+          if (cnt == 0) {
+            m_run = m_new;
+          } else if (m_new > m_run + 8.f) {
+            factor = ex2(m_run - m_new);
+            l_run *= factor;
+            m_run = m_new;
+            rescale = true;
+          }
+          lsum = form_p(std::false_type{}, m_run == -INFINITY ? 0.f : m_run, mx);
         }
-        l_run += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+        l_run += lsum;
         tmem_wait_st();
         if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
           // O_h so far must be final in TMEM before it is rescaled
