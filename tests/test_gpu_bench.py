@@ -23,7 +23,7 @@ STEPS, WARMUP = 4, 3
 def _bench(*args):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", str(STEPS),
                         "--warmup", str(WARMUP), "--e2e-steps", "2", "--no-cpu-baseline", *args],
-                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+                       capture_output=True, text=True, timeout=240, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
     assert len(lines) == 1, r.stdout
