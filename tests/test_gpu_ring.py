@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_helpers import assert_close, full_reference, ring_inputs, run_ring
+from gpu_helpers import assert_close, dev, full_reference, ring_inputs, run_ring
+from oracle import layouts as OL
 
 pytestmark = pytest.mark.gpu
 
@@ -65,3 +66,20 @@ def test_rows_of_probabilities_sum_to_one_through_v_ones():
     got = run_ring(w, lay, bwd=False)
     o = got["o"].float().cpu().numpy()
     assert np.max(np.abs(o - 1.0)) < 1e-2
+
+
+def test_running_max_jumps_after_the_first_tile():
+    """Keys at natural positions [0, 256) scaled by 8: rank 1's query rows
+    (positions 256-767, cp 2 zigzag) visit their own chunk first, with modest scores,
+    and then rank 0's chunk, whose scores are larger by far more than 2^8 in the
+    exponent.  The forward then raises the running max and forms those tiles again,
+    across whole warps; the results must still match the oracle."""
+    w = W.Workload("jump_T1024_D128_cp2_zz", 1, 4, 2, 1024, 128, 2, "zigzag", "bf16")
+    q, k, v, do = W.draw_cast(w)
+    k = k.clone()
+    k[:, :, :256] *= 8  # exact in bf16
+    nat = (q, k, v, do)
+    pos = torch.from_numpy(OL.positions(w.T, w.cp // w.a2a, w.layout))
+    lay = [x[:, :, pos].contiguous().to(dev()) for x in nat]
+    got = run_ring(w, lay)
+    assert_close(w, got, full_reference(w, nat))
