@@ -87,3 +87,43 @@ def test_tensor_peak_burst_or_sustained():
     assert burst == 1900.0 and "burst" in what
     sus, what = bench.tensor_peak(pk, "measured", 1.5)
     assert sus == 1700.0 and "sustained" in what
+
+
+def test_packed_pair_count_matches_the_document_mask():
+    """The FLOP count of a packed step rests on the attended pairs: brute force
+    over the oracle's document mask must give the closed form bench.py uses."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import workloads as W
+    from oracle import attention as OA
+    w = W.Workload("pairs_T512", 2, 3, 1, 512, 64, 2, "zigzag", "bf16")
+    starts, pairs = bench.packed_documents(w, 6, seed=7)
+    pos = np.arange(w.T)
+    brute = sum(int(OA.packed_visible(pos, pos, starts[b]).sum()) for b in range(w.B)) * w.H_q
+    assert pairs == brute
+    assert starts.shape == (w.B, 7) and starts[0, 0] == 0 and starts[0, -1] == w.T
+    assert np.all(np.diff(starts[0]) > 0)  # distinct cuts: no empty document
+
+
+def test_permute_bytes_per_launch():
+    """A step permutes q, k, v, dO and o, dk, dv, dq once each (one read, one write):
+    the average launch moves the bytes of one query-sized and one K/V-sized tensor."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    w = W.LLAMA
+    per_step = 2 * 2 * w.D * (4 * w.B * w.H_q * w.T + 4 * w.B * w.H_kv * w.T)
+    bound, nbytes = bench.kernel_flops_or_bytes("layout_zigzag", w)
+    assert bound == "hbm" and nbytes == per_step / 8
+
+
+def test_hbm_roofline_arithmetic():
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    roof = bench.hbm_roofline("layout_zigzag", 1.0e8, 0.02, pk, "measured")
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    assert abs(roof["achieved"] - 5000.0) < 1e-6
+    assert abs(roof["frac"] - 5000.0 / 6800.0) < 1e-12
+    assert bench.hbm_roofline("x", None, 1.0, pk, "measured")["achieved"] is None
