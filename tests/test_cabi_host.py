@@ -125,8 +125,10 @@ def test_allgather_ranks_flags_and_workspace_are_checked(cp):
 def test_packed_arguments_are_checked(cp):
     d = _desc(cp)
     need = cp.cpattn_packed_workspace(d)
-    # documents of every position (lo, hi: int32 each) plus the backward statistics
-    assert need >= 2 * 512 * 4 + cp.cpattn_ring_bwd_workspace(d) and need % 256 == 0
+    # documents of every position (lo, hi: int32 each), the work orders of the
+    # 128-token tiles (int32 each), then the backward statistics
+    # (each section rounded up to 256 bytes: B1 T512 gives 2 x 2048 + 2 x 256)
+    assert need == 2 * 2048 + 2 * 256 + cp.cpattn_ring_bwd_workspace(d)
     assert cp.cpattn_packed_workspace(_desc(cp, a2a=2, cp=4, T=512)) == 0
     f = [FAKE] * 5
     assert cp.cpattn_ring_fwd_packed(d, FAKE, 0, *f, FAKE, need, 0) == 1      # n_docs < 1
