@@ -25,6 +25,7 @@ CASES = [
     W.Workload("ag_tc_T1024_cp2_contig", 2, 2, 2, 1024, 64, 2, "contiguous", "bf16"),
     W.Workload("ag_tc_T1024_cp4_zz_gqa3", 1, 3, 1, 1024, 128, 4, "zigzag", "bf16"),
     W.Workload("ag_tc_T512_cp1", 1, 2, 1, 512, 64, 1, "zigzag", "bf16"),
+    W.Workload("ag_tc_T2048_cp8_zz_D64_gqa2", 2, 4, 2, 2048, 64, 8, "zigzag", "bf16"),
     # SIMT paths: exact float32, and bf16 with a head dimension the tensor cores skip
     W.Workload("ag_simt_f32_T96_cp3_zz", 1, 2, 1, 96, 20, 3, "zigzag", "f32"),
     W.Workload("ag_simt_f32_T64_cp4", 2, 4, 2, 64, 16, 4, "contiguous", "f32"),

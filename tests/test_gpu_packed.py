@@ -30,6 +30,8 @@ CASES = [
      np.array([[0, 300, 301, 1200, 1200, 2048], [0, 128, 1024, 1025, 1919, 2048]], np.int32)),
     (W.Workload("pk_tc_T1024_cp2_contig_D64", 1, 4, 4, 1024, 64, 2, "contiguous", "bf16"), 37),
     (W.Workload("pk_tc_T1024_cp4_zz_gqa3", 1, 3, 1, 1024, 128, 4, "zigzag", "bf16"), 5),
+    # many short documents, a different cut in every row (work orders across rows)
+    (W.Workload("pk_tc_T2048_cp4_contig_D64_B3", 3, 4, 2, 2048, 64, 4, "contiguous", "bf16"), 40),
     (W.Workload("pk_simt_f32_T96_cp3_zz", 2, 2, 1, 96, 20, 3, "zigzag", "f32"), 4),
     (W.Workload("pk_simt_bf16_T128_cp2_D32", 1, 2, 2, 128, 32, 2, "zigzag", "bf16"), 3),
 ]
