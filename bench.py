@@ -35,6 +35,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -201,18 +202,30 @@ def kernel_flops_or_bytes(name, w, pairs=None):
     return "hbm", None
 
 
+_CODE_TOKEN = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"', re.S)
+
+
+def source_digest():
+    """Hash of the library's kernel sources with comments, trailing blanks and empty
+    lines removed, so that only a change of the code itself voids a capture."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "blockwise_online_softmax_cpattn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        code = _CODE_TOKEN.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+        lines = [ln.rstrip() for ln in code.splitlines()]
+        h.update(f.encode() + b"\0" + "\n".join(ln for ln in lines if ln).encode() + b"\0")
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel, workload):
     """dram bytes per launch from the committed ncu summary, if the kernel's
     sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "blockwise_online_softmax_cpattn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    digest = h.hexdigest()[:16]
+    digest = source_digest()
     with open(path) as f:
         for line in f:
             parts = line.split()

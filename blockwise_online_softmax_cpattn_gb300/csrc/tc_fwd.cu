@@ -25,21 +25,25 @@
 //   warp 0        TMA producer: the Q tile, then the K tiles through a ring of
 //                 shared-memory stages (128-byte swizzle); warp 3: the V tiles
 //                 through a ring of their own.
-//   warp 1        S issuer (one thread): S = Q K^T (SS form) into one of two
-//                 TMEM buffers, so S of the next tile is formed while the
-//                 softmax of this one runs.
-//   warp 2        PV issuer (one thread): O_h += P_h V_h (TS form, P_h read from
-//                 TMEM) for each half as soon as that half's P is stored.
-//                 Two issuers because a thread needs about 35-50 cycles to issue
-//                 one tcgen05.mma that runs 64 cycles at N = 128, the pipe queues
-//                 only a few, and a thread's next memory access after a
-//                 tcgen05.commit waits for the committed MMAs: one thread that
-//                 also waited on the softmax would leave the pipe idle.
+//   warp 1        S issuer: S = Q K^T (SS form) into one of two TMEM buffers, so
+//                 S of the next tile is formed while the softmax of this one runs.
+//   warp 2        PV issuer: O_h += P_h V_h (TS form, P_h read from TMEM) for each
+//                 half as soon as that half's P is stored.
+//                 Both issuers run as whole warps with warp-uniform descriptor
+//                 arithmetic and issue from one elected lane, which issues
+//                 markedly faster than a lone thread.  Two issuers because a
+//                 tcgen05.mma that runs 64 cycles at N = 128 takes tens of cycles
+//                 to issue, the pipe queues only a few, and a thread's next memory
+//                 access after a tcgen05.commit waits for the committed MMAs: one
+//                 issuer that also waited on the softmax would leave the pipe idle.
 //   warps 4..11   softmax: warp w serves TMEM lane quadrant w%4 (32 rows) and
 //                 column half (w-4)/4.  tcgen05.ld of its 64 scores, causal
-//                 mask, max, P = 2^(s*scale*log2e - m) rounded to bf16 into
-//                 TMEM, sum in fp32.  O_h is rescaled only when the running max
-//                 grows by more than 2^8 (exact after the final division).
+//                 mask, P = 2^(s*scale*log2e - m) rounded to bf16 into TMEM, sum
+//                 in fp32.  O_h is rescaled only when the running max grows by
+//                 more than 2^8 (exact after the final division); thanks to that
+//                 slack P is formed against the running max in the same pass that
+//                 takes the tile's max, and formed again only when a row's max
+//                 rose by more than 2^8.
 //   epilogue      M = max(m_0, m_1), w_h = 2^(m_h - M), L = w_0 l_0 + w_1 l_1,
 //                 O = (w_0 O_0 + w_1 O_1) / L rounded once to the output dtype,
 //                 LSE = ln 2 (M + log2 L).
