@@ -127,3 +127,22 @@ def test_hbm_roofline_arithmetic():
     assert abs(roof["achieved"] - 5000.0) < 1e-6
     assert abs(roof["frac"] - 5000.0 / 6800.0) < 1e-12
     assert bench.hbm_roofline("x", None, 1.0, pk, "measured")["achieved"] is None
+
+
+def test_source_digest_ignores_comments_only(tmp_path, monkeypatch):
+    """The DRAM-traffic figures stay valid across comment edits and are voided by any
+    change of the code (strings included)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "blockwise_online_softmax_cpattn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    src = 'int f(int x) {  // doubles\n  return 2 * x;  /* one\n line */\n}\nconst char* s = "a // b";\n'
+    (csrc / "k.cu").write_text(src)
+    d0 = bench.source_digest()
+    (csrc / "k.cu").write_text(src.replace("// doubles", "// twice x").replace("one\n line", "a\nb\nc"))
+    assert bench.source_digest() == d0
+    (csrc / "k.cu").write_text(src.replace("2 * x", "3 * x"))
+    assert bench.source_digest() != d0
+    (csrc / "k.cu").write_text(src.replace('"a // b"', '"a // c"'))
+    assert bench.source_digest() != d0
