@@ -4,14 +4,17 @@ The oracle computes sampled outputs one by one from the definition: output rows
 and dQ rows of chosen heads at chosen positions (each with all of its keys), and
 dK/dV rows in bands near the end of the sequence (only the queries after them
 take part).  Properties that hold at any size cover the rest: sum_j dK_j = 0 per
-K/V head and sum_j dV_j = the group's sum of dO.
+K/V head and sum_j dV_j = the group's sum of dO.  At the LLaMA shape the oracle
+also computes one whole K/V group (its four query heads at every position), so a
+slip confined to some middle tiles cannot hide between the samples.
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads as W
-from gpu_helpers import LSE_ABS_TOL, TOL, cp_mod, desc_of, dev, rel, ring_inputs, run_ring
+from gpu_helpers import (LSE_ABS_TOL, TOL, cp_mod, desc_of, dev, rel, ring_inputs, run_ring,
+                         to_nat)
 from oracle import attention as OA
 from oracle import layouts as OL
 
@@ -65,6 +68,24 @@ def check_sampled(w, nat, got, heads, kv_bands, rows_seed=0):
     assert err <= 1e-2 * float(do_dev.abs().max()) + 1e-2 * float(dv.abs().sum(dim=2).max()) / 64
 
 
+def check_whole_group(w, nat, got, g):
+    """Every element of one K/V group against the oracle: O, LSE and dQ of its
+    n_rep query heads at all T positions, and all of dK, dV of K/V head g."""
+    n_rep = w.H_q // w.H_kv
+    hq = slice(g * n_rep, (g + 1) * n_rep)
+    q, do = (W.as_f64(x[:, hq]) for x in (nat[0], nat[3]))
+    k, v = (W.as_f64(x[:, g:g + 1]) for x in (nat[1], nat[2]))
+    ro, rlse = OA.attention_fwd(q, k, v, w.scale)
+    rdq, rdk, rdv = OA.attention_bwd(q, k, v, do, w.scale)
+    tol = TOL[w.dtype]
+    assert rel(to_nat(got["o"][:, hq], w), ro) <= tol["o"], ("o", g)
+    lse = to_nat(got["lse"][:, hq].unsqueeze(-1), w)[..., 0]
+    assert float(np.max(np.abs(lse - rlse))) <= LSE_ABS_TOL[w.dtype], ("lse", g)
+    assert rel(to_nat(got["dq"][:, hq], w), rdq) <= tol["grad"], ("dq", g)
+    assert rel(to_nat(got["dk"][:, g:g + 1], w), rdk) <= tol["grad"], ("dk", g)
+    assert rel(to_nat(got["dv"][:, g:g + 1], w), rdv) <= tol["grad"], ("dv", g)
+
+
 def test_llama_gqa_T8192_cp8_zigzag():
     w = W.LLAMA
     nat, lay = ring_inputs(w)
@@ -74,6 +95,9 @@ def test_llama_gqa_T8192_cp8_zigzag():
     bands = [(0, np.arange(T - 384, T)), (7, np.arange(T // 2, T // 2 + 128)),
              (3, np.arange(T - 128, T))]
     check_sampled(w, nat, got, heads=[0, 3, 13, 31], kv_bands=bands)
+    # one K/V group in full (query heads 20-23, K/V head 5): every tile of every
+    # work item of those heads, middle tiles included
+    check_whole_group(w, nat, got, g=5)
 
 
 def test_qwen3_gqa_a2a2_p2p4_zigzag():
