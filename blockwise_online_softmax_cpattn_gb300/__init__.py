@@ -7,7 +7,9 @@ call returns the ``cpattn_status`` code (0 = OK).  ``check(status)`` turns a
 non-zero code into ``CpattnError``.
 
 The shared library is built in-tree by ``build_lib.build()``; importing this
-package without it raises ImportError (there is no fallback).
+package without it raises ImportError (there is no fallback).  With the
+environment variable CPATTN_DEBUG_LIB=1 the package loads the CPATTN_DEBUG build
+(``libcpattn_debug.so``, the same kernels with bounds checks) instead.
 """
 from __future__ import annotations
 
@@ -17,7 +19,8 @@ import os
 from typing import Optional
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libcpattn.so")
+DEBUG_LIB = os.environ.get("CPATTN_DEBUG_LIB") == "1"
+LIB_PATH = os.path.join(_PKG, "libcpattn_debug.so" if DEBUG_LIB else "libcpattn.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -26,7 +29,7 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = 0, 1, 2, 3, 4, 5
 F32, BF16 = 0, 1
 CONTIGUOUS, ZIGZAG = 0, 1
 ZIGZAG_FWD, ZIGZAG_INV, A2A_FWD, A2A_INV = 0, 1, 2, 3

@@ -454,6 +454,7 @@ const char* cpattn_status_string(cpattn_status status) {
     case CPATTN_ERR_UNSUPPORTED: return "unsupported shape or option";
     case CPATTN_ERR_CUDA: return "CUDA error";
     case CPATTN_ERR_TIMEOUT: return "device wait timed out";
+    case CPATTN_ERR_BOUNDS: return "device bounds check failed (debug build)";
     default: return "unknown status";
   }
 }

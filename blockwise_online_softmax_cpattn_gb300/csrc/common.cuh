@@ -15,6 +15,7 @@ namespace cpattn {
 // Device status codes (the values of cpattn_status).
 constexpr int kStatusLaunch = 3;   // a kernel found its launch unusable (reported as a CUDA error)
 constexpr int kStatusTimeout = 4;
+constexpr int kStatusBounds = 5;   // a bounds check of a CPATTN_DEBUG build failed
 
 // ---------------------------------------------------------------------------
 // Token position maps.  Slot = index on the layout-order token axis; position =
@@ -152,6 +153,23 @@ __device__ __forceinline__ int item_of(int k, int n_items) {
 
 __device__ __forceinline__ void latch_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
+}
+
+// Bounds checks of the tensor-core kernels' hand-computed global rows (TMA tile
+// rows, statistics loads, epilogue stores).  A build with CPATTN_DEBUG defined
+// evaluates them: a failed check latches CPATTN_ERR_BOUNDS in the device status
+// word and the caller skips the access (a skipped load then also ends in a
+// bounded-wait time-out).  Other builds compile them away.
+__device__ __forceinline__ bool in_bounds(int64_t first, int64_t count, int64_t extent,
+                                          int* status) {
+#ifdef CPATTN_DEBUG
+  if (first >= 0 && count >= 0 && first + count <= extent) return true;
+  latch_status(status, kStatusBounds);
+  return false;
+#else
+  (void)first, (void)count, (void)extent, (void)status;
+  return true;
+#endif
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

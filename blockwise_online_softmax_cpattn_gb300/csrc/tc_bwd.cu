@@ -23,8 +23,11 @@
 //
 // Delta = rowsum(dO * O) comes from the pre-pass kernel (merge.cu).  Compute
 // warps: 8, warp w handles TMEM lane quadrant w%4 and column half (w-4)/4.
-// Warp 0 loads through TMA; warps 1 and 3 issue the score products (S and dP)
-// and warp 2 the gradient products (dV/dK or dQ), one thread each.
+// Warp 0 loads through TMA.  The MMA issuers are whole warps: every lane runs
+// the issue loop (warp-uniform descriptor arithmetic and waits) and one lane,
+// chosen by elect.sync, issues each tcgen05 instruction and commit.  dK/dV:
+// warp 1 issues S^T, warp 2 dP^T, dV and dK.  dQ: warp 1 issues S, warp 3 dP,
+// warp 2 dQ.
 // Every mbarrier wait is bounded (see tc_fwd.cu for the abort protocol).
 #include <math.h>
 
@@ -35,8 +38,13 @@ namespace tcbwd {
 
 constexpr int kTile = 128;
 constexpr int kThreads = 384;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kTimeoutNs = 2000000000ull;     // 2 s
+constexpr uint64_t kDebugTimeoutNs = 50000000ull;  // 50 ms under the fault hook
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;
+// Values of the descriptor's test hook that make one of these kernels withhold a
+// load (1 is the forward's)
+constexpr int kFaultDkdv = 2;
+constexpr int kFaultDq = 3;
 constexpr float kLog2e = 1.44269504088896340736f;
 
 enum : int { kEmpty = 0, kFull = 1, kDiag = 2 };
@@ -64,6 +72,9 @@ struct Params {
   // dQ kernel's query tiles and the dK/dV kernel's key tiles
   const int* ord_q;
   const int* ord_k;
+  // test hook: kFaultDkdv / kFaultDq make that kernel's producer withhold its first
+  // query-side load, so the bounded waits on it run out (50 ms under any hook value)
+  int debug_fault;
 };
 
 // Query tiles of rank r at positions >= kpos0 (chunk bounds and kpos0 lie on the
@@ -89,8 +100,8 @@ __device__ __forceinline__ int classify(int qpos0, int kpos0, const int* lo_row)
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t par, volatile int* abort,
-                                          int* status) {
-  bool ok = mbar_wait(bar, par, abort, status, kTimeoutNs);
+                                          int* status, uint64_t tmo) {
+  bool ok = mbar_wait(bar, par, abort, status, tmo);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -176,6 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t tmo = p.debug_fault ? kDebugTimeoutNs : kTimeoutNs;
+  // row extents of the tensors (for the bounds checks of a CPATTN_DEBUG build): q,
+  // k/v, and dO / the statistics / dQ (the rank's rows only in all-gather mode)
+  const int64_t q_rows = (int64_t)p.B * p.Hq * p.T, kv_rows = (int64_t)p.B * p.Hkv * p.T;
+  const int64_t s_rows = p.ag_rank >= 0 ? (int64_t)p.B * p.Hq * p.m.c : q_rows;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
@@ -246,31 +262,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_do);
       const int krow = (b * p.Hkv + g) * p.T + kslot0;
       mbar_expect_tx(kv_full, 2 * L::kTB);
-      for (int kb = 0; kb < D / 64; ++kb) {
-        tma_load_2d(sbase + L::kK + kb * (kTile * 128), &tm_k, kb * 64, krow, kv_full);
-        tma_load_2d(sbase + L::kV + kb * (kTile * 128), &tm_v, kb * 64, krow, kv_full);
-      }
+      if (in_bounds(krow, kTile, kv_rows, p.status))
+        for (int kb = 0; kb < D / 64; ++kb) {
+          tma_load_2d(sbase + L::kK + kb * (kTile * 128), &tm_k, kb * 64, krow, kv_full);
+          tma_load_2d(sbase + L::kV + kb * (kTile * 128), &tm_v, kb * 64, krow, kv_full);
+        }
       StageRing<QS> qr;
       StageRing<DS> dr;
+      bool first = true;
       Walk wk;
       for (walk_start(wk); !wk.done(); walk_next(wk)) {
         const int qbh = b * p.Hq + g * p.n_rep + wk.rep;
         const int qrow = qbh * p.T + wk.slot();
         // rows of dO and of the statistics (the rank's own rows in all-gather mode)
         const int srow = AG ? qbh * p.m.c + (wk.slot() - p.ag_rank * p.m.c) : qrow;
-        if (!mbar_wait(q_empty(qr.stage), qr.par ^ 1, abort, p.status, kTimeoutNs)) break;
-        mbar_expect_tx(q_full(qr.stage), L::kTB + 512);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kQ + qr.stage * L::kTB + kb * (kTile * 128), &tm_q, kb * 64, qrow,
-                      q_full(qr.stage));
-        bulk_load(sbase + L::kLse + qr.stage * 512, p.lse2 + srow, 512, q_full(qr.stage));
-        qr.mark_issued();
-        if (!mbar_wait(do_empty(dr.stage), dr.par ^ 1, abort, p.status, kTimeoutNs)) break;
+        if (!mbar_wait(q_empty(qr.stage), qr.par ^ 1, abort, p.status, tmo)) break;
+        // fault hook: the first Q tile never arrives, so the waits on it run out
+        if (!(p.debug_fault == kFaultDkdv && first)) {
+          mbar_expect_tx(q_full(qr.stage), L::kTB + 512);
+          if (in_bounds(qrow, kTile, q_rows, p.status) && in_bounds(srow, kTile, s_rows, p.status)) {
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_2d(sbase + L::kQ + qr.stage * L::kTB + kb * (kTile * 128), &tm_q, kb * 64,
+                          qrow, q_full(qr.stage));
+            bulk_load(sbase + L::kLse + qr.stage * 512, p.lse2 + srow, 512, q_full(qr.stage));
+          }
+          qr.mark_issued();
+        }
+        first = false;
+        if (!mbar_wait(do_empty(dr.stage), dr.par ^ 1, abort, p.status, tmo)) break;
         mbar_expect_tx(do_full(dr.stage), L::kTB + 512);
-        for (int kb = 0; kb < D / 64; ++kb)
-          tma_load_2d(sbase + L::kDO + dr.stage * L::kTB + kb * (kTile * 128), &tm_do, kb * 64,
-                      srow, do_full(dr.stage));
-        bulk_load(sbase + L::kDelta + dr.stage * 512, p.delta + srow, 512, do_full(dr.stage));
+        if (in_bounds(srow, kTile, s_rows, p.status)) {
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_2d(sbase + L::kDO + dr.stage * L::kTB + kb * (kTile * 128), &tm_do, kb * 64,
+                        srow, do_full(dr.stage));
+          bulk_load(sbase + L::kDelta + dr.stage * 512, p.delta + srow, 512, do_full(dr.stage));
+        }
         dr.mark_issued();
         qr.advance();
         dr.advance();
@@ -291,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // issues.
       const bool leader = elect_one();
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);
-      bool ok = warp_wait(kv_full, 0, abort, p.status);
+      bool ok = warp_wait(kv_full, 0, abort, p.status, tmo);
       tc_fence_after();
       constexpr uint32_t kTD = L::kTB >> 4;
       const uint64_t kd = sdesc_sw128(sbase + L::kK, 16, 1024);
@@ -306,10 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The two warps wait for each other's previous product to be queued
         // (S^T(t+1) after dP^T(t), dP^T(t+1) after S^T(t+1)), which keeps the two
         // arrival barriers in lockstep.
-        if (cnt > 0 && !(ok = warp_wait(dp_issued, (cnt - 1) & 1, abort, p.status))) break;
-        if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status))) break;
+        if (cnt > 0 && !(ok = warp_wait(dp_issued, (cnt - 1) & 1, abort, p.status, tmo))) break;
+        if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status, tmo))) break;
         // the S region is free once the compute warps have loaded the previous S^T
-        if (cnt > 0 && !(ok = warp_wait(s_free, (cnt - 1) & 1, abort, p.status))) break;
+        if (cnt > 0 && !(ok = warp_wait(s_free, (cnt - 1) & 1, abort, p.status, tmo))) break;
         tc_fence_after();
         const uint64_t qd = qd0 + (uint64_t)(qr.stage * kTD);
 #pragma unroll
@@ -353,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_tiles =
           PK ? p.n_rep * (pk_last - (kpos0 >> 7) + 1)
              : p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0) : (p.T - kpos0) >> 7);
-      bool ok = warp_wait(kv_full, 0, abort, p.status);
+      bool ok = warp_wait(kv_full, 0, abort, p.status, tmo);
       tc_fence_after();
       StageRing<QS> qr;   // Q stage of tile t
       StageRing<DS> dr;   // dO stage of tile t
@@ -374,14 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         dpr.advance();
       };
       // dP^T(0), behind S^T(0)
-      if (ok && n_tiles > 0 && (ok = warp_wait(do_full(dpr.stage), dpr.par, abort, p.status)) &&
-          (ok = warp_wait(s_issued, 0, abort, p.status))) {
+      if (ok && n_tiles > 0 && (ok = warp_wait(do_full(dpr.stage), dpr.par, abort, p.status, tmo)) &&
+          (ok = warp_wait(s_issued, 0, abort, p.status, tmo))) {
         tc_fence_after();
         issue_dp();
       }
       for (int t = 0; ok && t < n_tiles; ++t) {
         // dV(t) += P^T(t) dO(t)  (dO landed before dP^T(t) was issued)
-        if (!(ok = warp_wait(p_full, t & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(p_full, t & 1, abort, p.status, tmo))) break;
         tc_fence_after();
         const uint64_t dod = dod_mn0 + (uint64_t)(dr.stage * kTD);
 #pragma unroll
@@ -393,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dK(t) += dS^T(t) Q(t) (Q landed before S^T(t)); dO(t+1) landed and S^T(t+1)
         // queued for dP^T(t+1)
         const bool more = t + 1 < n_tiles;
-        if (!(ok = warp_wait(ds_full, t & 1, abort, p.status))) break;
-        if (more && !(ok = warp_wait(do_full(dpr.stage), dpr.par, abort, p.status))) break;
-        if (more && !(ok = warp_wait(s_issued, (t + 1) & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(ds_full, t & 1, abort, p.status, tmo))) break;
+        if (more && !(ok = warp_wait(do_full(dpr.stage), dpr.par, abort, p.status, tmo))) break;
+        if (more && !(ok = warp_wait(s_issued, (t + 1) & 1, abort, p.status, tmo))) break;
         tc_fence_after();
         const uint64_t qd = qd_mn0 + (uint64_t)(qr.stage * kTD);
 #pragma unroll
@@ -441,14 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (walk_start(wk); !wk.done(); walk_next(wk)) {
       const int qpos0 = wk.pos();
       const int cls = classify(qpos0, kpos0, lo_row);
-      if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status))) break;  // -LSE log2e landed
+      if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status, tmo))) break;  // -LSE log2e landed
       const float* lse_t = lse_s + qr.stage * 128 + half * 64;
       const float* del_t = del_s + dr.stage * 128 + half * 64;
       // this half's 64 per-query LSE values, fetched while S^T is still being computed
       float4 nl4[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) nl4[i] = reinterpret_cast<const float4*>(lse_t)[i];
-      if (!(ok = warp_wait(s_full, cnt & 1, abort, p.status))) break;
+      if (!(ok = warp_wait(s_full, cnt & 1, abort, p.status, tmo))) break;
       tc_fence_after();
       uint32_t sr[2][32];
       tmem_ld32(t_s, sr[0]);
@@ -481,11 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[j0 + 1] = p1;
         }
       // -Delta of this half's 64 queries (it travels with dO), fetched before dP^T is ready
-      if (!(ok = warp_wait(do_full(dr.stage), dr.par, abort, p.status))) break;
+      if (!(ok = warp_wait(do_full(dr.stage), dr.par, abort, p.status, tmo))) break;
       float4 nd4[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) nd4[k] = reinterpret_cast<const float4*>(del_t)[k];
-      if (!(ok = warp_wait(dp_full, cnt & 1, abort, p.status))) break;
+      if (!(ok = warp_wait(dp_full, cnt & 1, abort, p.status, tmo))) break;
       tc_fence_after();
       tmem_ld32(t_dp, sr[0]);
       tmem_ld32(t_dp + 32, sr[1]);
@@ -526,11 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       qr.advance();
       dr.advance();
     }
-    if (ok && cnt > 0) ok = warp_wait(final_bar, 0, abort, p.status);
+    if (ok && cnt > 0) ok = warp_wait(final_bar, 0, abort, p.status, tmo);
+    // (the TMEM loads below are warp-collective: only the global stores are guarded)
+    const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
+    const bool store = in_bounds(orow, 1, kv_rows, p.status);
     if (ok && AG) {
       // all-gather: float32 share of this rank's queries, added to the sum so far
       tc_fence_after();
-      const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
       float* dkf = static_cast<float*>(p.out0) + orow * D + half * (D / 2);
       float* dvf = static_cast<float*>(p.out1) + orow * D + half * (D / 2);
       if (cnt > 0 || !p.accumulate) {
@@ -548,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mul = which ? p.scale : 1.f;
             float4* dst = reinterpret_cast<float4*>((which ? dkf : dvf) + c * 32);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 8 && store; ++j) {
               float4 x = make_float4(__uint_as_float(v32[4 * j]) * mul,
                                      __uint_as_float(v32[4 * j + 1]) * mul,
                                      __uint_as_float(v32[4 * j + 2]) * mul,
@@ -567,7 +595,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (ok) {
       tc_fence_after();
-      const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
       __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(p.out0) + orow * D + half * (D / 2);
       __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.out1) + orow * D + half * (D / 2);
 #pragma unroll 1
@@ -580,12 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v32[j] = 0u;
         }
-        store_row32_bf16(dv + c * 32, v32, 1.f);
+        if (store) store_row32_bf16(dv + c * 32, v32, 1.f);
         if (cnt > 0) {
           tmem_ld32(tmem + lane_off + 256 + D + half * (D / 2) + c * 32, v32);
           tmem_wait_ld();
         }
-        store_row32_bf16(dk + c * 32, v32, p.scale);
+        if (store) store_row32_bf16(dk + c * 32, v32, p.scale);
       }
     }
   }
@@ -665,6 +692,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t tmo = p.debug_fault ? kDebugTimeoutNs : kTimeoutNs;
+  // row extents of the tensors (for the bounds checks of a CPATTN_DEBUG build): q,
+  // k/v, and dO / the statistics / dQ (the rank's rows only in all-gather mode)
+  const int64_t q_rows = (int64_t)p.B * p.Hq * p.T, kv_rows = (int64_t)p.B * p.Hkv * p.T;
+  const int64_t s_rows = p.ag_rank >= 0 ? (int64_t)p.B * p.Hq * p.m.c : q_rows;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
@@ -760,27 +792,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
         const DqItem it = decode(w);
         // Q and dO of this item once the S and dP issuers are done with the last one's
-        if (k > 0 && !(ok = mbar_wait(qdo_empty, (k - 1) & 1, abort, p.status, kTimeoutNs))) break;
-        mbar_expect_tx(qdo_full, 2 * L::kTB);
-        for (int kb = 0; kb < D / 64; ++kb) {
-          tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)it.qrow, qdo_full);
-          tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)it.srow, qdo_full);
+        if (k > 0 && !(ok = mbar_wait(qdo_empty, (k - 1) & 1, abort, p.status, tmo))) break;
+        // fault hook: the first item's Q and dO never arrive, so the waits on them run out
+        if (!(p.debug_fault == kFaultDq && k == 0)) {
+          mbar_expect_tx(qdo_full, 2 * L::kTB);
+          if (in_bounds(it.qrow, kTile, q_rows, p.status) &&
+              in_bounds(it.srow, kTile, s_rows, p.status))
+          for (int kb = 0; kb < D / 64; ++kb) {
+            tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, (int)it.qrow, qdo_full);
+            tma_load_2d(sbase + L::kDO + kb * (kTile * 128), &tm_do, kb * 64, (int)it.srow,
+                        qdo_full);
+          }
+          q_last = k;
         }
-        q_last = k;
         Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           const int row = it.kv_row_base + wk.slot();
-          if (!(ok = mbar_wait(k_empty(kr.stage), kr.par ^ 1, abort, p.status, kTimeoutNs))) break;
+          if (!(ok = mbar_wait(k_empty(kr.stage), kr.par ^ 1, abort, p.status, tmo))) break;
           mbar_expect_tx(k_full(kr.stage), L::kTB);
-          for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_2d(sbase + L::kK + kr.stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64, row,
-                        k_full(kr.stage));
+          const bool kv_ok = in_bounds(row, kTile, kv_rows, p.status);
+          if (kv_ok)
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_2d(sbase + L::kK + kr.stage * L::kTB + kb * (kTile * 128), &tm_k, kb * 64,
+                          row, k_full(kr.stage));
           kr.mark_issued();
-          if (!(ok = mbar_wait(v_empty(vr.stage), vr.par ^ 1, abort, p.status, kTimeoutNs))) break;
+          if (!(ok = mbar_wait(v_empty(vr.stage), vr.par ^ 1, abort, p.status, tmo))) break;
           mbar_expect_tx(v_full(vr.stage), L::kTB);
-          for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_2d(sbase + L::kV + vr.stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64, row,
-                        v_full(vr.stage));
+          if (kv_ok)
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_2d(sbase + L::kV + vr.stage * L::kTB + kb * (kTile * 128), &tm_v, kb * 64,
+                          row, v_full(vr.stage));
           vr.mark_issued();
           kr.advance();
           vr.advance();
@@ -813,22 +854,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int w;
       for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
         const DqItem it = decode(w);
-        if (!(ok = warp_wait(qdo_full, k & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(qdo_full, k & 1, abort, p.status, tmo))) break;
         Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
           uint32_t dst;
           uint64_t bd;
           if (is_s) {
             // S(g): the S region is free once the compute warps have read S(g-1)
-            if (g > 0 && !(ok = warp_wait(s_free, (g - 1) & 1, abort, p.status))) break;
-            if (!(ok = warp_wait(k_full(kr.stage), kr.par, abort, p.status))) break;
+            if (g > 0 && !(ok = warp_wait(s_free, (g - 1) & 1, abort, p.status, tmo))) break;
+            if (!(ok = warp_wait(k_full(kr.stage), kr.par, abort, p.status, tmo))) break;
             dst = tmem;
             bd = bd0 + (uint64_t)(kr.stage * kTD);
           } else {
             // dP(g) into buffer g&1: free once dQ(g-2) has read the dS stored there
-            if (g >= 2 && !(ok = warp_wait(dq_done(g & 1), ((g - 2) >> 1) & 1, abort, p.status)))
+            if (g >= 2 && !(ok = warp_wait(dq_done(g & 1), ((g - 2) >> 1) & 1, abort, p.status, tmo)))
               break;
-            if (!(ok = warp_wait(v_full(vr.stage), vr.par, abort, p.status))) break;
+            if (!(ok = warp_wait(v_full(vr.stage), vr.par, abort, p.status, tmo))) break;
             dst = tmem + 128 + 128 * (g & 1);
             bd = bd0 + (uint64_t)(vr.stage * kTD);
           }
@@ -876,9 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int t = 0;  // tile of this item
         Walk wk;
         for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
-          if (!(ok = warp_wait(ds_full(g & 1), (g >> 1) & 1, abort, p.status))) break;
+          if (!(ok = warp_wait(ds_full(g & 1), (g >> 1) & 1, abort, p.status, tmo))) break;
           // the item's first dQ overwrites the accumulator the previous epilogue read
-          if (t == 0 && k > 0 && !(ok = warp_wait(dq_free, (k - 1) & 1, abort, p.status))) break;
+          if (t == 0 && k > 0 && !(ok = warp_wait(dq_free, (k - 1) & 1, abort, p.status, tmo))) break;
           tc_fence_after();
           // K(g) landed before S(g), which the compute warps read before storing dS(g)
           const uint64_t kd_mn = kd_mn0 + (uint64_t)(kr.stage * kTD);
@@ -919,14 +960,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const DqItem it = decode(w);
       const int* lo_row = doc_row(it);
       const int lo_q = PK ? lo_row[it.qpos0 + row] : 0;  // packed: first key of the document
-      const float2 nl2 = make_float2(p.lse2[it.srow + row], p.lse2[it.srow + row]);  // -LSE log2e
-      const float2 ndl = make_float2(p.delta[it.srow + row], p.delta[it.srow + row]);  // -Delta
+      const bool row_ok = in_bounds(it.srow + row, 1, s_rows, p.status);
+      const float sl = row_ok ? p.lse2[it.srow + row] : 0.f, sd = row_ok ? p.delta[it.srow + row] : 0.f;
+      const float2 nl2 = make_float2(sl, sl);  // -LSE log2e
+      const float2 ndl = make_float2(sd, sd);  // -Delta
       int cnt = 0;  // tiles of this item
       Walk wk;
       for (walk_start(wk, it); !wk.done(); walk_next(wk, it)) {
         const int kpos0 = wk.pos();
         const int cls = classify(it.qpos0, kpos0, lo_row);
-        if (!(ok = warp_wait(s_full, g & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(s_full, g & 1, abort, p.status, tmo))) break;
         tc_fence_after();
         uint32_t sr[2][32];
         tmem_ld32(t_s, sr[0]);
@@ -953,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pr[j0] = p0;
             pr[j0 + 1] = p1;
           }
-        if (!(ok = warp_wait(dp_full(g & 1), (g >> 1) & 1, abort, p.status))) break;
+        if (!(ok = warp_wait(dp_full(g & 1), (g >> 1) & 1, abort, p.status, tmo))) break;
         tc_fence_after();
         const uint32_t t_dp = tmem + lane_off + 128 + 128 * (g & 1) + half * 64;
         tmem_ld32(t_dp, sr[0]);
@@ -980,11 +1023,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (cnt > 0 &&
-          !(ok = warp_wait(dq_done((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.status)))
+          !(ok = warp_wait(dq_done((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.status, tmo)))
         break;
       tc_fence_after();
       __nv_bfloat16* dq =
           static_cast<__nv_bfloat16*>(p.out0) + (it.srow + row) * D + half * (D / 2);
+      // (the TMEM loads are warp-collective: only the global stores are guarded)
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v32[32];
@@ -995,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) v32[jj] = 0u;
         }
-        store_row32_bf16(dq + c * 32, v32, p.scale);
+        if (row_ok) store_row32_bf16(dq + c * 32, v32, p.scale);
       }
       // the accumulator has been read: the next item's first dQ may overwrite it
       tc_fence_before();
@@ -1086,6 +1130,7 @@ static tcbwd::Params bwd_params(const Ring& R, const float* lse2, const float* d
   p.doc_hi = nullptr;
   p.ord_q = nullptr;
   p.ord_k = nullptr;
+  p.debug_fault = R.debug_fault;
   return p;
 }
 

@@ -212,6 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = p.debug_fault ? kDebugTimeoutNs : kTimeoutNs;
+  // row extents of the tensors (for the bounds checks of a CPATTN_DEBUG build)
+  const int64_t q_rows = (int64_t)p.B * p.Hq * p.T, kv_rows = (int64_t)p.B * p.Hkv * p.T;
+  const int64_t o_rows = p.q_rank >= 0 ? (int64_t)p.B * p.Hq * p.m.c : q_rows;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) {
@@ -278,11 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (is_k) {
           // the Q buffer is free once the last S of the previous item has read it
           if (k > 0 && !(ok = mbar_wait(q_empty, (k - 1) & 1, abort, p.status, tmo))) break;
-          if (!(k == 0 && p.debug_fault)) {  // fault hook: the first Q load never happens
+          if (!(k == 0 && p.debug_fault == 1)) {  // fault hook: the first Q load never happens
             mbar_expect_tx(q_full, L::kTileBytes);
             const int row = (it.b * p.Hq + it.h) * p.T + it.slot0;
-            for (int kb = 0; kb < D / 64; ++kb)
-              tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, row, q_full);
+            if (in_bounds(row, kTile, q_rows, p.status))
+              for (int kb = 0; kb < D / 64; ++kb)
+                tma_load_2d(sbase + L::kQ + kb * (kTile * 128), &tm_q, kb * 64, row, q_full);
             q_last = k;
           }
         }
@@ -293,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(empty, par ^ 1, abort, p.status, tmo))) break;
           const int row = kv_row_base + wk.slot();
           mbar_expect_tx(full, L::kTileBytes);
-          for (int kb = 0; kb < D / 64; ++kb)
-            tma_load_2d(base + stage * L::kTileBytes + kb * (kTile * 128), tm, kb * 64, row, full);
+          if (in_bounds(row, kTile, kv_rows, p.status))
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_2d(base + stage * L::kTileBytes + kb * (kTile * 128), tm, kb * 64, row, full);
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | ((uint32_t)par << stage);
           if (++stage == nst) stage = 0, par ^= 1;
@@ -575,6 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t orow = local ? bh * p.m.c + (it.slot0 - p.q_rank * p.m.c) + row
                                  : bh * p.T + it.slot0 + row;
       // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
+      // (the TMEM loads are warp-collective: only the global stores are guarded)
+      const bool store = in_bounds(orow, 1, o_rows, p.status);
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         const int col = half * (D / 2) + c * 32;
@@ -591,12 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           v[j] = a0 * __uint_as_float(o0[j]) + a1 * __uint_as_float(o1[j]);
-        if (OUT_F32) {
+        if (store && OUT_F32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + col);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        } else {
+        } else if (store) {
           uint4* dst =
               reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
 #pragma unroll
@@ -606,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pack_bf16(v[8 * j + 6], v[8 * j + 7]));
         }
       }
-      if (half == 0) p.lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * kLn2 : -INFINITY;
+      if (half == 0 && store) p.lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * kLn2 : -INFINITY;
       // O has been read: the next item's first PV may overwrite it
       tc_fence_before();
       mbar_arrive(o_free);

@@ -45,8 +45,9 @@
  * Errors: invalid arguments are reported synchronously, before anything is
  * enqueued (CPATTN_ERR_INVALID_ARG; CPATTN_ERR_UNSUPPORTED for shapes outside the
  * implemented set).  Launch failures return CPATTN_ERR_CUDA.  Errors detected on
- * the device (a bounded wait that ran out) are latched in a per-device status
- * word and reported by cpattn_check.
+ * the device (a bounded wait that ran out; in a CPATTN_DEBUG build also a failed
+ * bounds check) are latched in a per-device status word and reported by
+ * cpattn_check.
  */
 #ifndef CPATTN_H
 #define CPATTN_H
@@ -63,7 +64,10 @@ typedef enum cpattn_status {
   CPATTN_ERR_INVALID_ARG = 1,
   CPATTN_ERR_UNSUPPORTED = 2,
   CPATTN_ERR_CUDA = 3,
-  CPATTN_ERR_TIMEOUT = 4
+  CPATTN_ERR_TIMEOUT = 4,
+  CPATTN_ERR_BOUNDS = 5  /* only from a library built with CPATTN_DEBUG: a kernel's
+                            bounds check on a computed tensor row failed, and the
+                            access was skipped */
 } cpattn_status;
 
 typedef enum cpattn_dtype { CPATTN_F32 = 0, CPATTN_BF16 = 1 } cpattn_dtype;
@@ -90,9 +94,12 @@ typedef struct cpattn_desc {
   int32_t dtype;       /* cpattn_dtype */
   float scale;         /* softmax scale, > 0 (1/sqrt(D) for standard attention) */
   int32_t causal;      /* must be 1: the pages define causal self-attention only */
-  int32_t debug_fault; /* 0.  Test hook: 1 makes the tensor-core forward withhold one
-                          load so that its bounded wait runs out (CPATTN_ERR_TIMEOUT
-                          via cpattn_check, within about 50 ms). */
+  int32_t debug_fault; /* 0.  Test hook of the bounded waits: 1 makes the tensor-core
+                          forward, 2 the backward's dK/dV kernel and 3 its dQ kernel
+                          withhold one load, so that the waits on it run out
+                          (CPATTN_ERR_TIMEOUT via cpattn_check, within about 50 ms;
+                          any non-zero value shortens every bounded wait of the
+                          tensor-core kernels to 50 ms). */
 } cpattn_desc;
 
 /*
@@ -171,6 +178,9 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
  *   Sharing: every call on a device uses the same scratch, which keeps the last
  *   call's contents (nothing needs clearing: each call writes what it reads).
  *   Two calls that overlap on the GPU race on it; order them on one stream.
+ *   Device reset: the scratch's address is cached per device for the life of
+ *   the process; after cudaDeviceReset it is stale, so do not call this entry
+ *   point again in a process that has reset the device.
  * Other errors as cpattn_ring_bwd.
  */
 cpattn_status cpattn_ring_bwd_noalloc(const cpattn_desc* desc, const void* q, const void* k,
@@ -275,8 +285,10 @@ cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* sr
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the
- * current device.  Returns CPATTN_ERR_TIMEOUT if a kernel's bounded wait ran out
- * since the last check, CPATTN_ERR_CUDA on a CUDA error, else CPATTN_OK.
+ * current device.  Returns the first device error since the last check
+ * (CPATTN_ERR_TIMEOUT: a kernel's bounded wait ran out; CPATTN_ERR_BOUNDS: a
+ * bounds check of a CPATTN_DEBUG build failed), CPATTN_ERR_CUDA on a CUDA error,
+ * else CPATTN_OK.
  */
 cpattn_status cpattn_check(void* stream);
 
