@@ -68,6 +68,16 @@ cudaError_t launch_simt_allgather_bwd(const Ring& R, int q_rank, const void* q, 
                                       const void* dO, void* dq, float* dk_sum, float* dv_sum,
                                       int accumulate, cudaStream_t st);
 
+// One ring step of the backward: rank q_rank's rows (lse/delta/dO hold its c rows
+// per (b, h)) against the keys of chunk kv_rank; float32 contributions to the
+// rank's dQ rows (dq_part, c rows per (b, h)) and to the chunk's dK/dV rows
+// (dk_part/dv_part, c rows per (b, g)), overwritten or added when `accumulate`.
+cudaError_t launch_simt_partial_bwd(const Ring& R, int q_rank, int kv_rank, const void* q,
+                                    const void* k, const void* v, const float* lse,
+                                    const float* delta, const void* dO, float* dq_part,
+                                    float* dk_part, float* dv_part, int accumulate,
+                                    cudaStream_t st);
+
 // ---- tc_fwd.cu / tc_bwd.cu (bf16 tcgen05 path, D in {64, 128}) --------------
 bool tc_supported(const Ring& R);
 // doc_lo (packed sequences, ring mode only): per batch row and natural position
@@ -88,6 +98,14 @@ cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, co
                                     const void* v, const float* lse2, const float* delta,
                                     const void* dO, void* dq, float* dk_sum, float* dv_sum,
                                     int accumulate, int* status, cudaStream_t st);
+
+// One ring step of the backward (see launch_simt_partial_bwd); lse2 / delta are the
+// pre-pass statistics of the rank's rows.
+cudaError_t launch_tc_partial_bwd(const Ring& R, int q_rank, int kv_rank, const void* q,
+                                  const void* k, const void* v, const float* lse2,
+                                  const float* delta, const void* dO, float* dq_part,
+                                  float* dk_part, float* dv_part, int accumulate, int* status,
+                                  cudaStream_t st);
 
 // The register split of the tensor-core kernels (3 warpgroups: one control, two
 // math) must fit in what a launch of `kern` allocates; a split that does not fit

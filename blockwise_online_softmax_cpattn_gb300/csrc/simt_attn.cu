@@ -135,19 +135,23 @@ struct SimtBwd {
   // what they hold when `accumulate` is set.
   int ag_rank;
   int accumulate;
+  // One ring step (kv_rank >= 0, with ag_rank the query rank): only the keys of
+  // chunk kv_rank take part; dQ is float32 and dK/dV hold the chunk's c rows per
+  // (b, g), all overwritten or added to like dK/dV above.
+  int kv_rank;
   // packed sequences: first / last position of each position's document, [B][T]
   const int* doc_lo;
   const int* doc_hi;
 };
 
-template <typename T>
+template <typename T, typename TO>
 __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(SimtBwd p, const T* __restrict__ q,
                                                           const T* __restrict__ k,
                                                           const T* __restrict__ v,
                                                           const float* __restrict__ lse,
                                                           const float* __restrict__ delta,
                                                           const T* __restrict__ dO,
-                                                          T* __restrict__ dq) {
+                                                          TO* __restrict__ dq) {
   const int lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   // w indexes the rows of dO / lse / Delta / dQ: all T slots, or the rank's c
@@ -166,8 +170,9 @@ __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(SimtBwd p, const T* __
   const T* kb = k + ((int64_t)b * p.Hkv + g) * p.T * D;
   const T* vb = v + ((int64_t)b * p.Hkv + g) * p.T * D;
   const int lo_q = p.doc_lo ? p.doc_lo[(int64_t)b * p.T + qpos] : 0;
-  for (int i = 0; i < p.m.cp; ++i) {
-    const int s = (r - i + p.m.cp) % p.m.cp;
+  const bool step = p.kv_rank >= 0;
+  for (int i = 0; i < (step ? 1 : p.m.cp); ++i) {
+    const int s = step ? p.kv_rank : (r - i + p.m.cp) % p.m.cp;
     for (int t = s * p.m.c; t < (s + 1) * p.m.c; ++t) {
       const int kp = p.m.pos(t);
       if (kp > qpos || kp < lo_q) continue;
@@ -183,7 +188,11 @@ __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(SimtBwd p, const T* __
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     int d = lane + 32 * j;
-    if (d < D) dq[w * D + d] = from_f<T>(acc[j] * p.scale);
+    if (d < D) {
+      float x = acc[j] * p.scale;
+      if (step && p.accumulate) x += to_f(dq[w * D + d]);
+      dq[w * D + d] = from_f<TO>(x);
+    }
   }
 }
 
@@ -197,14 +206,17 @@ __global__ void __launch_bounds__(256) simt_bwd_dkdv_kernel(
     TO* __restrict__ dk, TO* __restrict__ dv) {
   const int lane = threadIdx.x & 31;
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (w >= (int64_t)p.B * p.Hkv * p.T) return;
-  const int64_t bg = w / p.T;
-  const int slot = (int)(w - bg * p.T);
+  // w indexes the rows of dK / dV: all T slots, or (one ring step) chunk kv_rank's c
+  const bool step = p.kv_rank >= 0;
+  const int n_slots = step ? p.m.c : p.T;
+  if (w >= (int64_t)p.B * p.Hkv * n_slots) return;
+  const int64_t bg = w / n_slots;
+  const int slot = (int)(w - bg * n_slots) + (step ? p.kv_rank * p.m.c : 0);
   const int b = (int)(bg / p.Hkv), g = (int)(bg % p.Hkv);
   const int D = p.D;
   float kv_[4], vv[4], ak[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
-  load_row(k + w * D, D, lane, kv_);
-  load_row(v + w * D, D, lane, vv);
+  load_row(k + (bg * p.T + slot) * D, D, lane, kv_);
+  load_row(v + (bg * p.T + slot) * D, D, lane, vv);
   const int kpos = p.m.pos(slot);
   const int s = slot / p.m.c;
   const int hi_k = p.doc_hi ? p.doc_hi[(int64_t)b * p.T + kpos] : p.T;
@@ -304,6 +316,7 @@ static SimtBwd make_bwd(const Ring& R) {
   p.scale = R.scale;
   p.ag_rank = -1;
   p.accumulate = 0;
+  p.kv_rank = -1;
   p.doc_lo = nullptr;
   p.doc_hi = nullptr;
   return p;
@@ -317,11 +330,11 @@ cudaError_t launch_simt_bwd_dq(const Ring& R, const void* q, const void* k, cons
   const int64_t warps = (int64_t)p.B * p.Hq * p.T;
   timing_begin("simt_bwd_dq", st);
   if (R.bf16)
-    simt_bwd_dq_kernel<__nv_bfloat16><<<blocks_for(warps), 256, 0, st>>>(
+    simt_bwd_dq_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks_for(warps), 256, 0, st>>>(
         p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
         (const __nv_bfloat16*)dO, (__nv_bfloat16*)dq);
   else
-    simt_bwd_dq_kernel<float><<<blocks_for(warps), 256, 0, st>>>(
+    simt_bwd_dq_kernel<float, float><<<blocks_for(warps), 256, 0, st>>>(
         p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
         (float*)dq);
   cudaError_t e = cudaGetLastError();
@@ -360,19 +373,53 @@ cudaError_t launch_simt_allgather_bwd(const Ring& R, int q_rank, const void* q, 
   const int64_t kv_warps = (int64_t)p.B * p.Hkv * p.T;
   timing_begin("simt_allgather_bwd", st);
   if (R.bf16) {
-    simt_bwd_dq_kernel<__nv_bfloat16><<<blocks_for(q_warps), 256, 0, st>>>(
+    simt_bwd_dq_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks_for(q_warps), 256, 0, st>>>(
         p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
         (const __nv_bfloat16*)dO, (__nv_bfloat16*)dq);
     simt_bwd_dkdv_kernel<__nv_bfloat16, float><<<blocks_for(kv_warps), 256, 0, st>>>(
         p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
         (const __nv_bfloat16*)dO, dk_sum, dv_sum);
   } else {
-    simt_bwd_dq_kernel<float><<<blocks_for(q_warps), 256, 0, st>>>(
+    simt_bwd_dq_kernel<float, float><<<blocks_for(q_warps), 256, 0, st>>>(
         p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
         (float*)dq);
     simt_bwd_dkdv_kernel<float, float><<<blocks_for(kv_warps), 256, 0, st>>>(
         p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
         dk_sum, dv_sum);
+  }
+  cudaError_t e = cudaGetLastError();
+  timing_end(st);
+  return e;
+}
+
+// One ring step of the backward: rank q_rank's queries against chunk kv_rank's
+// keys; float32 contributions to the rank's dQ rows and to the chunk's dK/dV rows.
+cudaError_t launch_simt_partial_bwd(const Ring& R, int q_rank, int kv_rank, const void* q,
+                                    const void* k, const void* v, const float* lse,
+                                    const float* delta, const void* dO, float* dq_part,
+                                    float* dk_part, float* dv_part, int accumulate,
+                                    cudaStream_t st) {
+  SimtBwd p = make_bwd(R);
+  p.ag_rank = q_rank;
+  p.kv_rank = kv_rank;
+  p.accumulate = accumulate ? 1 : 0;
+  const int64_t warps = (int64_t)p.B * p.Hq * p.m.c;
+  const int64_t kv_warps = (int64_t)p.B * p.Hkv * p.m.c;
+  timing_begin("simt_partial_bwd", st);
+  if (R.bf16) {
+    simt_bwd_dq_kernel<__nv_bfloat16, float><<<blocks_for(warps), 256, 0, st>>>(
+        p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
+        (const __nv_bfloat16*)dO, dq_part);
+    simt_bwd_dkdv_kernel<__nv_bfloat16, float><<<blocks_for(kv_warps), 256, 0, st>>>(
+        p, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, lse, delta,
+        (const __nv_bfloat16*)dO, dk_part, dv_part);
+  } else {
+    simt_bwd_dq_kernel<float, float><<<blocks_for(warps), 256, 0, st>>>(
+        p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
+        dq_part);
+    simt_bwd_dkdv_kernel<float, float><<<blocks_for(kv_warps), 256, 0, st>>>(
+        p, (const float*)q, (const float*)k, (const float*)v, lse, delta, (const float*)dO,
+        dk_part, dv_part);
   }
   cudaError_t e = cudaGetLastError();
   timing_end(st);

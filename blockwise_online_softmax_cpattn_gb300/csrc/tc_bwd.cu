@@ -64,6 +64,10 @@ struct Params {
   // hold when `accumulate` is set.
   int ag_rank;
   int accumulate;
+  // One ring step (kv_chunk >= 0, with ag_rank the query rank): only the K/V tiles
+  // of chunk kv_chunk take part.  dK/dV hold that chunk's c rows per (b, g), and dQ
+  // is float32 (the rank's rows), overwritten or added to like dK/dV.
+  int kv_chunk;
   // packed sequences (ring mode): first / last natural position of each position's
   // document per batch row, [B][T]; nullptr for plain causal attention
   const int* doc_lo;
@@ -226,8 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     b = rem / p.Hkv;
     g = rem - (rem / p.Hkv) * p.Hkv;
   }
-  const int kpos0 = ti * kTile;
-  const int kslot0 = p.m.slot(kpos0);
+  // one ring step: tile ti of chunk kv_chunk in slot order (its earliest positions
+  // first); otherwise the tile at natural position ti * 128
+  const bool step = AG && p.kv_chunk >= 0;
+  const int kslot0 = step ? p.kv_chunk * p.m.c + ti * kTile : p.m.slot(ti * kTile);
+  const int kpos0 = step ? p.m.pos(kslot0) : ti * kTile;
   const int s_own = kslot0 / p.m.c;
   // query tiles in the order the chunk's gradient travels the ring back to its
   // owner: ranks s, s+1, ..., s-1; every query head of the group per rank; tiles
@@ -554,8 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && cnt > 0) ok = warp_wait(final_bar, 0, abort, p.status, tmo);
     // (the TMEM loads below are warp-collective: only the global stores are guarded)
-    const int64_t orow = ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
-    const bool store = in_bounds(orow, 1, kv_rows, p.status);
+    // one ring step: the chunk's own c rows per (b, g)
+    const int64_t orow = step ? ((int64_t)b * p.Hkv + g) * p.m.c + (kslot0 - p.kv_chunk * p.m.c) + row
+                              : ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
+    const bool store = in_bounds(orow, 1, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status);
     if (ok && AG) {
       // all-gather: float32 share of this rank's queries, added to the sum so far
       tc_fence_after();
@@ -767,7 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (PK) {
       w.start(p.m, doc_row(it)[it.qpos0] >> 7, it.qpos0 >> 7, 1);
     } else {
-      w.start(p.m, it.r_own, p.m.cp, -1, 1);
+      // ring order from the rank's own chunk, or the one chunk of a ring step
+      if (p.kv_chunk >= 0) w.start(p.m, p.kv_chunk, 1, -1, 1);
+      else w.start(p.m, it.r_own, p.m.cp, -1, 1);
       while (!w.done() && classify(it.qpos0, w.pos(), nullptr) == kEmpty) w.next();
     }
   };
@@ -1026,8 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           !(ok = warp_wait(dq_done((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.status, tmo)))
         break;
       tc_fence_after();
-      __nv_bfloat16* dq =
-          static_cast<__nv_bfloat16*>(p.out0) + (it.srow + row) * D + half * (D / 2);
+      const int64_t dq_off = (it.srow + row) * D + half * (D / 2);
       // (the TMEM loads are warp-collective: only the global stores are guarded)
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
@@ -1039,7 +1049,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) v32[jj] = 0u;
         }
-        if (row_ok) store_row32_bf16(dq + c * 32, v32, p.scale);
+        if (!row_ok) continue;
+        if (p.kv_chunk >= 0) {
+          // one ring step: the float32 contribution, overwritten or added
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + dq_off + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4 x = make_float4(__uint_as_float(v32[4 * j]) * p.scale,
+                                   __uint_as_float(v32[4 * j + 1]) * p.scale,
+                                   __uint_as_float(v32[4 * j + 2]) * p.scale,
+                                   __uint_as_float(v32[4 * j + 3]) * p.scale);
+            if (p.accumulate) {
+              const float4 y = dst[j];
+              x.x += y.x;
+              x.y += y.y;
+              x.z += y.z;
+              x.w += y.w;
+            }
+            dst[j] = x;
+          }
+        } else {
+          store_row32_bf16(static_cast<__nv_bfloat16*>(p.out0) + dq_off + c * 32, v32, p.scale);
+        }
       }
       // the accumulator has been read: the next item's first dQ may overwrite it
       tc_fence_before();
@@ -1083,8 +1114,13 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
                   : (packed ? dkdv_kernel<D, false, true> : dkdv_kernel<D, false, false>);
   cudaError_t e = prep(kdkdv, DkdvSmem<D>::kBytes);
   if (e != cudaSuccess) return e;
-  const int kv_items = R.B * R.Hkv * (R.T / kTile);
-  timing_begin(ag ? "tc_allgather_dkdv" : packed ? "tc_packed_dkdv" : "tc_bwd_dkdv", st);
+  const bool step = ag && base.kv_chunk >= 0;  // one ring step: the chunk's K/V tiles only
+  const int kv_items = R.B * R.Hkv * ((step ? R.T / R.cp : R.T) / kTile);
+  timing_begin(step     ? "tc_partial_dkdv"
+               : ag     ? "tc_allgather_dkdv"
+               : packed ? "tc_packed_dkdv"
+                        : "tc_bwd_dkdv",
+               st);
   kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pk);
   e = cudaGetLastError();
   timing_end(st);
@@ -1101,7 +1137,11 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  timing_begin(ag ? "tc_allgather_dq" : packed ? "tc_packed_dq" : "tc_bwd_dq", st);
+  timing_begin(step     ? "tc_partial_dq"
+               : ag     ? "tc_allgather_dq"
+               : packed ? "tc_packed_dq"
+                        : "tc_bwd_dq",
+               st);
   kdq<<<q_items < sms ? q_items : sms, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
   e = cudaGetLastError();
   timing_end(st);
@@ -1126,6 +1166,7 @@ static tcbwd::Params bwd_params(const Ring& R, const float* lse2, const float* d
   p.status = status;
   p.ag_rank = -1;
   p.accumulate = 0;
+  p.kv_chunk = -1;
   p.doc_lo = nullptr;
   p.doc_hi = nullptr;
   p.ord_q = nullptr;
@@ -1145,6 +1186,19 @@ cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const voi
   p.ord_k = ord_k;
   if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st);
   return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st);
+}
+
+cudaError_t launch_tc_partial_bwd(const Ring& R, int q_rank, int kv_rank, const void* q,
+                                  const void* k, const void* v, const float* lse2,
+                                  const float* delta, const void* dO, float* dq_part,
+                                  float* dk_part, float* dv_part, int accumulate, int* status,
+                                  cudaStream_t st) {
+  tcbwd::Params p = bwd_params(R, lse2, delta, status);
+  p.ag_rank = q_rank;
+  p.kv_chunk = kv_rank;
+  p.accumulate = accumulate ? 1 : 0;
+  if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq_part, dk_part, dv_part, st);
+  return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq_part, dk_part, dv_part, st);
 }
 
 cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,

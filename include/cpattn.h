@@ -118,6 +118,43 @@ cpattn_status cpattn_partial_fwd(const cpattn_desc* desc, int q_rank, int kv_ran
                                  const void* q, const void* k, const void* v,
                                  float* o_part, float* lse_part, void* stream);
 
+/* Bytes of device workspace cpattn_partial_bwd needs (float32 row statistics of
+ * one rank's rows). */
+size_t cpattn_partial_bwd_workspace(const cpattn_desc* desc);
+
+/*
+ * One ring step of the backward pass (tutorial "上下文并行", section "朴素 Ring
+ * Attention": at step i rank r holds the K/V chunk of rank s = (r - i) mod cp and
+ * recomputes that step's probabilities from the saved statistics; pull request
+ * #181, mode table row "p2p": each chunk's K/V gradient travels the ring with the
+ * chunk and arrives back at its owner).  The gradient contributions of rank
+ * q_rank's queries against the K/V chunk of rank kv_rank:
+ *   q, k, v     : full layout-order tensors (as cpattn_partial_fwd: only q_rank's
+ *                 query slots and kv_rank's key slots are read)
+ *   o, lse, dO  : rank q_rank's rows of the forward's output, of its LSE (the whole
+ *                 forward's, every step merged) and of the upstream gradient:
+ *                 [B', H_q', c, D] dtype, [B', H_q', c] float32, [B', H_q', c, D]
+ *   dq_part     : [B', H_q', c, D] float32, the step's dQ contribution to the
+ *                 rank's rows
+ *   dk_part, dv_part : [B', H_kv', c, D] float32, the step's dK / dV contribution
+ *                 to chunk kv_rank's rows (slot order within the chunk)
+ *   accumulate  : 0 overwrites dq_part, dk_part and dv_part; 1 adds to them
+ *   workspace   : at least cpattn_partial_bwd_workspace(desc) bytes (smaller ->
+ *                 CPATTN_ERR_INVALID_ARG); contents on entry do not matter
+ * Summed over the steps -- dq_part of rank r over every kv_rank, dk_part/dv_part
+ * of chunk s over every q_rank -- the contributions give cpattn_ring_bwd's dq
+ * (rank r's rows) and dk/dv (chunk s's rows), in float32.  A pair with no
+ * visible (query, key) pair contributes zeros.  (B', H_q', H_kv' = H_kv/a2a, c
+ * as for cpattn_partial_fwd.)
+ * Errors: a rank outside [0, cp/a2a) or accumulate not 0/1 ->
+ * CPATTN_ERR_INVALID_ARG; others as cpattn_ring_bwd.
+ */
+cpattn_status cpattn_partial_bwd(const cpattn_desc* desc, int q_rank, int kv_rank,
+                                 const void* q, const void* k, const void* v, const void* o,
+                                 const float* lse, const void* dO, float* dq_part,
+                                 float* dk_part, float* dv_part, int accumulate,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
 /*
  * Online-softmax merge of two partial results over disjoint key sets (tutorial,
  * section "朴素 Ring Attention": the block order does not matter as long as the

@@ -135,6 +135,33 @@ def partial_attention(q_rows, k_rows, v_rows, q_pos, k_pos, scale):
     return o, lse
 
 
+def partial_attention_bwd(q_rows, k_rows, v_rows, do_rows, o_rows, lse_rows, q_pos, k_pos,
+                          scale):
+    """One ring step's gradient contributions: a set of query rows against one set
+    of key/value rows.
+
+    The backward of the tutorial's section "朴素 Ring Attention" recomputes each
+    step's probabilities; the pull request's "p2p" mode sends each K/V chunk's
+    gradient around the ring with the chunk.  Per step that is the analytic
+    softmax backward restricted to the keys held at the step, with the WHOLE
+    forward's statistics: P_ij = exp(S_ij - LSE_i) for visible pairs (global
+    positions) and 0 otherwise, Delta_i = dO_i . O_i with the whole forward's
+    output, dP_ij = dO_i . v_j, dS_ij = P_ij (dP_ij - Delta_i).
+    q_rows, do_rows, o_rows [n, D], lse_rows [n], k_rows, v_rows [m, D].
+    Returns (dq [n, D], dk [m, D], dv [m, D]): the block's contribution to the
+    rows' dQ, and the rows' contribution to the keys' dK and dV.  Over a
+    partition of the keys the dq contributions add up to the rows' dQ; over a
+    partition of the queries the dk, dv contributions add up to the keys' dK, dV.
+    """
+    S = scores(q_rows, k_rows, scale)
+    vis = causal_visible(q_pos, k_pos)
+    P = np.where(vis, np.exp(np.where(vis, S, 0.0) - np.asarray(lse_rows)[:, None]), 0.0)
+    delta = np.sum(do_rows * o_rows, axis=1)
+    dP = do_rows @ v_rows.T
+    dS = P * (dP - delta[:, None])
+    return scale * (dS @ k_rows), scale * (dS.T @ q_rows), P.T @ do_rows
+
+
 def merge(o_a, lse_a, o_b, lse_b):
     """Merge two normalised partial results over disjoint key sets.
 

@@ -71,7 +71,10 @@ def test_ring_and_partial_stay_in_bounds(w):
          "dk": guarded_like(k), "dv": guarded_like(v),
          "ws": Guarded((cp.cpattn_ring_bwd_workspace(d),), torch.uint8),
          "o_part": Guarded((B, H, c, D), f32), "lse_part": Guarded((B, H, c), f32),
-         "o_m": Guarded((B, H, c, D), f32), "lse_m": Guarded((B, H, c), f32)}
+         "o_m": Guarded((B, H, c, D), f32), "lse_m": Guarded((B, H, c), f32),
+         "dq_part": Guarded((B, H, c, D), f32), "dk_part": Guarded((B, w.H_kv, c, D), f32),
+         "dv_part": Guarded((B, w.H_kv, c, D), f32),
+         "ws_part": Guarded((cp.cpattn_partial_bwd_workspace(d),), torch.uint8)}
     cp.check(cp.cpattn_ring_fwd(d, q, k, v, b["o"].t, b["lse"].t))
     cp.check(cp.cpattn_ring_bwd(d, q, k, v, b["o"].t, b["lse"].t, do, b["dq"].t, b["dk"].t,
                                 b["dv"].t, b["ws"].t))
@@ -80,8 +83,14 @@ def test_ring_and_partial_stay_in_bounds(w):
     # the merge of the diagonal step with itself (out of place): lse + ln 2, same o
     cp.check(cp.cpattn_merge(B * H * c, D, b["o_part"].t, b["lse_part"].t, b["o_part"].t,
                              b["lse_part"].t, b["o_m"].t, b["lse_m"].t))
+    # one backward ring step: the last rank's rows against chunk 0
+    sl = slice(r * c, (r + 1) * c)
+    o_r, lse_r, do_r = (x[:, :, sl].contiguous() for x in (b["o"].t, b["lse"].t, do))
+    cp.check(cp.cpattn_partial_bwd(d, r, 0, q, k, v, o_r, lse_r, do_r, b["dq_part"].t,
+                                   b["dk_part"].t, b["dv_part"].t, 0, b["ws_part"].t))
     cp.check(cp.cpattn_check())
-    check_all(b, written=("o", "lse", "dq", "dk", "dv", "o_part", "lse_part", "o_m", "lse_m"))
+    check_all(b, written=("o", "lse", "dq", "dk", "dv", "o_part", "lse_part", "o_m", "lse_m",
+                          "dq_part", "dk_part", "dv_part"))
 
 
 @pytest.mark.parametrize("w", [RING[0], RING[2]], ids=lambda w: w.name)

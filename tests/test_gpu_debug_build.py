@@ -17,8 +17,9 @@ from conftest import ROOT
 
 pytestmark = pytest.mark.gpu
 
-SUITES = ["tests/test_gpu_ring.py", "tests/test_gpu_partial.py", "tests/test_gpu_allgather.py",
-          "tests/test_gpu_packed.py", "tests/test_gpu_canary.py", "tests/test_gpu_ulysses.py"]
+SUITES = ["tests/test_gpu_ring.py", "tests/test_gpu_partial.py", "tests/test_gpu_partial_bwd.py",
+          "tests/test_gpu_allgather.py", "tests/test_gpu_packed.py", "tests/test_gpu_canary.py",
+          "tests/test_gpu_ulysses.py"]
 
 
 def test_parity_suites_pass_under_bounds_checks():

@@ -233,6 +233,57 @@ def test_ring_merge_equals_full_attention_any_order(rng, layout, cp, T):
                 assert np.max(np.abs(acc_l - lse_full[0, h, qs])) < 1e-12
 
 
+@pytest.mark.parametrize("layout,cp,T", [("zigzag", 4, 48), ("contiguous", 3, 45),
+                                         ("zigzag", 2, 20), ("contiguous", 4, 64)])
+def test_partial_backward_steps_sum_to_the_full_backward(rng, layout, cp, T):
+    """The per-step contributions of the ring backward (whole-forward statistics,
+    one K/V chunk at a time): over the chunks a rank's queries meet they add up to
+    the rank's dQ, and over the ranks a chunk meets (and the query heads of its
+    group) to the chunk's dK and dV -- the backward pinned above."""
+    q, k, v, do = _rand(rng, 1, 4, 2, T, 6)
+    scale = 0.4
+    o, lse = A.attention_fwd(q, k, v, scale)
+    dq, dk, dv = A.attention_bwd(q, k, v, do, scale)
+    c = T // cp
+    pos = L.positions(T, cp, layout)
+    gq, gk, gv = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv)
+    for h in range(4):
+        g = h // 2
+        for r in range(cp):
+            qs = pos[r * c:(r + 1) * c]
+            for i in range(cp):
+                s = L.ring_source(r, i, cp)
+                ks = pos[s * c:(s + 1) * c]
+                a, b, e = A.partial_attention_bwd(q[0, h, qs], k[0, g, ks], v[0, g, ks],
+                                                  do[0, h, qs], o[0, h, qs], lse[0, h, qs], qs,
+                                                  ks, scale)
+                gq[0, h, qs] += a
+                gk[0, g, ks] += b
+                gv[0, g, ks] += e
+    assert rel_err(gq, dq) < 1e-12 and rel_err(gk, dk) < 1e-12 and rel_err(gv, dv) < 1e-12
+
+
+def test_partial_backward_of_one_chunk_is_the_backward(rng):
+    """With a single chunk (cp = 1) the step is the whole backward of the head."""
+    q, k, v, do = _rand(rng, 1, 1, 1, 30, 5)
+    o, lse = A.attention_fwd(q, k, v, 0.5)
+    dq, dk, dv = A.attention_bwd(q, k, v, do, 0.5)
+    pos = np.arange(30)
+    a, b, e = A.partial_attention_bwd(q[0, 0], k[0, 0], v[0, 0], do[0, 0], o[0, 0], lse[0, 0],
+                                      pos, pos, 0.5)
+    assert rel_err(a, dq[0, 0]) < 1e-13 and rel_err(b, dk[0, 0]) < 1e-13
+    assert rel_err(e, dv[0, 0]) < 1e-13
+
+
+def test_partial_backward_of_a_hidden_chunk_is_zero(rng):
+    """Queries that see none of the chunk's keys contribute nothing."""
+    q, k, v, do = _rand(rng, 1, 1, 1, 8, 3)
+    o = rng.standard_normal((8, 3))
+    a, b, e = A.partial_attention_bwd(q[0, 0], k[0, 0], v[0, 0], do[0, 0], o, np.zeros(8),
+                                      np.arange(8), np.arange(8, 16), 1.0)
+    assert not a.any() and not b.any() and not e.any()
+
+
 def test_empty_partial_is_merge_identity(rng):
     """A query set that sees none of the keys yields (0, -inf)."""
     q = rng.standard_normal((4, 3)); k = rng.standard_normal((5, 3)); v = rng.standard_normal((5, 3))
