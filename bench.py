@@ -17,6 +17,11 @@ host cores, each step a bounded sample of the same workload.
 documents of seeded random lengths (causal attention inside each document); the
 FLOPs count the pairs the packed mask attends.
 
+--mode hbm times the HBM-bound kernels alone, one launch at a time with L2 flushed
+before each: the (O, LSE) merge at the LLaMA and Qwen3 ring-step sizes, the a2a
+head<->sequence re-layout at the Qwen3 size, and the zigzag chunk copies at the
+LLaMA size; GB/s of algorithmic bytes against the measured copy bandwidth.
+
 --mode allgather times the all-gather mode instead (pull request #181, mode table
 row "all_gather"): one step = cpattn_allgather_fwd and cpattn_allgather_bwd for
 every emulated rank, with the layout-order q, k, v and each rank's dO rows already
@@ -63,7 +68,7 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="ring", choices=["ring", "allgather"])
+    ap.add_argument("--mode", default="ring", choices=["ring", "allgather", "hbm"])
     ap.add_argument("--packed-docs", type=int, default=0,
                     help="ring mode over packed sequences: this many documents per row, "
                          "seeded random lengths (0: one sequence per row)")
@@ -704,6 +709,85 @@ def run_allgather(args, rank, world):
             "clocks": clocks, "e2e": e2e, "kernels": kernels}
 
 
+def run_hbm(args):
+    """The HBM-bound kernels alone: each launch timed with CUDA events on its stream,
+    L2 flushed (256 MiB write) before every launch, outside the events."""
+    import torch
+    import blockwise_online_softmax_cpattn_gb300 as cp
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    pk, src_pk = peaks()
+    reps = max(5, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        cp.check(cp.cpattn_check())
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    out = {}
+
+    def record(name, nbytes, ms, what):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"bytes": nbytes, "ms": ms, "gbs": gbs, "frac": gbs / pk["hbm_gbs"],
+                     "what": what}
+
+    # (O, LSE) merge of one ring step's partials: B * H_q * c rows of D floats
+    for label, w in (("llama", W.LLAMA), ("qwen3", W.QWEN3)):
+        rows = w.B * w.a2a * (w.H_q // w.a2a) * (w.T // (w.cp // w.a2a))
+        o_a, o_b = (torch.randn(rows, w.D, generator=g).to(dev) for _ in range(2))
+        l_a, l_b = (torch.randn(rows, generator=g).to(dev) for _ in range(2))
+        o_o, l_o = torch.empty_like(o_a), torch.empty_like(l_a)
+        ms = timed(lambda: cp.check(cp.cpattn_merge(rows, w.D, o_a, l_a, o_b, l_b, o_o, l_o)))
+        record(f"merge_{label}", rows * (3 * 4 * w.D + 12), ms,
+               f"cpattn_merge, {rows} rows x D {w.D} (one ring step of {w.name}): "
+               "two (O, LSE) read, one written, float32")
+        del o_a, o_b, o_o
+    # a2a re-layout of the Qwen3 workload (a2a 2 x p2p 4): q-sized and k-sized
+    w = W.QWEN3
+    d = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, w.D, w.cp, w.layout, w.dtype, a2a=w.a2a)
+    for h, tag in ((w.H_q, "q"), (w.H_kv, "kv")):
+        x = torch.randn(w.B * w.T * h * w.D, generator=g).to(torch.bfloat16).to(dev)
+        y = torch.empty_like(x)
+        n = x.numel() * 2
+        record(f"a2a_fwd_{tag}", 2 * n,
+               timed(lambda: cp.check(cp.cpattn_layout(cp.A2A_FWD, d, x, y, h))),
+               f"cpattn_layout A2A_FWD of the {tag} tensor of {w.name} ({h} heads, "
+               f"{n / 1e6:.1f} MB): one read, one write")
+        record(f"a2a_inv_{tag}", 2 * n,
+               timed(lambda: cp.check(cp.cpattn_layout(cp.A2A_INV, d, y, x, h))),
+               f"cpattn_layout A2A_INV of the {tag} tensor of {w.name}: one read, one write")
+        del x, y
+    # zigzag chunk copies of the LLaMA workload
+    w = W.LLAMA
+    d = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, w.D, w.cp, w.layout, w.dtype)
+    for h, tag in ((w.H_q, "q"), (w.H_kv, "kv")):
+        x = torch.randn(w.B, h, w.T, w.D, generator=g).to(torch.bfloat16).to(dev)
+        y = torch.empty_like(x)
+        n = x.numel() * 2
+        record(f"zigzag_fwd_{tag}", 2 * n,
+               timed(lambda: cp.check(cp.cpattn_layout(cp.ZIGZAG_FWD, d, x, y, h))),
+               f"cpattn_layout ZIGZAG_FWD of the {tag} tensor of {w.name} ({n / 1e6:.1f} MB)")
+        del x, y
+    return {"metric": "HBM-bound kernels: GB/s of algorithmic bytes per launch", "unit": "GB/s",
+            "n_gpus": 1, "higher_is_better": True, "data": "synthetic",
+            "peak": pk["hbm_gbs"], "peak_source": f"{src_pk} copy bandwidth",
+            "l2": "flushed before every launch (256 MiB device write, outside the events)",
+            "reps": reps, "kernels": out}
+
+
 # ---------------------------------------------------------------------------
 # the oracle (CPU) legs
 # ---------------------------------------------------------------------------
@@ -788,6 +872,10 @@ def main():
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend)
+    if args.mode == "hbm":
+        if rank == 0:
+            print(json.dumps(run_hbm(args)))
+        return
     out = run_allgather(args, rank, world) if args.mode == "allgather" else run_cpattn(args, rank, world)
     if rank == 0:
         w = W.ALL[args.workload]
