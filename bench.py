@@ -2,9 +2,10 @@
 """Benchmark of causal ring attention (forward + backward) on GB300.
 
 One step = the whole hot path over one batch of synthetic input already in HBM:
-  layout permute of q, k, v, dO (natural -> zigzag layout order; the all-to-all
-  re-layout for the hierarchical a2a x p2p workload) -> cpattn_ring_fwd ->
-  cpattn_ring_bwd -> inverse permute of o, dq, dk, dv.
+  layout permute of q, k, v, dO (natural -> zigzag layout order, one
+  cpattn_layout_batch call; the all-to-all re-layout for the hierarchical a2a x p2p
+  workload) -> cpattn_ring_fwd -> cpattn_ring_bwd -> inverse permute of o, dq, dk,
+  dv (one call).
 FLOPs counted: 4*D per attended (q, k) pair forward, 10*D backward (attended
 pairs = B * H_q * T (T + 1) / 2; masked work inside diagonal tiles is not
 counted).  `value` is TFLOP/s over all GPUs; L2 is flushed (256 MiB write)
@@ -200,6 +201,10 @@ def kernel_flops_or_bytes(name, w, pairs=None):
         return "tensor", 2.0 * w.D * pairs / w.cp
     if name == "bwd_prepass":
         return "hbm", 2.0 * rows_q * w.D * elt + 12.0 * rows_q
+    if name == "layout_zigzag_batch":
+        # one launch permutes a step's four inputs (q, k, v, dO) or its four outputs
+        # (o, dk, dv, dq): each read once and written once
+        return "hbm", 2.0 * (2 * rows_q + 2 * rows_kv) * w.D * elt
     if name.startswith("layout"):
         # a step permutes q, k, v, dO and o, dk, dv, dq (each read once and written
         # once): the average launch moves (rows_q + rows_kv) rows each way
@@ -316,13 +321,13 @@ def run_cpattn(args, rank, world):
         return cp.cpattn_ring_bwd(d, q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, ws)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
+    H_out = [w.H_q, w.H_kv, w.H_kv, w.H_q]  # o, dk, dv, dq
+
     def step():
-        for s_, l_, h in zip(src, lay, H):
-            cp.check(cp.cpattn_layout(fwd_perm, desc, s_, l_, h))
+        cp.check(cp.cpattn_layout_batch(fwd_perm, desc, src, lay, H))
         cp.check(ring_fwd(lay[0], lay[1], lay[2], o, lse))
         cp.check(ring_bwd(lay[0], lay[1], lay[2], o, lse, lay[3], dq, dk, dv))
-        for x, y, h in zip((o, dk, dv, dq), outs, (w.H_q, w.H_kv, w.H_kv, w.H_q)):
-            cp.check(cp.cpattn_layout(inv_perm, desc, x, y, h))
+        cp.check(cp.cpattn_layout_batch(inv_perm, desc, [o, dk, dv, dq], outs, H_out))
 
     def barrier():
         if world > 1:
@@ -409,8 +414,7 @@ def run_cpattn(args, rank, world):
             e_do.record(side_in)
         for dst_, hsrc in zip(src[:3], up_host[:3]):
             dst_.copy_(hsrc, non_blocking=True)
-        for s_, l_, h in zip(src[:3], lay[:3], H[:3]):
-            cp.check(cp.cpattn_layout(fwd_perm, desc, s_, l_, h))
+        cp.check(cp.cpattn_layout_batch(fwd_perm, desc, src[:3], lay[:3], H[:3]))
         cp.check(ring_fwd(lay[0], lay[1], lay[2], o, lse))
         cp.check(cp.cpattn_layout(inv_perm, desc, o, outs[0], w.H_q))
         e_o.record(stream)
@@ -420,8 +424,7 @@ def run_cpattn(args, rank, world):
         stream.wait_event(e_do)
         cp.check(cp.cpattn_layout(fwd_perm, desc, src[3], lay[3], H[3]))
         cp.check(ring_bwd(lay[0], lay[1], lay[2], o, lse, lay[3], dq, dk, dv))
-        for x, y, h in zip((dk, dv, dq), outs[1:], (w.H_kv, w.H_kv, w.H_q)):
-            cp.check(cp.cpattn_layout(inv_perm, desc, x, y, h))
+        cp.check(cp.cpattn_layout_batch(inv_perm, desc, [dk, dv, dq], outs[1:], H_out[1:]))
         for hdst, dsrc in zip(host_out[1:], outs[1:]):
             hdst.copy_(dsrc, non_blocking=True)
         stream.wait_stream(side_out)  # o's download is part of the step
@@ -458,8 +461,9 @@ def run_cpattn(args, rank, world):
                 ev_do[c].record(side_in)
         for c in range(n_chunks):
             stream.wait_event(ev_in[c])
-            for s_, l_, h in zip(src[:3], lay[:3], H[:3]):
-                cp.check(cp.cpattn_layout(fwd_perm, d_c, hs(s_, c, h), hs(l_, c, h), h // n_chunks))
+            cp.check(cp.cpattn_layout_batch(
+                fwd_perm, d_c, [hs(s_, c, h) for s_, h in zip(src[:3], H[:3])],
+                [hs(l_, c, h) for l_, h in zip(lay[:3], H[:3])], [h // n_chunks for h in H[:3]]))
             cp.check(ring_fwd(hs(lay[0], c, w.H_q), hs(lay[1], c, w.H_kv), hs(lay[2], c, w.H_kv),
                               hs(o, c, w.H_q), hs(lse, c, w.H_q), d=d_c))
             cp.check(cp.cpattn_layout(inv_perm, d_c, hs(o, c, w.H_q), hs(outs[0], c, w.H_q),
@@ -475,8 +479,10 @@ def run_cpattn(args, rank, world):
             cp.check(ring_bwd(hs(lay[0], c, w.H_q), hs(lay[1], c, w.H_kv), hs(lay[2], c, w.H_kv),
                               hs(o, c, w.H_q), hs(lse, c, w.H_q), hs(lay[3], c, w.H_q),
                               hs(dq, c, w.H_q), hs(dk, c, w.H_kv), hs(dv, c, w.H_kv), d=d_c))
-            for x, y, h in zip((dk, dv, dq), outs[1:], (w.H_kv, w.H_kv, w.H_q)):
-                cp.check(cp.cpattn_layout(inv_perm, d_c, hs(x, c, h), hs(y, c, h), h // n_chunks))
+            cp.check(cp.cpattn_layout_batch(
+                inv_perm, d_c, [hs(x, c, h) for x, h in zip((dk, dv, dq), H_out[1:])],
+                [hs(y, c, h) for y, h in zip(outs[1:], H_out[1:])],
+                [h // n_chunks for h in H_out[1:]]))
             ev_g[c].record(stream)
             side_out.wait_event(ev_g[c])
             with torch.cuda.stream(side_out):

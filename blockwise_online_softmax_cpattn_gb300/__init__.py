@@ -85,6 +85,9 @@ _sigs = {
                                    _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t,
                                    _vp]),
     "cpattn_layout": (_st, [ctypes.c_int, ctypes.POINTER(CpattnDesc), _vp, _vp, ctypes.c_int, _vp]),
+    "cpattn_layout_batch": (_st, [ctypes.c_int, ctypes.POINTER(CpattnDesc), ctypes.c_int,
+                                  ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                  ctypes.POINTER(ctypes.c_int), _vp]),
     "cpattn_check": (_st, [_vp]),
     "cpattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "cpattn_timing_enable": (_st, [ctypes.c_int]),
@@ -218,6 +221,18 @@ def cpattn_allgather_bwd(desc, q_rank, q, k, v, o, lse, dO, dq, dk_sum, dv_sum, 
 def cpattn_layout(permute, desc, src, dst, n_heads, stream=None) -> int:
     return _lib.cpattn_layout(permute, ctypes.byref(desc), _ptr(src), _ptr(dst), n_heads,
                               _stream(stream))
+
+
+def cpattn_layout_batch(permute, desc, srcs, dsts, n_heads, stream=None) -> int:
+    """cpattn_layout over several tensors at once: srcs[i] -> dsts[i], n_heads[i] heads."""
+    n = len(srcs)
+    if len(dsts) != n or len(n_heads) != n:
+        raise ValueError("srcs, dsts and n_heads must have the same length")
+    src_arr = (_vp * n)(*[_ptr(x) for x in srcs])
+    dst_arr = (_vp * n)(*[_ptr(x) for x in dsts])
+    heads = (ctypes.c_int * n)(*[int(h) for h in n_heads])
+    return _lib.cpattn_layout_batch(permute, ctypes.byref(desc), n, src_arr, dst_arr, heads,
+                                    _stream(stream))
 
 
 def cpattn_check(stream=None) -> int:

@@ -446,14 +446,19 @@ cpattn_status cpattn_partial_bwd(const cpattn_desc* desc, int q_rank, int kv_ran
                                            dk_part, dv_part, accumulate, st));
 }
 
-cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* src, void* dst,
-                            int n_heads, void* stream) {
+// Checks of one tensor of a permute; fills the arguments shared by every tensor.
+static cpattn_status permute_args(int permute, const cpattn_desc* desc, const void* src,
+                                  const void* dst, int n_heads, PermuteArgs* out) {
   cpattn_status s = validate(desc, nullptr);
   if (s != CPATTN_OK) return s;
   if (permute < CPATTN_ZIGZAG_FWD || permute > CPATTN_A2A_INV || n_heads <= 0)
     return CPATTN_ERR_INVALID_ARG;
   if (!aligned16(src) || !aligned16(dst) || src == dst) return CPATTN_ERR_INVALID_ARG;
-  PermuteArgs a;
+  if (permute >= CPATTN_A2A_FWD) {
+    if (n_heads % desc->a2a || desc->T % desc->cp) return CPATTN_ERR_INVALID_ARG;
+    if (desc->layout == CPATTN_ZIGZAG && desc->T % (2 * desc->cp)) return CPATTN_ERR_INVALID_ARG;
+  }
+  PermuteArgs& a = *out;
   a.kind = permute;
   a.B = desc->B;
   a.H = n_heads;
@@ -463,12 +468,27 @@ cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* sr
   a.cp = desc->cp;
   a.a2a = desc->a2a;
   a.zz = desc->layout == CPATTN_ZIGZAG;
-  if (permute >= CPATTN_A2A_FWD) {
-    if (n_heads % desc->a2a || desc->T % desc->cp) return CPATTN_ERR_INVALID_ARG;
-    if (a.zz && desc->T % (2 * desc->cp)) return CPATTN_ERR_INVALID_ARG;
-  } else {
-    // zigzag permutes act on [B * n_heads] sequences of T tokens over the ring's ranks
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_layout_batch(int permute, const cpattn_desc* desc, int n,
+                                  const void* const* src, void* const* dst, const int* n_heads,
+                                  void* stream) {
+  if (n < 1 || n > kMaxBatch || !src || !dst || !n_heads) return CPATTN_ERR_INVALID_ARG;
+  PermuteArgs a;
+  for (int i = 0; i < n; ++i) {
+    cpattn_status s = permute_args(permute, desc, src[i], dst[i], n_heads[i], &a);
+    if (s != CPATTN_OK) return s;
   }
+  cudaGetLastError();
+  return from_cuda(launch_permute_batch(a, n, src, dst, n_heads, (cudaStream_t)stream));
+}
+
+cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* src, void* dst,
+                            int n_heads, void* stream) {
+  PermuteArgs a;
+  cpattn_status s = permute_args(permute, desc, src, dst, n_heads, &a);
+  if (s != CPATTN_OK) return s;
   cudaGetLastError();
   return from_cuda(launch_permute(a, src, dst, (cudaStream_t)stream));
 }

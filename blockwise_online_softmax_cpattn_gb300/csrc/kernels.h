@@ -26,6 +26,11 @@ struct PermuteArgs {
   int cp, a2a, zz;         // cp = ranks of the token shards; ring ranks = cp / a2a
 };
 cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cudaStream_t st);
+// n permutes of one kind over tensors of one descriptor, n_heads[i] heads each
+// (a.H is ignored); zigzag permutes of 16-byte rows go out as a single launch.
+constexpr int kMaxBatch = 8;
+cudaError_t launch_permute_batch(const PermuteArgs& a, int n, const void* const* src,
+                                 void* const* dst, const int* n_heads, cudaStream_t st);
 
 // ---- merge.cu --------------------------------------------------------------
 // Packed sequences: from the document starts [B][n_docs + 1] (natural positions,

@@ -129,14 +129,28 @@ static cudaError_t run_rows(const PermuteDev& p, const void* src, void* dst, int
 constexpr int kChunkThreads = 256;
 constexpr int kUnroll = 8;
 
+// The tensors one chunk-copy launch moves: up to kMaxBatch of them, all with the
+// same chunk size; tensor i's chunks are units [first[i], first[i + 1]) of the
+// launch (B * heads sequences of nchunk chunks each).
+struct ChunkBatch {
+  const int4* src[kMaxBatch];
+  int4* dst[kMaxBatch];
+  int64_t first[kMaxBatch + 1];
+  int n;
+};
+
 __global__ void __launch_bounds__(kChunkThreads) chunk_copy_kernel(
-    const int4* __restrict__ src, int4* __restrict__ dst, int64_t chunk_vecs, int nchunk,
-    int cp, int zz, int inverse, int splits) {
+    ChunkBatch jobs, int64_t chunk_vecs, int nchunk, int cp, int zz, int inverse, int splits) {
   const int64_t blk = blockIdx.x;
   const int part = (int)(blk % splits);
-  const int64_t rest = blk / splits;
-  const int k = (int)(rest % nchunk);  // destination chunk
-  const int64_t bh = rest / nchunk;
+  int64_t unit = blk / splits;
+  int ti = 0;  // the tensor this unit belongs to
+  while (ti + 1 < jobs.n && unit >= jobs.first[ti + 1]) ++ti;
+  unit -= jobs.first[ti];
+  const int4* __restrict__ src = jobs.src[ti];
+  int4* __restrict__ dst = jobs.dst[ti];
+  const int k = (int)(unit % nchunk);  // destination chunk
+  const int64_t bh = unit / nchunk;
   int c = k;                            // source chunk
   if (zz) {
     if (!inverse) c = (k & 1) ? 2 * cp - 1 - (k >> 1) : (k >> 1);
@@ -160,24 +174,35 @@ __global__ void __launch_bounds__(kChunkThreads) chunk_copy_kernel(
   }
 }
 
-static cudaError_t run_chunks(const PermuteArgs& a, const void* src, void* dst, int row_bytes,
+// n zigzag permutes of tensors with the same T, D and element size (heads[i] heads
+// each) as one launch of chunk moves.
+static cudaError_t run_chunks(const PermuteArgs& a, int n, const void* const* src,
+                              void* const* dst, const int* heads, int row_bytes,
                               cudaStream_t st) {
   const int cpr = a.cp / a.a2a;  // ranks of the ring the permute serves
   const int nchunk = a.zz ? 2 * cpr : cpr;
   const int64_t chunk_vecs = (int64_t)(a.T / nchunk) * row_bytes / 16;
-  const int64_t seqs = (int64_t)a.B * a.H;
+  ChunkBatch jobs;
+  jobs.n = n;
+  jobs.first[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    jobs.src[i] = static_cast<const int4*>(src[i]);
+    jobs.dst[i] = static_cast<int4*>(dst[i]);
+    jobs.first[i + 1] = jobs.first[i] + (int64_t)a.B * heads[i] * nchunk;
+  }
+  const int64_t units = jobs.first[n];
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // enough blocks to cover every SM several times over
   int splits = 1;
-  while (splits < 64 && seqs * nchunk * splits < 4LL * sms && chunk_vecs % (2 * splits) == 0 &&
+  while (splits < 64 && units * splits < 4LL * sms && chunk_vecs % (2 * splits) == 0 &&
          chunk_vecs / (2 * splits) >= kChunkThreads)
     splits *= 2;
-  const int64_t blocks = seqs * nchunk * splits;
+  const int64_t blocks = units * splits;
   if (blocks <= 0 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   chunk_copy_kernel<<<(unsigned)blocks, kChunkThreads, 0, st>>>(
-      (const int4*)src, (int4*)dst, chunk_vecs, nchunk, cpr, a.zz, a.kind == kZigzagInv, splits);
+      jobs, chunk_vecs, nchunk, cpr, a.zz, a.kind == kZigzagInv, splits);
   return cudaGetLastError();
 }
 
@@ -214,7 +239,7 @@ cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cud
   cudaError_t e;
   const int nchunk = a.zz ? 2 * (a.cp / a.a2a) : a.cp / a.a2a;
   if (a.kind <= kZigzagInv && row_bytes % 16 == 0 && al % 16 == 0 && a.T % nchunk == 0)
-    e = run_chunks(a, src, dst, row_bytes, st);
+    e = run_chunks(a, 1, &src, &dst, &a.H, row_bytes, st);
   else if (row_bytes % 16 == 0 && al % 16 == 0 && row_bytes / 16 == 16)
     e = run_rows<2>(p, src, dst, rows, st);
   else if (row_bytes % 16 == 0 && al % 16 == 0 && row_bytes / 16 == 8)
@@ -229,6 +254,32 @@ cudaError_t launch_permute(const PermuteArgs& a, const void* src, void* dst, cud
     e = run<int>(p, src, dst, rows, row_bytes / 4, st);
   else
     e = run<short>(p, src, dst, rows, row_bytes / 2, st);
+  timing_end(st);
+  return e;
+}
+
+// Several permutes of one kind over tensors of one descriptor (n_heads[i] heads
+// each): zigzag permutes whose rows are whole 16-byte vectors go out as one launch
+// of chunk moves; anything else as one launch per tensor.
+cudaError_t launch_permute_batch(const PermuteArgs& a, int n, const void* const* src,
+                                 void* const* dst, const int* n_heads, cudaStream_t st) {
+  const int row_bytes = a.D * a.elt;
+  const int nchunk = a.zz ? 2 * (a.cp / a.a2a) : a.cp / a.a2a;
+  bool chunks = a.kind <= kZigzagInv && row_bytes % 16 == 0 && a.T % nchunk == 0 &&
+                n <= kMaxBatch;
+  for (int i = 0; i < n && chunks; ++i)
+    chunks = (((uintptr_t)src[i] | (uintptr_t)dst[i]) % 16) == 0;
+  if (!chunks) {
+    for (int i = 0; i < n; ++i) {
+      PermuteArgs ai = a;
+      ai.H = n_heads[i];
+      cudaError_t e = launch_permute(ai, src[i], dst[i], st);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  timing_begin("layout_zigzag_batch", st);
+  cudaError_t e = run_chunks(a, n, src, dst, n_heads, row_bytes, st);
   timing_end(st);
   return e;
 }

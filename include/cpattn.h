@@ -321,6 +321,21 @@ cpattn_status cpattn_layout(int permute, const cpattn_desc* desc, const void* sr
                             int n_heads, void* stream);
 
 /*
+ * The permutes of several tensors of one descriptor in one call, e.g. a step's q,
+ * k, v and dO before the ring, or o, dq, dk and dv after it: tensor i goes from
+ * src[i] to dst[i] and has n_heads[i] heads.  The result is that of n calls of
+ * cpattn_layout; zigzag permutes whose rows are whole 16-byte vectors run as a
+ * single launch of chunk moves (the K/V-sized tensors alone would be launch-bound).
+ *   n        : 1 <= n <= 8
+ *   src, dst, n_heads : HOST arrays of n entries (device pointers in src and dst)
+ * Errors: n out of range or a null array -> CPATTN_ERR_INVALID_ARG; each tensor is
+ * checked as by cpattn_layout, before anything is enqueued.
+ */
+cpattn_status cpattn_layout_batch(int permute, const cpattn_desc* desc, int n,
+                                  const void* const* src, void* const* dst, const int* n_heads,
+                                  void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns the first device error since the last check
  * (CPATTN_ERR_TIMEOUT: a kernel's bounded wait ran out; CPATTN_ERR_BOUNDS: a

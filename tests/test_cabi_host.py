@@ -141,3 +141,22 @@ def test_packed_arguments_are_checked(cp):
     assert cp.cpattn_ring_bwd_packed(d, FAKE, 0, *b, FAKE, need, 0) == 1
     assert cp.cpattn_ring_bwd_packed(d, FAKE, 2, *b, FAKE, need - 1, 0) == 1
     assert cp.cpattn_ring_bwd_packed(_desc(cp, causal=0), FAKE, 2, *b, FAKE, need, 0) == 2
+
+
+def test_layout_batch_arguments_are_checked(cp):
+    d = _desc(cp)
+    srcs = [FAKE, FAKE + 4096]
+    dsts = [FAKE + 8192, FAKE + 12288]
+    assert cp.cpattn_layout_batch(0, d, [], [], [], 0) == 1                  # n = 0
+    assert cp.cpattn_layout_batch(0, d, [FAKE] * 9, [FAKE + 64] * 9, [4] * 9, 0) == 1  # n > 8
+    assert cp.cpattn_layout_batch(0, d, srcs, [dsts[0], srcs[1]], [4, 2], 0) == 1     # src == dst
+    assert cp.cpattn_layout_batch(0, d, srcs, dsts, [4, 0], 0) == 1          # no heads
+    assert cp.cpattn_layout_batch(0, d, [srcs[0], FAKE + 8], dsts, [4, 2], 0) == 1    # misaligned
+    assert cp.cpattn_layout_batch(9, d, srcs, dsts, [4, 2], 0) == 1          # no such permute
+    assert cp.cpattn_layout_batch(0, _desc(cp, H_q=3), srcs, dsts, [4, 2], 0) == 1  # descriptor
+    lib = ctypes.CDLL(cp.LIB_PATH)
+    f = lib.cpattn_layout_batch
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.POINTER(cp.CpattnDesc), ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(0, ctypes.byref(d), 1, None, None, None, None) == 1             # null arrays

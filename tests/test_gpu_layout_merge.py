@@ -35,6 +35,37 @@ def test_zigzag_permute_bit_exact(dtype, B, H, T, D, cp_, layout):
     cp.check(cp.cpattn_check())
 
 
+@pytest.mark.parametrize("kind", ["fwd", "inv"])
+@pytest.mark.parametrize("dtype,layout,B,Hq,Hkv,T,D,cp_", [
+    (torch.bfloat16, "zigzag", 1, 32, 8, 8192, 128, 8),     # the LLaMA step's four tensors
+    (torch.bfloat16, "contiguous", 2, 4, 2, 1024, 64, 4),
+    (torch.float32, "zigzag", 2, 3, 1, 96, 20, 3),
+    (torch.float32, "zigzag", 2, 3, 1, 96, 6, 3),           # 24-byte rows: per-tensor launches
+    (torch.float32, "zigzag", 1, 4, 4, 256, 16, 2)])
+def test_layout_batch_equals_single_permutes(kind, dtype, layout, B, Hq, Hkv, T, D, cp_):
+    """cpattn_layout_batch over a step's q, k, v, dO equals cpattn_layout on each,
+    bit for bit, and so the oracle's index map."""
+    cp = cp_mod()
+    g = torch.Generator().manual_seed(13)
+    dt = "bf16" if dtype == torch.bfloat16 else "f32"
+    heads = [Hq, Hkv, Hkv, Hq]
+    xs = [torch.randn(B, h, T, D, generator=g).to(dtype) for h in heads]
+    d = cp.make_desc(B, Hq, Hkv, T, D, cp_, layout, dt)
+    perm = cp.ZIGZAG_FWD if kind == "fwd" else cp.ZIGZAG_INV
+    src = [x.to(dev()) for x in xs]
+    got = [torch.empty_like(x) for x in src]
+    cp.check(cp.cpattn_layout_batch(perm, d, src, got, heads))
+    for x, y, h in zip(src, got, heads):
+        one = torch.empty_like(x)
+        cp.check(cp.cpattn_layout(perm, d, x, one, h))
+        assert torch.equal(_bits(y), _bits(one))
+    pos = OL.positions(T, cp_, layout)
+    idx = torch.from_numpy(pos if kind == "fwd" else OL.layout_slots(T, cp_, layout))
+    for x, y in zip(xs, got):
+        assert torch.equal(_bits(y.cpu()), _bits(x[:, :, idx].contiguous()))
+    cp.check(cp.cpattn_check())
+
+
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 @pytest.mark.parametrize("B,H,T,D,cp_,a2a", [(1, 8, 256, 64, 8, 2), (2, 4, 128, 32, 4, 2),
                                              (1, 6, 96, 16, 6, 3), (1, 32, 32768, 128, 8, 2),
