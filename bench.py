@@ -23,6 +23,13 @@ before each: the (O, LSE) merge at the LLaMA and Qwen3 ring-step sizes, the a2a
 head<->sequence re-layout at the Qwen3 size, and the zigzag chunk copies at the
 LLaMA size; GB/s of algorithmic bytes against the measured copy bandwidth.
 
+--mode p2p times the ring of per-step library calls (cpattn_partial_fwd,
+cpattn_merge, cpattn_partial_bwd) that the point-to-point ring across GPUs runs:
+under torch.distributed.run with N processes, the real ring over N = cp ranks (one
+per GPU, K/V exchanged by NCCL); in one process, all cp ranks of the workload in
+lockstep on one GPU, replayed from a CUDA graph (the step is hundreds of small
+launches).  Same FLOP count as the ring.
+
 --mode allgather times the all-gather mode instead (pull request #181, mode table
 row "all_gather"): one step = cpattn_allgather_fwd and cpattn_allgather_bwd for
 every emulated rank, with the layout-order q, k, v and each rank's dO rows already
@@ -69,7 +76,10 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.ALL))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="ring", choices=["ring", "allgather", "hbm"])
+    ap.add_argument("--mode", default="ring", choices=["ring", "allgather", "hbm", "p2p"])
+    ap.add_argument("--no-graph", action="store_true",
+                    help="--mode p2p on one GPU: launch the steps eagerly instead of "
+                         "replaying them from a CUDA graph")
     ap.add_argument("--packed-docs", type=int, default=0,
                     help="ring mode over packed sequences: this many documents per row, "
                          "seeded random lengths (0: one sequence per row)")
@@ -193,6 +203,13 @@ def kernel_flops_or_bytes(name, w, pairs=None):
     if name in ("tc_bwd_dq", "simt_bwd_dq", "tc_packed_dq"):        # the dQ product only
         return "tensor", 2.0 * w.D * pairs
     # all-gather mode: one launch covers one rank's rows (1/cp of the pairs on average)
+    # one ring step (rank, chunk): 1 / cp^2 of the pairs on average
+    if name == "tc_partial_fwd":
+        return "tensor", 4.0 * w.D * pairs / w.cp ** 2
+    if name == "tc_partial_dkdv":
+        return "tensor", 8.0 * w.D * pairs / w.cp ** 2
+    if name == "tc_partial_dq":
+        return "tensor", 2.0 * w.D * pairs / w.cp ** 2
     if name == "tc_allgather_fwd":
         return "tensor", 4.0 * w.D * pairs / w.cp
     if name == "tc_allgather_dkdv":
@@ -715,6 +732,141 @@ def run_allgather(args, rank, world):
             "clocks": clocks, "e2e": e2e, "kernels": kernels}
 
 
+def run_p2p(args, rank, world):
+    """The point-to-point ring of per-step library calls: the real ring over the
+    world's ranks (world = cp), or all cp ranks emulated in lockstep on one GPU."""
+    import torch
+    import blockwise_online_softmax_cpattn_gb300 as cp
+    from blockwise_online_softmax_cpattn_gb300 import ring as R
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.ALL[args.workload]
+    if w.a2a != 1:
+        raise SystemExit("--mode p2p takes a plain ring workload (a2a = 1)")
+    if world > 1:
+        w = w.replace(cp=world)  # one rank per GPU
+    stream = torch.cuda.current_stream()
+    desc = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, w.D, w.cp, w.layout, w.dtype)
+    nat = W.draw_cast(w)
+    H = [w.H_q, w.H_kv, w.H_kv, w.H_q]
+    lay = []
+    for x, h in zip(nat, H):  # layout order, prepared outside the timed region
+        y = torch.empty(w.B, h, w.T, w.D, dtype=x.dtype, device=dev)
+        cp.check(cp.cpattn_layout(cp.ZIGZAG_FWD, desc, x.to(dev), y, h))
+        lay.append(y)
+    chunks = [R.rank_chunks(x, w.cp) for x in lay]  # [tensor][rank]
+    steps = R.LibrarySteps(desc, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    if world > 1:
+        exch = R.DistExchange()
+        mine = [c[rank] for c in chunks]
+
+        def step():
+            o, lse, _ = R.ring_forward(steps, exch, mine[0], mine[1], mine[2])
+            return R.ring_backward(steps, exch, mine[0], mine[1], mine[2], o, lse, mine[3])[:3]
+    else:
+        def step():
+            os_, lses, _ = R.emulate_ring_forward(steps, w.cp, *chunks[:3])
+            return R.emulate_ring_backward(steps, w.cp, *chunks[:3], os_, lses, chunks[3])[:3]
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cp.check(cp.cpattn_check())
+    graph = None
+    if world == 1 and not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+
+    def run_once():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        run_once()
+        b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    cp.check(cp.cpattn_check())
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, dev)
+    flops = w.fwd_flops + w.bwd_flops
+    value = flops / (ms * 1e-3) / 1e12   # the ranks share one problem: no world factor
+    # per-kernel durations (eager launches of the same steps, events on the stream)
+    cp.cpattn_timing_reset()
+    cp.cpattn_timing_enable(True)
+    for _ in range(min(args.steps, 5)):
+        flush.zero_()
+        step()
+    cp.check(cp.cpattn_timing_collect())
+    cp.cpattn_timing_enable(False)
+    table = cp.cpattn_timing_table()
+    cp.cpattn_timing_reset()
+    n_timed = min(args.steps, 5)
+    launches_per_step = sum(n for _, n in table.values()) / n_timed
+    total = sum(t for t, _ in table.values())
+    kernels = {name: {"avg_ms": tot / n, "launches": n, "share": tot / total}
+               for name, (tot, n) in table.items()}
+    dom = max(table, key=lambda n: table[n][0])
+    pk, src_pk = peaks()
+    peak, peak_what = tensor_peak(pk, src_pk, t1 - t0)
+    bound, work = kernel_flops_or_bytes(dom, w)
+    avg_ms = table[dom][0] / table[dom][1]
+    if bound == "tensor":
+        achieved = work / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_what,
+                "work_per_launch": work, "avg_launch_ms": avg_ms,
+                "note": "work per launch is the average over the cp^2 (rank, chunk) steps",
+                "traffic": None}
+    else:
+        roof = hbm_roofline(dom, work, avg_ms, pk, src_pk)
+        roof["traffic"] = None
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": config_of(w, {
+                "mode": "p2p",
+                "parallelism": (f"ring over {world} GPUs, K/V exchanged by NCCL point to point"
+                                if world > 1 else
+                                f"the {w.cp} ranks of the ring emulated in lockstep on one GPU"),
+                "graph": graph is not None,
+                "l2": "flushed before every timed step (256 MiB device write, outside the events)",
+                "step": "per rank and step: cpattn_partial_fwd + cpattn_merge, then "
+                        "cpattn_partial_bwd with the chunk's float32 dK/dV travelling the ring",
+                "pct_of_bf16_peak": value / peak, "peak_source": peak_what}),
+            "roofline": roof, "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clocks, "e2e": None,
+            "e2e_note": "not measured in this mode: the inputs are the ranks' chunks, "
+                        "already resident", "kernels": kernels}
+
+
 def run_hbm(args):
     """The HBM-bound kernels alone: each launch timed with CUDA events on its stream,
     L2 flushed (256 MiB write) before every launch, outside the events."""
@@ -882,7 +1034,12 @@ def main():
         if rank == 0:
             print(json.dumps(run_hbm(args)))
         return
-    out = run_allgather(args, rank, world) if args.mode == "allgather" else run_cpattn(args, rank, world)
+    if args.mode == "p2p":
+        out = run_p2p(args, rank, world)
+    elif args.mode == "allgather":
+        out = run_allgather(args, rank, world)
+    else:
+        out = run_cpattn(args, rank, world)
     if rank == 0:
         w = W.ALL[args.workload]
         if world == 1 and not args.no_cpu_baseline:

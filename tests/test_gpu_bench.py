@@ -83,3 +83,18 @@ def test_bench_a2a_ulysses():
     out = _bench("--workload", "llama_gqa_T8192_ulysses8")
     _check_contract(out, "tc_")
     assert any(name.startswith("layout_a2a") for name in out["kernels"])
+
+
+def test_bench_p2p_ring_emulated_gpt2():
+    """--mode p2p on one GPU: the per-step library calls of the ring across GPUs,
+    all cp ranks in lockstep, replayed from a CUDA graph."""
+    out = _bench("--workload", "gpt2_small_T1024_cp4_zigzag", "--mode", "p2p")
+    assert REQUIRED - {"e2e"} <= set(out) and out["e2e"] is None
+    assert out["unit"] == "TFLOP/s" and out["value"] > 0 and out["n_gpus"] == 1
+    assert out["config"]["mode"] == "p2p" and out["config"]["graph"] is True
+    names = set(out["kernels"])
+    assert {"tc_partial_fwd", "merge", "tc_partial_dkdv", "tc_partial_dq"} <= names
+    # cp^2 forward steps per training step, over the min(steps, 5) steps of the
+    # per-kernel timing pass
+    assert out["kernels"]["tc_partial_fwd"]["launches"] == min(STEPS, 5) * 4 * 4
+    assert out["roofline"]["frac"] < 2.0

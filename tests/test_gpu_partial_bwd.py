@@ -117,3 +117,38 @@ def test_ring_driver_emulated_on_one_gpu(w):
             LSE_ABS_TOL[w.dtype]
         for name, got in (("dq", dqs[r]), ("dk", dks[r]), ("dv", dvs[r])):
             assert rel(W.as_f64(got), ref[name][:, :, p]) <= tol["grad"], (w.name, name, r)
+
+
+def test_ring_driver_replays_from_a_cuda_graph():
+    """The emulated ring's library calls are safe to capture in a CUDA graph: a
+    replay gives the eager run's results bit for bit (the kernels are deterministic)
+    and so matches the oracle."""
+    from blockwise_online_softmax_cpattn_gb300 import ring as R
+    cp = cp_mod()
+    w = CASES[0]
+    nat, lay = ring_inputs(w)
+    steps = R.LibrarySteps(desc_of(w), device=dev())
+    chunks = [R.rank_chunks(x, w.cp) for x in lay]
+
+    def step():
+        os_, lses, _ = R.emulate_ring_forward(steps, w.cp, *chunks[:3])
+        dqs, dks, dvs, _ = R.emulate_ring_backward(steps, w.cp, *chunks[:3], os_, lses, chunks[3])
+        return os_ + lses + dqs + dks + dvs
+
+    eager = [x.clone() for x in step()]
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        captured = step()
+    for x in captured:
+        x.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    cp.check(cp.cpattn_check())
+    for a, b in zip(captured, eager):
+        assert torch.equal(a, b)
