@@ -63,9 +63,11 @@ _sigs = {
     "cpattn_partial_fwd": (_st, [ctypes.POINTER(CpattnDesc), ctypes.c_int, ctypes.c_int, _vp, _vp,
                                  _vp, _vp, _vp, _vp]),
     "cpattn_partial_bwd_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
+    "cpattn_partial_bwd_stats": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp,
+                                       ctypes.c_size_t, _vp]),
     "cpattn_partial_bwd": (_st, [ctypes.POINTER(CpattnDesc), ctypes.c_int, ctypes.c_int, _vp, _vp,
-                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp,
-                                 ctypes.c_size_t, _vp]),
+                                 _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t,
+                                 _vp]),
     "cpattn_merge": (_st, [ctypes.c_int64, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "cpattn_ring_fwd": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp, _vp, _vp]),
     "cpattn_ring_bwd_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
@@ -138,11 +140,17 @@ def cpattn_partial_bwd_workspace(desc) -> int:
     return _lib.cpattn_partial_bwd_workspace(ctypes.byref(desc))
 
 
-def cpattn_partial_bwd(desc, q_rank, kv_rank, q, k, v, o, lse, dO, dq_part, dk_part, dv_part,
-                       accumulate, workspace, ws_bytes=None, stream=None) -> int:
+def cpattn_partial_bwd_stats(desc, o, lse, dO, workspace, ws_bytes=None, stream=None) -> int:
+    return _lib.cpattn_partial_bwd_stats(ctypes.byref(desc), _ptr(o), _ptr(lse), _ptr(dO),
+                                         _ptr(workspace), _ws_bytes(workspace, ws_bytes),
+                                         _stream(stream))
+
+
+def cpattn_partial_bwd(desc, q_rank, kv_rank, q, k, v, dO, dq_part, dk_part, dv_part, accumulate,
+                       workspace, ws_bytes=None, stream=None) -> int:
     return _lib.cpattn_partial_bwd(ctypes.byref(desc), q_rank, kv_rank, _ptr(q), _ptr(k), _ptr(v),
-                                   _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq_part), _ptr(dk_part),
-                                   _ptr(dv_part), int(accumulate), _ptr(workspace),
+                                   _ptr(dO), _ptr(dq_part), _ptr(dk_part), _ptr(dv_part),
+                                   int(accumulate), _ptr(workspace),
                                    _ws_bytes(workspace, ws_bytes), _stream(stream))
 
 

@@ -409,40 +409,57 @@ cpattn_status cpattn_allgather_bwd(const cpattn_desc* desc, int q_rank, const vo
 // ---------------------------------------------------------------------------
 // one ring step of the backward
 // ---------------------------------------------------------------------------
-// Workspace: Delta, then the LSE in base 2, of the rank's rows (as the all-gather
-// backward's).
+// Workspace: two float32 sections of the rank's rows, each 256-byte aligned.  The
+// tensor-core path keeps -Delta and -LSE log2(e) there, the SIMT path Delta and
+// the LSE (natural log).
 size_t cpattn_partial_bwd_workspace(const cpattn_desc* desc) {
   return cpattn_allgather_bwd_workspace(desc);
 }
 
+cpattn_status cpattn_partial_bwd_stats(const cpattn_desc* desc, const void* o, const float* lse,
+                                       const void* dO, void* workspace, size_t ws_bytes,
+                                       void* stream) {
+  Ring R;
+  cpattn_status s = validate(desc, &R);
+  if (s != CPATTN_OK) return s;
+  if (!aligned16(o) || !aligned16(lse) || !aligned16(dO) || !aligned16(workspace))
+    return CPATTN_ERR_INVALID_ARG;
+  if (ws_bytes < cpattn_partial_bwd_workspace(desc)) return CPATTN_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  float* delta = static_cast<float*>(workspace);
+  float* sec1 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ag_section(R));
+  const int64_t rows = (int64_t)R.B * R.Hq * (R.T / R.cp);
+  const bool tc = R.bf16 && tc_supported(R);
+  cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? sec1 : nullptr, st);
+  if (e == cudaSuccess && !tc)
+    e = cudaMemcpyAsync(sec1, lse, rows * sizeof(float), cudaMemcpyDeviceToDevice, st);
+  return from_cuda(e);
+}
+
 cpattn_status cpattn_partial_bwd(const cpattn_desc* desc, int q_rank, int kv_rank,
-                                 const void* q, const void* k, const void* v, const void* o,
-                                 const float* lse, const void* dO, float* dq_part,
-                                 float* dk_part, float* dv_part, int accumulate,
-                                 void* workspace, size_t ws_bytes, void* stream) {
+                                 const void* q, const void* k, const void* v, const void* dO,
+                                 float* dq_part, float* dk_part, float* dv_part, int accumulate,
+                                 const void* workspace, size_t ws_bytes, void* stream) {
   Ring R;
   cpattn_status s = validate(desc, &R);
   if (s != CPATTN_OK) return s;
   if (q_rank < 0 || q_rank >= R.cp || kv_rank < 0 || kv_rank >= R.cp ||
       (accumulate != 0 && accumulate != 1))
     return CPATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      !aligned16(dO) || !aligned16(dq_part) || !aligned16(dk_part) || !aligned16(dv_part) ||
-      !aligned16(workspace))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq_part) ||
+      !aligned16(dk_part) || !aligned16(dv_part) || !aligned16(workspace))
     return CPATTN_ERR_INVALID_ARG;
   if (ws_bytes < cpattn_partial_bwd_workspace(desc)) return CPATTN_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
-  float* delta = static_cast<float*>(workspace);
-  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ag_section(R));
-  const int64_t rows = (int64_t)R.B * R.Hq * (R.T / R.cp);
-  const bool tc = R.bf16 && tc_supported(R);
-  cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
-  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  if (tc)
-    return from_cuda(launch_tc_partial_bwd(R, q_rank, kv_rank, q, k, v, lse2, delta, dO, dq_part,
+  const float* delta = static_cast<const float*>(workspace);
+  const float* sec1 =
+      reinterpret_cast<const float*>(static_cast<const char*>(workspace) + ag_section(R));
+  if (R.bf16 && tc_supported(R))
+    return from_cuda(launch_tc_partial_bwd(R, q_rank, kv_rank, q, k, v, sec1, delta, dO, dq_part,
                                            dk_part, dv_part, accumulate, status_ptr(), st));
-  return from_cuda(launch_simt_partial_bwd(R, q_rank, kv_rank, q, k, v, lse, delta, dO, dq_part,
+  return from_cuda(launch_simt_partial_bwd(R, q_rank, kv_rank, q, k, v, sec1, delta, dO, dq_part,
                                            dk_part, dv_part, accumulate, st));
 }
 

@@ -83,7 +83,9 @@ class _BwdRank:
 
     def __init__(self, steps, rank: int, cp: int, q, k, v, o, lse, do):
         self.steps, self.rank, self.cp = steps, rank, cp
-        self.rows = (q, o, lse, do)
+        self.rows = (q, do)
+        # the rank's row statistics, once for all of its steps
+        steps.bwd_stats(rank, o, lse, do)
         self.kv = [k, v]
         self.dq = steps.new_q_grad()
         self.dkv = list(steps.new_kv_grads())
@@ -92,10 +94,10 @@ class _BwdRank:
     def step(self, i: int) -> None:
         s = ring_source(self.rank, i, self.cp)
         self.held.append(s)
-        q, o, lse, do = self.rows
+        q, do = self.rows
         # step 0: the rank's own chunk, whose accumulators start here; later steps
         # add to what the previous ranks left in them
-        self.steps.partial_bwd(self.rank, s, q, self.kv[0], self.kv[1], o, lse, do, self.dq,
+        self.steps.partial_bwd(self.rank, s, q, self.kv[0], self.kv[1], do, self.dq,
                                self.dkv[0], self.dkv[1], accumulate=i > 0)
 
 
@@ -237,8 +239,8 @@ class LibrarySteps:
         self.q_full = torch.zeros(B, Hq, T, D, **kw)
         self.k_full = torch.zeros(B, Hkv, T, D, **kw)
         self.v_full = torch.zeros(B, Hkv, T, D, **kw)
-        self.ws = torch.empty(cpattn_partial_bwd_workspace(desc), dtype=torch.uint8,
-                              device=self.device)
+        self.ws_bytes = cpattn_partial_bwd_workspace(desc)
+        self.stats = {}  # rank -> its row statistics (one workspace per rank)
 
     def _place(self, r: int, s: int, q, k, v) -> None:
         c = self.c
@@ -269,11 +271,18 @@ class LibrarySteps:
         return (t.empty(self.kv_shape, dtype=t.float32, device=self.device),
                 t.empty(self.kv_shape, dtype=t.float32, device=self.device))
 
-    def partial_bwd(self, r, s, q, k, v, o, lse, do, dq, dk, dv, accumulate) -> None:
+    def bwd_stats(self, r: int, o, lse, do) -> None:
+        from . import check, cpattn_partial_bwd_stats
+        if r not in self.stats:
+            self.stats[r] = self.torch.empty(self.ws_bytes, dtype=self.torch.uint8,
+                                             device=self.device)
+        check(cpattn_partial_bwd_stats(self.desc, o, lse, do, self.stats[r], None, self.stream))
+
+    def partial_bwd(self, r, s, q, k, v, do, dq, dk, dv, accumulate) -> None:
         from . import check, cpattn_partial_bwd
         self._place(r, s, q, k, v)
-        check(cpattn_partial_bwd(self.desc, r, s, self.q_full, self.k_full, self.v_full, o, lse,
-                                 do, dq, dk, dv, 1 if accumulate else 0, self.ws, None,
+        check(cpattn_partial_bwd(self.desc, r, s, self.q_full, self.k_full, self.v_full, do, dq,
+                                 dk, dv, 1 if accumulate else 0, self.stats[r], None,
                                  self.stream))
 
     def finish_fwd(self, o, lse):

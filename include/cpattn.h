@@ -118,9 +118,25 @@ cpattn_status cpattn_partial_fwd(const cpattn_desc* desc, int q_rank, int kv_ran
                                  const void* q, const void* k, const void* v,
                                  float* o_part, float* lse_part, void* stream);
 
-/* Bytes of device workspace cpattn_partial_bwd needs (float32 row statistics of
- * one rank's rows). */
+/* Bytes of device workspace that holds one rank's row statistics for
+ * cpattn_partial_bwd (float32, two values per query row of the rank). */
 size_t cpattn_partial_bwd_workspace(const cpattn_desc* desc);
+
+/*
+ * The row statistics of a rank's backward ring steps, computed once per rank and
+ * backward pass (the backward's pre-pass, Delta = rowsum(dO * O), with the LSE in
+ * the form the kernels read), into `workspace`; every cpattn_partial_bwd of that
+ * rank reads them, so the pre-pass is not repeated at each of its cp steps.
+ *   o, lse, dO : the rank's rows of the forward's output, of its LSE (the whole
+ *                forward's, every step merged) and of the upstream gradient:
+ *                [B', H_q', c, D] dtype, [B', H_q', c] float32, [B', H_q', c, D]
+ *   workspace  : at least cpattn_partial_bwd_workspace(desc) bytes (smaller ->
+ *                CPATTN_ERR_INVALID_ARG)
+ * Errors as cpattn_ring_bwd.
+ */
+cpattn_status cpattn_partial_bwd_stats(const cpattn_desc* desc, const void* o, const float* lse,
+                                       const void* dO, void* workspace, size_t ws_bytes,
+                                       void* stream);
 
 /*
  * One ring step of the backward pass (tutorial "上下文并行", section "朴素 Ring
@@ -131,16 +147,16 @@ size_t cpattn_partial_bwd_workspace(const cpattn_desc* desc);
  * q_rank's queries against the K/V chunk of rank kv_rank:
  *   q, k, v     : full layout-order tensors (as cpattn_partial_fwd: only q_rank's
  *                 query slots and kv_rank's key slots are read)
- *   o, lse, dO  : rank q_rank's rows of the forward's output, of its LSE (the whole
- *                 forward's, every step merged) and of the upstream gradient:
- *                 [B', H_q', c, D] dtype, [B', H_q', c] float32, [B', H_q', c, D]
+ *   dO          : rank q_rank's rows of the upstream gradient, [B', H_q', c, D]
+ *   workspace   : the rank's statistics, as cpattn_partial_bwd_stats left them for
+ *                 the same rank's o, lse and dO (read only)
  *   dq_part     : [B', H_q', c, D] float32, the step's dQ contribution to the
  *                 rank's rows
  *   dk_part, dv_part : [B', H_kv', c, D] float32, the step's dK / dV contribution
  *                 to chunk kv_rank's rows (slot order within the chunk)
  *   accumulate  : 0 overwrites dq_part, dk_part and dv_part; 1 adds to them
- *   workspace   : at least cpattn_partial_bwd_workspace(desc) bytes (smaller ->
- *                 CPATTN_ERR_INVALID_ARG); contents on entry do not matter
+ *   ws_bytes    : at least cpattn_partial_bwd_workspace(desc) (smaller ->
+ *                 CPATTN_ERR_INVALID_ARG)
  * Summed over the steps -- dq_part of rank r over every kv_rank, dk_part/dv_part
  * of chunk s over every q_rank -- the contributions give cpattn_ring_bwd's dq
  * (rank r's rows) and dk/dv (chunk s's rows), in float32.  A pair with no
@@ -150,10 +166,9 @@ size_t cpattn_partial_bwd_workspace(const cpattn_desc* desc);
  * CPATTN_ERR_INVALID_ARG; others as cpattn_ring_bwd.
  */
 cpattn_status cpattn_partial_bwd(const cpattn_desc* desc, int q_rank, int kv_rank,
-                                 const void* q, const void* k, const void* v, const void* o,
-                                 const float* lse, const void* dO, float* dq_part,
-                                 float* dk_part, float* dv_part, int accumulate,
-                                 void* workspace, size_t ws_bytes, void* stream);
+                                 const void* q, const void* k, const void* v, const void* dO,
+                                 float* dq_part, float* dk_part, float* dv_part, int accumulate,
+                                 const void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Online-softmax merge of two partial results over disjoint key sets (tutorial,

@@ -160,3 +160,18 @@ def test_layout_batch_arguments_are_checked(cp):
     f.argtypes = [ctypes.c_int, ctypes.POINTER(cp.CpattnDesc), ctypes.c_int, ctypes.c_void_p,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     assert f(0, ctypes.byref(d), 1, None, None, None, None) == 1             # null arrays
+
+
+def test_partial_bwd_arguments_are_checked(cp):
+    d = _desc(cp)  # cp = 2
+    need = cp.cpattn_partial_bwd_workspace(d)
+    assert need == cp.cpattn_allgather_bwd_workspace(d) and need % 256 == 0
+    assert cp.cpattn_partial_bwd_stats(d, FAKE, FAKE, FAKE, FAKE, need - 1, 0) == 1
+    assert cp.cpattn_partial_bwd_stats(d, FAKE, FAKE + 4, FAKE, FAKE, need, 0) == 1
+    assert cp.cpattn_partial_bwd_stats(_desc(cp, D=192), FAKE, FAKE, FAKE, FAKE, need, 0) == 2
+    args = [FAKE] * 7
+    assert cp.cpattn_partial_bwd(d, 2, 0, *args, 0, FAKE, need, 0) == 1       # q rank
+    assert cp.cpattn_partial_bwd(d, 0, -1, *args, 0, FAKE, need, 0) == 1      # kv rank
+    assert cp.cpattn_partial_bwd(d, 0, 1, *args, 2, FAKE, need, 0) == 1       # accumulate
+    assert cp.cpattn_partial_bwd(d, 0, 1, *args, 1, FAKE, need - 1, 0) == 1   # workspace
+    assert cp.cpattn_partial_bwd(d, 0, 1, *args[:6], 0, 0, FAKE, need, 0) == 1  # null dv_part

@@ -86,8 +86,9 @@ def test_ring_and_partial_stay_in_bounds(w):
     # one backward ring step: the last rank's rows against chunk 0
     sl = slice(r * c, (r + 1) * c)
     o_r, lse_r, do_r = (x[:, :, sl].contiguous() for x in (b["o"].t, b["lse"].t, do))
-    cp.check(cp.cpattn_partial_bwd(d, r, 0, q, k, v, o_r, lse_r, do_r, b["dq_part"].t,
-                                   b["dk_part"].t, b["dv_part"].t, 0, b["ws_part"].t))
+    cp.check(cp.cpattn_partial_bwd_stats(d, o_r, lse_r, do_r, b["ws_part"].t))
+    cp.check(cp.cpattn_partial_bwd(d, r, 0, q, k, v, do_r, b["dq_part"].t, b["dk_part"].t,
+                                   b["dv_part"].t, 0, b["ws_part"].t))
     cp.check(cp.cpattn_check())
     check_all(b, written=("o", "lse", "dq", "dk", "dv", "o_part", "lse_part", "o_m", "lse_m",
                           "dq_part", "dk_part", "dv_part"))

@@ -48,19 +48,27 @@ def test_partial_bwd_steps_match_oracle_and_sum_to_the_backward(w):
     n_rep = w.H_q // w.H_kv
     pos = OL.positions(w.T, w.cp, w.layout)
     tol = TOL[w.dtype]["grad"]
-    ws = torch.empty(cp.cpattn_partial_bwd_workspace(d), dtype=torch.uint8, device=dev())
     f32 = dict(dtype=torch.float32, device=dev())
     acc_dq = [torch.empty(w.B, w.H_q, c, w.D, **f32) for _ in range(w.cp)]
     acc_dk = [torch.empty(w.B, w.H_kv, c, w.D, **f32) for _ in range(w.cp)]
     acc_dv = [torch.empty(w.B, w.H_kv, c, w.D, **f32) for _ in range(w.cp)]
+    # every rank's statistics, once (a workspace per rank)
+    do_rows, stats = [], []
+    for r in range(w.cp):
+        sl_r = slice(r * c, (r + 1) * c)
+        o_r, lse_r, do_r = (x[:, :, sl_r].contiguous() for x in (o, lse, dol))
+        stats.append(torch.full((cp.cpattn_partial_bwd_workspace(d),), 255, dtype=torch.uint8,
+                                device=dev()))
+        cp.check(cp.cpattn_partial_bwd_stats(d, o_r, lse_r, do_r, stats[r]))
+        do_rows.append(do_r)
     for i in range(w.cp):
         for r in range(w.cp):
             s = OL.ring_source(r, i, w.cp)
             sl_r, sl_s = slice(r * c, (r + 1) * c), slice(s * c, (s + 1) * c)
-            o_r, lse_r, do_r = (x[:, :, sl_r].contiguous() for x in (o, lse, dol))
+            do_r = do_rows[r]
             # the step alone (accumulate = 0) against the oracle's step
             one = [torch.full_like(t, float("nan")) for t in (acc_dq[r], acc_dk[s], acc_dv[s])]
-            cp.check(cp.cpattn_partial_bwd(d, r, s, ql, kl, vl, o_r, lse_r, do_r, *one, 0, ws))
+            cp.check(cp.cpattn_partial_bwd(d, r, s, ql, kl, vl, do_r, *one, 0, stats[r]))
             qp, kp = pos[sl_r], pos[sl_s]
             sdq = np.zeros((w.B, w.H_q, c, w.D))
             sdk = np.zeros((w.B, w.H_kv, c, w.D))
@@ -81,8 +89,8 @@ def test_partial_bwd_steps_match_oracle_and_sum_to_the_backward(w):
                 else:
                     assert rel(g64, ref) <= tol, (w.name, r, s, name, rel(g64, ref))
             # the ring in step order: dQ of rank r and the chunk's dK/dV accumulate
-            cp.check(cp.cpattn_partial_bwd(d, r, s, ql, kl, vl, o_r, lse_r, do_r, acc_dq[r],
-                                           acc_dk[s], acc_dv[s], int(i > 0), ws))
+            cp.check(cp.cpattn_partial_bwd(d, r, s, ql, kl, vl, do_r, acc_dq[r], acc_dk[s],
+                                           acc_dv[s], int(i > 0), stats[r]))
     cp.check(cp.cpattn_check())
     for r in range(w.cp):
         p = pos[r * c:(r + 1) * c]

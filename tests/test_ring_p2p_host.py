@@ -87,8 +87,13 @@ class OracleSteps:
         return (torch.full(shape, float("nan"), dtype=torch.float64),
                 torch.full(shape, float("nan"), dtype=torch.float64))
 
-    def partial_bwd(self, r, s, q, k, v, o, lse, do, dq, dk, dv, accumulate):
+    def bwd_stats(self, r, o, lse, do):
+        self.rank_stats = getattr(self, "rank_stats", {})
+        self.rank_stats[r] = (o.clone(), lse.clone())
+
+    def partial_bwd(self, r, s, q, k, v, do, dq, dk, dv, accumulate):
         self._check(r, s, q, k, v)
+        o, lse = self.rank_stats[r]
         qp, kp = self.pos[self._sl(r)], self.pos[self._sl(s)]
         B, H = q.shape[:2]
         gq, gk, gv = np.zeros(dq.shape), np.zeros(dk.shape), np.zeros(dv.shape)
