@@ -232,12 +232,23 @@ def kernel_flops_or_bytes(name, w, pairs=None):
 _CODE_TOKEN = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"', re.S)
 
 
-def source_digest():
-    """Hash of the library's kernel sources with comments, trailing blanks and empty
-    lines removed, so that only a change of the code itself voids a capture."""
+# The translation unit each kernel is compiled from: its .cu file and the headers it
+# includes.  A capture stays valid while these are unchanged (other files, such as
+# the host-side C ABI in api.cu, cannot change the kernel's code).
+KERNEL_SOURCES = {
+    "tc_ring_fwd": ("tc_fwd.cu", "common.cuh", "kernels.h"),
+    "tc_bwd_dkdv": ("tc_bwd.cu", "common.cuh", "kernels.h"),
+    "tc_bwd_dq": ("tc_bwd.cu", "common.cuh", "kernels.h"),
+}
+
+
+def source_digest(files=None):
+    """Hash of library sources (all of csrc/, or the given files of it) with comments,
+    trailing blanks and empty lines removed, so that only a change of the code itself
+    voids a capture."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blockwise_online_softmax_cpattn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(os.listdir(csrc) if files is None else files):
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             text = fh.read()
         code = _CODE_TOKEN.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
@@ -247,12 +258,12 @@ def source_digest():
 
 
 def traffic_for(kernel, workload):
-    """dram bytes per launch from the committed ncu summary, if the kernel's
-    sources are unchanged since the capture."""
+    """dram bytes per launch from the committed ncu summary, if the sources of the
+    kernel's translation unit are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
-    digest = source_digest()
+    digest = source_digest(KERNEL_SOURCES[kernel])
     with open(path) as f:
         for line in f:
             parts = line.split()

@@ -146,3 +146,27 @@ def test_source_digest_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.source_digest() != d0
     (csrc / "k.cu").write_text(src.replace('"a // b"', '"a // c"'))
     assert bench.source_digest() != d0
+
+
+def test_traffic_is_keyed_to_the_kernels_own_sources(tmp_path, monkeypatch):
+    """A capture's DRAM bytes are reported while the kernel's translation unit is
+    unchanged, stay valid across edits of other sources (the host-side C ABI), and
+    are voided by a code change in the kernel's .cu file or a header it includes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "blockwise_online_softmax_cpattn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    for f, text in (("tc_fwd.cu", "int fwd() { return 1; }\n"), ("common.cuh", "#pragma once\n"),
+                    ("kernels.h", "#pragma once\n"), ("api.cu", "int api() { return 2; }\n")):
+        (csrc / f).write_text(text)
+    digest = bench.source_digest(bench.KERNEL_SOURCES["tc_ring_fwd"])
+    (tmp_path / "profiles" / "ncu_traffic.txt").write_text(
+        f"# header\ntc_ring_fwd wl 123 {digest}\n")
+    assert bench.traffic_for("tc_ring_fwd", "wl") == 123.0
+    assert bench.traffic_for("tc_ring_fwd", "other") is None
+    (csrc / "api.cu").write_text("int api() { return 3; }\n")
+    assert bench.traffic_for("tc_ring_fwd", "wl") == 123.0
+    (csrc / "common.cuh").write_text("#pragma once\nconstexpr int k = 1;\n")
+    assert bench.traffic_for("tc_ring_fwd", "wl") is None
