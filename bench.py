@@ -457,90 +457,49 @@ def run_cpattn(args, rank, world):
             hdst.copy_(dsrc, non_blocking=True)
         stream.wait_stream(side_out)  # o's download is part of the step
 
-    # Head-chunked pipeline (one batch row, plain ring): the heads split into two
-    # halves, each a problem of its own for the library (H_q/2 query heads and their
-    # H_kv/2 K/V heads), so the second half's upload runs while the first half is
-    # computed and the first half's gradients download while the second is.
-    n_chunks = 2
-    chunked = w.B == 1 and w.a2a == 1 and w.H_kv % n_chunks == 0
-    if chunked:
-        d_c = cp.make_desc(w.B, w.H_q // n_chunks, w.H_kv // n_chunks, w.T, w.D, w.cp, w.layout,
-                           w.dtype)
+    # The plain ring (not packed): one cpattn_ring_step_host call per step, the
+    # library's own overlap of the transfers with the compute (independent halves of
+    # the problem, two copy streams); its host outputs are natural order, as outs.
+    host_step = not packed and w.a2a == 1
+    if host_step:
+        ws_step = torch.empty(cp.cpattn_ring_step_host_workspace(desc), dtype=torch.uint8,
+                              device=dev)
+        h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        d2h += h_lse.numel() * 4
 
-        def hs(x, c, h):
-            n = h // n_chunks
-            return x[:, c * n:(c + 1) * n]
-
-        ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
-        ev_do = [torch.cuda.Event() for _ in range(n_chunks)]
-        ev_o = [torch.cuda.Event() for _ in range(n_chunks)]
-        ev_g = [torch.cuda.Event() for _ in range(n_chunks)]
-
-    def e2e_step_chunked(a_ev):
-        side_in.wait_event(a_ev)
-        side_out.wait_event(a_ev)
-        with torch.cuda.stream(side_in):
-            for c in range(n_chunks):
-                for dst_, hsrc, h in zip(src[:3], up_host[:3], H[:3]):
-                    hs(dst_, c, h).copy_(hs(hsrc, c, h), non_blocking=True)
-                ev_in[c].record(side_in)
-            for c in range(n_chunks):
-                hs(src[3], c, H[3]).copy_(hs(up_host[3], c, H[3]), non_blocking=True)
-                ev_do[c].record(side_in)
-        for c in range(n_chunks):
-            stream.wait_event(ev_in[c])
-            cp.check(cp.cpattn_layout_batch(
-                fwd_perm, d_c, [hs(s_, c, h) for s_, h in zip(src[:3], H[:3])],
-                [hs(l_, c, h) for l_, h in zip(lay[:3], H[:3])], [h // n_chunks for h in H[:3]]))
-            cp.check(ring_fwd(hs(lay[0], c, w.H_q), hs(lay[1], c, w.H_kv), hs(lay[2], c, w.H_kv),
-                              hs(o, c, w.H_q), hs(lse, c, w.H_q), d=d_c))
-            cp.check(cp.cpattn_layout(inv_perm, d_c, hs(o, c, w.H_q), hs(outs[0], c, w.H_q),
-                                      w.H_q // n_chunks))
-            ev_o[c].record(stream)
-            side_out.wait_event(ev_o[c])
-            with torch.cuda.stream(side_out):
-                hs(host_out[0], c, w.H_q).copy_(hs(outs[0], c, w.H_q), non_blocking=True)
-        for c in range(n_chunks):
-            stream.wait_event(ev_do[c])
-            cp.check(cp.cpattn_layout(fwd_perm, d_c, hs(src[3], c, H[3]), hs(lay[3], c, H[3]),
-                                      H[3] // n_chunks))
-            cp.check(ring_bwd(hs(lay[0], c, w.H_q), hs(lay[1], c, w.H_kv), hs(lay[2], c, w.H_kv),
-                              hs(o, c, w.H_q), hs(lse, c, w.H_q), hs(lay[3], c, w.H_q),
-                              hs(dq, c, w.H_q), hs(dk, c, w.H_kv), hs(dv, c, w.H_kv), d=d_c))
-            cp.check(cp.cpattn_layout_batch(
-                inv_perm, d_c, [hs(x, c, h) for x, h in zip((dk, dv, dq), H_out[1:])],
-                [hs(y, c, h) for y, h in zip(outs[1:], H_out[1:])],
-                [h // n_chunks for h in H_out[1:]]))
-            ev_g[c].record(stream)
-            side_out.wait_event(ev_g[c])
-            with torch.cuda.stream(side_out):
-                for hdst, dsrc, h in zip(host_out[1:], outs[1:], (w.H_kv, w.H_kv, w.H_q)):
-                    hs(hdst, c, h).copy_(hs(dsrc, c, h), non_blocking=True)
-        stream.wait_stream(side_out)  # every download is part of the step
+    def e2e_step_library(a_ev):
+        cp.check(cp.cpattn_ring_step_host(desc, *up_host, host_out[0], h_lse, host_out[3],
+                                          host_out[1], host_out[2], ws_step))
 
     torch.cuda.synchronize()
     for a, b in ev2:
         flush.zero_()
         a.record(stream)
-        (e2e_step_chunked if chunked else e2e_step_overlapped)(a)
+        (e2e_step_library if host_step else e2e_step_overlapped)(a)
         b.record(stream)
     torch.cuda.synchronize()
     cp.check(cp.cpattn_check())
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev2), world, dev)
     # the end-to-end outputs are the device step's, bit for bit (the same calls on the
-    # same inputs; with head halves, independent problems with the same per-tile
-    # arithmetic)
+    # same inputs; in halves, independent problems with the same per-tile arithmetic)
     e2e_out = [x.clone() for x in host_out]
     step()
     torch.cuda.synchronize()
     if not all(torch.equal(a_, b_.cpu()) for a_, b_ in zip(e2e_out, outs)):
         raise RuntimeError("end-to-end outputs differ from the device-resident step's")
+    if host_step:
+        d_lse = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, 1, w.cp, w.layout, "f32")
+        lse_nat = torch.empty_like(lse)
+        cp.check(cp.cpattn_layout(inv_perm, d_lse, lse, lse_nat, w.H_q))
+        if not torch.equal(h_lse, lse_nat.cpu()):
+            raise RuntimeError("end-to-end LSE differs from the device-resident step's")
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "transfers": ("pinned host buffers on side streams inside each step's events; the "
-                         "heads split into two halves, each half a library call of its own, so "
-                         "uploads and downloads of one half overlap the other half's compute"
-                         if chunked else
+           "transfers": ("one cpattn_ring_step_host call per step on pinned host buffers: the "
+                         "library splits the problem into independent halves and overlaps one "
+                         "half's uploads and downloads with the other's compute on its own "
+                         "copy streams, all inside each step's events"
+                         if host_step else
                          "pinned host buffers (the ranks' token shards for the a2a layout); dO "
                          "upload overlaps the forward and o download overlaps the backward on "
                          "side streams inside each step's events")}

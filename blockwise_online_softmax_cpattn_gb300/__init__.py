@@ -75,6 +75,9 @@ _sigs = {
                               _vp, _vp, ctypes.c_size_t, _vp]),
     "cpattn_ring_bwd_noalloc": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp, _vp, _vp,
                                       _vp, _vp, _vp, _vp]),
+    "cpattn_ring_step_host_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
+    "cpattn_ring_step_host": (_st, [ctypes.POINTER(CpattnDesc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "cpattn_packed_workspace": (ctypes.c_size_t, [ctypes.POINTER(CpattnDesc)]),
     "cpattn_ring_fwd_packed": (_st, [ctypes.POINTER(CpattnDesc), _vp, ctypes.c_int, _vp, _vp, _vp,
                                      _vp, _vp, _vp, ctypes.c_size_t, _vp]),
@@ -183,6 +186,21 @@ def cpattn_ring_bwd_noalloc(desc, q, k, v, o, lse, dO, dq, dk, dv, stream=None) 
     return _lib.cpattn_ring_bwd_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                         _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
                                         _stream(stream))
+
+
+def cpattn_ring_step_host_workspace(desc) -> int:
+    return _lib.cpattn_ring_step_host_workspace(ctypes.byref(desc))
+
+
+def cpattn_ring_step_host(desc, q, k, v, dO, o, lse, dq, dk, dv, workspace, ws_bytes=None,
+                          stream=None) -> int:
+    """One fwd+bwd step over HOST tensors (natural order; pinned for overlap): uploads,
+    permutes, ring forward and backward, permutes back and downloads, the transfers
+    overlapping the compute."""
+    return _lib.cpattn_ring_step_host(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(dO),
+                                      _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      _ptr(workspace), _ws_bytes(workspace, ws_bytes),
+                                      _stream(stream))
 
 
 def cpattn_packed_workspace(desc) -> int:

@@ -241,6 +241,36 @@ cpattn_status cpattn_ring_bwd_noalloc(const cpattn_desc* desc, const void* q, co
                                       void* stream);
 
 /*
+ * One forward + backward step over tensors in HOST memory, with the transfers
+ * overlapping the compute.  The pages put no host transfer on the path; this call
+ * is the library's own form of what a caller whose tensors live on the host does
+ * each step (upload, permute to layout order, cpattn_ring_fwd, cpattn_ring_bwd,
+ * permute back, download), so that the copies hide behind the kernels instead of
+ * adding to them.  The problem is cut into two independent halves when it splits
+ * evenly (batch rows when B is even, else the K/V heads with their query heads when
+ * B = 1 and H_kv is even): one half's uploads run while the other computes, and its
+ * results download while the next work runs, on two copy streams the library
+ * creates once per device; calls on one device share them.
+ *   q, k, v, dO       : HOST, natural token order, [B, H, T, D] in desc->dtype
+ *   o, dq, dk, dv     : HOST, natural token order, same shapes
+ *   lse               : HOST, [B, H_q, T] float32, natural order
+ *   workspace         : device memory, 256-byte aligned, at least
+ *                       cpattn_ring_step_host_workspace(desc) bytes (staging, the
+ *                       layout-order tensors and the backward's statistics)
+ * Host buffers should be page-locked (cudaHostAlloc); pageable memory works but its
+ * copies do not overlap.  The call returns after enqueueing; the host outputs are
+ * complete when `stream`'s work is (for example after cpattn_check(stream)).
+ * Errors: desc->a2a != 1 -> CPATTN_ERR_UNSUPPORTED; a null pointer, a misaligned or
+ * too small workspace -> CPATTN_ERR_INVALID_ARG, before anything is enqueued;
+ * others as cpattn_ring_fwd / cpattn_ring_bwd.
+ */
+size_t cpattn_ring_step_host_workspace(const cpattn_desc* desc);
+cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const void* q, const void* k,
+                                    const void* v, const void* dO, void* o, float* lse, void* dq,
+                                    void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                    void* stream);
+
+/*
  * Packed sequences (transformers pull request #50497: the packed variant restarts
  * the position ids mid-sequence and the mask is rebuilt for the documents; the
  * InfiniTrain pull request #181 leaves packed / variable-length sequences out).

@@ -175,3 +175,19 @@ def test_partial_bwd_arguments_are_checked(cp):
     assert cp.cpattn_partial_bwd(d, 0, 1, *args, 2, FAKE, need, 0) == 1       # accumulate
     assert cp.cpattn_partial_bwd(d, 0, 1, *args, 1, FAKE, need - 1, 0) == 1   # workspace
     assert cp.cpattn_partial_bwd(d, 0, 1, *args[:6], 0, 0, FAKE, need, 0) == 1  # null dv_part
+
+
+def test_host_step_arguments_are_checked(cp):
+    d = _desc(cp)
+    need = cp.cpattn_ring_step_host_workspace(d)
+    # staging of q, k, v, dO; layout-order q, k, v, dO, o, LSE, dq, dk, dv; the
+    # natural-order LSE; the backward's statistics of one half
+    q, k, lse = 1 * 4 * 512 * 64 * 2, 1 * 2 * 512 * 64 * 2, 1 * 4 * 512 * 4
+    assert need >= 6 * q + 6 * k + 2 * lse and need % 256 == 0
+    assert cp.cpattn_ring_step_host_workspace(_desc(cp, a2a=2, cp=4, T=512)) == 0
+    h = [FAKE] * 9
+    assert cp.cpattn_ring_step_host(_desc(cp, a2a=2, cp=4, T=512), *h, FAKE, need, 0) == 2
+    assert cp.cpattn_ring_step_host(d, *h, FAKE, need - 1, 0) == 1           # workspace size
+    assert cp.cpattn_ring_step_host(d, *h, FAKE + 16, need, 0) == 1          # 256-byte alignment
+    assert cp.cpattn_ring_step_host(d, *h[:8], 0, FAKE, need, 0) == 1        # null dv
+    assert cp.cpattn_ring_step_host(_desc(cp, H_q=3), *h, FAKE, need, 0) == 1

@@ -61,9 +61,11 @@ def test_bench_ring_gpt2():
     out = _bench("--workload", "gpt2_small_T1024")
     _check_contract(out, "tc_")
     assert out["config"]["workload"] == "gpt2_small_T1024"
-    # B4 H12 T1024 D64: q, k, v, dO in and o, dk, dv, dq out, bf16
+    # B4 H12 T1024 D64: q, k, v, dO in and o, dk, dv, dq (bf16) and the LSE (float32)
+    # out, through one cpattn_ring_step_host call per step
     assert out["e2e"]["h2d_bytes_per_step"] == 4 * 4 * 12 * 1024 * 64 * 2
-    assert out["e2e"]["d2h_bytes_per_step"] == 4 * 4 * 12 * 1024 * 64 * 2
+    assert out["e2e"]["d2h_bytes_per_step"] == 4 * 4 * 12 * 1024 * 64 * 2 + 4 * 12 * 1024 * 4
+    assert out["e2e"]["transfers"].startswith("one cpattn_ring_step_host call")
 
 
 def test_bench_allgather_gpt2():
