@@ -218,7 +218,7 @@ def kernel_flops_or_bytes(name, w, pairs=None):
         return "tensor", 2.0 * w.D * pairs / w.cp
     if name == "bwd_prepass":
         return "hbm", 2.0 * rows_q * w.D * elt + 12.0 * rows_q
-    if name == "layout_zigzag_batch":
+    if name in ("layout_zigzag_batch", "layout_a2a_batch"):
         # one launch permutes a step's four inputs (q, k, v, dO) or its four outputs
         # (o, dk, dv, dq): each read once and written once
         return "hbm", 2.0 * (2 * rows_q + 2 * rows_kv) * w.D * elt

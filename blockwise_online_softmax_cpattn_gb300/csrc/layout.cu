@@ -107,6 +107,67 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(PermuteDev p, const in
   }
 }
 
+// Row gathers of several tensors (same kind, row size and token count; head
+// counts of their own) in one launch: rows [first[i], first[i + 1]) of the launch
+// are tensor i's.
+struct RowBatch {
+  const int4* src[kMaxBatch];
+  int4* dst[kMaxBatch];
+  int64_t first[kMaxBatch + 1];
+  int H[kMaxBatch];
+  int n;
+};
+
+template <int VPT>
+__global__ void __launch_bounds__(256) gather_rows_batch_kernel(PermuteDev p, RowBatch jobs) {
+  constexpr int vpr = kRowGroup * VPT;
+  const int lg = threadIdx.x % kRowGroup;
+  const int64_t rows = jobs.first[jobs.n];
+  const int64_t grp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kRowGroup;
+  const int64_t ngrp = (int64_t)gridDim.x * blockDim.x / kRowGroup;
+  for (int64_t r0 = grp; r0 < rows; r0 += ngrp * kRowsInFlight) {
+    int4 v[kRowsInFlight][VPT];
+    int4* d[kRowsInFlight];
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      const int64_t row = r0 + u * ngrp;
+      d[u] = nullptr;
+      if (row < rows) {
+        int ti = 0;  // the tensor this row belongs to
+        while (ti + 1 < jobs.n && row >= jobs.first[ti + 1]) ++ti;
+        const int64_t local = row - jobs.first[ti];
+        PermuteDev q = p;
+        q.H = jobs.H[ti];
+        q.Hs = q.H / p.a2a;
+        const int4* s = jobs.src[ti] + permute_src_row(q, local) * vpr + lg;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) v[u][i] = __ldcs(s + i * kRowGroup);
+        d[u] = jobs.dst[ti] + local * vpr + lg;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      if (d[u] != nullptr) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) __stcs(d[u] + i * kRowGroup, v[u][i]);
+      }
+    }
+  }
+}
+
+template <int VPT>
+static cudaError_t run_rows_batch(const PermuteDev& p, const RowBatch& jobs, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t rows = jobs.first[jobs.n];
+  int64_t blocks = (rows * kRowGroup + 255) / 256;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  if (blocks < 1) blocks = 1;
+  gather_rows_batch_kernel<VPT><<<(unsigned)blocks, 256, 0, st>>>(p, jobs);
+  return cudaGetLastError();
+}
+
 template <int VPT>
 static cudaError_t run_rows(const PermuteDev& p, const void* src, void* dst, int64_t rows,
                             cudaStream_t st) {
@@ -265,10 +326,41 @@ cudaError_t launch_permute_batch(const PermuteArgs& a, int n, const void* const*
                                  void* const* dst, const int* n_heads, cudaStream_t st) {
   const int row_bytes = a.D * a.elt;
   const int nchunk = a.zz ? 2 * (a.cp / a.a2a) : a.cp / a.a2a;
-  bool chunks = a.kind <= kZigzagInv && row_bytes % 16 == 0 && a.T % nchunk == 0 &&
-                n <= kMaxBatch;
-  for (int i = 0; i < n && chunks; ++i)
-    chunks = (((uintptr_t)src[i] | (uintptr_t)dst[i]) % 16) == 0;
+  bool aligned = n <= kMaxBatch;
+  for (int i = 0; i < n && aligned; ++i)
+    aligned = (((uintptr_t)src[i] | (uintptr_t)dst[i]) % 16) == 0;
+  const bool chunks = aligned && a.kind <= kZigzagInv && row_bytes % 16 == 0 && a.T % nchunk == 0;
+  const int vpr = row_bytes / 16;
+  const bool gathers = aligned && a.kind >= kA2AFwd && row_bytes % 16 == 0 &&
+                       (vpr == 8 || vpr == 16 || vpr == 32);
+  if (gathers) {
+    // the a2a re-layouts of all the tensors as one launch of row gathers
+    PermuteDev p;
+    p.kind = a.kind;
+    p.B = a.B;
+    p.T = a.T;
+    p.a2a = a.a2a;
+    p.c_src = a.T / a.cp;
+    p.ring = SeqMap::make(a.T, a.cp / a.a2a, a.zz);
+    p.shard = SeqMap::make(a.T, a.cp, a.zz);
+    p.H = n_heads[0];
+    p.Hs = p.H / a.a2a;
+    RowBatch jobs;
+    jobs.n = n;
+    jobs.first[0] = 0;
+    for (int i = 0; i < n; ++i) {
+      jobs.src[i] = static_cast<const int4*>(src[i]);
+      jobs.dst[i] = static_cast<int4*>(dst[i]);
+      jobs.H[i] = n_heads[i];
+      jobs.first[i + 1] = jobs.first[i] + (int64_t)a.B * n_heads[i] * a.T;
+    }
+    timing_begin("layout_a2a_batch", st);
+    cudaError_t e = vpr == 16 ? run_rows_batch<2>(p, jobs, st)
+                    : vpr == 8 ? run_rows_batch<1>(p, jobs, st)
+                               : run_rows_batch<4>(p, jobs, st);
+    timing_end(st);
+    return e;
+  }
   if (!chunks) {
     for (int i = 0; i < n; ++i) {
       PermuteArgs ai = a;

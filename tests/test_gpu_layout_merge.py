@@ -66,6 +66,33 @@ def test_layout_batch_equals_single_permutes(kind, dtype, layout, B, Hq, Hkv, T,
     cp.check(cp.cpattn_check())
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,T,D,cp_,a2a,dtype", [
+    (1, 32, 8, 8192, 128, 8, 8, torch.bfloat16),   # the full-Ulysses step's four tensors
+    (2, 8, 4, 1024, 64, 4, 2, torch.bfloat16),
+    (1, 8, 2, 512, 128, 4, 2, torch.float32),      # 512-byte rows
+    (1, 6, 3, 96, 24, 6, 3, torch.float32)])       # 96-byte rows: per-tensor launches
+def test_a2a_layout_batch_equals_single_permutes(B, Hq, Hkv, T, D, cp_, a2a, dtype):
+    """cpattn_layout_batch of the all-to-all re-layout (one launch of row gathers)
+    equals cpattn_layout on each tensor, bit for bit, both ways."""
+    cp = cp_mod()
+    g = torch.Generator().manual_seed(17)
+    dt = "bf16" if dtype == torch.bfloat16 else "f32"
+    heads = [Hq, Hkv, Hkv, Hq]
+    d = cp.make_desc(B, Hq, Hkv, T, D, cp_, "zigzag", dt, a2a=a2a)
+    shards = [torch.randn(B * T * h * D, generator=g).to(dtype).to(dev()) for h in heads]
+    got = [torch.empty_like(x) for x in shards]
+    cp.check(cp.cpattn_layout_batch(cp.A2A_FWD, d, shards, got, heads))
+    for x, y, h in zip(shards, got, heads):
+        one = torch.empty_like(x)
+        cp.check(cp.cpattn_layout(cp.A2A_FWD, d, x, one, h))
+        assert torch.equal(_bits(y), _bits(one))
+    back = [torch.empty_like(x) for x in shards]
+    cp.check(cp.cpattn_layout_batch(cp.A2A_INV, d, got, back, heads))
+    for x, y in zip(shards, back):
+        assert torch.equal(_bits(y), _bits(x))
+    cp.check(cp.cpattn_check())
+
+
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 @pytest.mark.parametrize("B,H,T,D,cp_,a2a", [(1, 8, 256, 64, 8, 2), (2, 4, 128, 32, 4, 2),
                                              (1, 6, 96, 16, 6, 3), (1, 32, 32768, 128, 8, 2),
