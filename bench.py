@@ -909,6 +909,20 @@ def run_hbm(args):
                timed(lambda: cp.check(cp.cpattn_layout(cp.ZIGZAG_FWD, d, x, y, h))),
                f"cpattn_layout ZIGZAG_FWD of the {tag} tensor of {w.name} ({n / 1e6:.1f} MB)")
         del x, y
+    # the batched permutes a step launches: the four tensors q, k, v, dO in one call
+    for label, w, perm, tag in ((("zigzag_batch_llama", W.LLAMA, cp.ZIGZAG_FWD, "zigzag"),
+                                 ("a2a_batch_ulysses", W.ULYSSES, cp.A2A_FWD, "a2a"))):
+        d = cp.make_desc(w.B, w.H_q, w.H_kv, w.T, w.D, w.cp, w.layout, w.dtype, a2a=w.a2a)
+        heads = [w.H_q, w.H_kv, w.H_kv, w.H_q]
+        xs = [torch.randn(w.B * h * w.T * w.D, generator=g).to(torch.bfloat16).to(dev)
+              for h in heads]
+        ys = [torch.empty_like(x) for x in xs]
+        n = sum(x.numel() * 2 for x in xs)
+        record(label, 2 * n,
+               timed(lambda: cp.check(cp.cpattn_layout_batch(perm, d, xs, ys, heads))),
+               f"cpattn_layout_batch of the {tag} permutes of a {w.name} step's q, k, v, dO "
+               f"({n / 1e6:.1f} MB) in one launch")
+        del xs, ys
     return {"metric": "HBM-bound kernels: GB/s of algorithmic bytes per launch", "unit": "GB/s",
             "n_gpus": 1, "higher_is_better": True, "data": "synthetic",
             "peak": pk["hbm_gbs"], "peak_source": f"{src_pk} copy bandwidth",
