@@ -137,6 +137,28 @@ class DistExchange:
         return recv
 
 
+class HostExchange(DistExchange):
+    """The same exchange staged through host memory, for process groups whose backend
+    moves host tensors only (gloo): each outgoing device tensor is copied to the
+    host (which waits for the work that produced it), sent, and received into host
+    buffers that are copied to the device on wait.  No transfer overlaps compute."""
+
+    def start(self, send: Sequence, recv: Sequence):
+        host_send = [t.detach().to("cpu") for t in send]
+        host_recv = [t.new_empty(t.shape, device="cpu") for t in recv]
+        reqs, _ = super().start(host_send, host_recv)
+        return reqs, (host_send, host_recv, list(recv))
+
+    @staticmethod
+    def wait(handle):
+        reqs, (_, host_recv, recv) = handle
+        for r in reqs:
+            r.wait()
+        for dst, src in zip(recv, host_recv):
+            dst.copy_(src)
+        return recv
+
+
 def ring_forward(steps, exch, q, k, v):
     """Rank exch.rank's forward over a ring of exch.world ranks.  q, k, v are the
     rank's own chunks ([B, H, c, D], layout order); returns its (O, LSE) rows and
@@ -299,6 +321,6 @@ def rank_chunks(x, cp: int) -> list:
     return [x[:, :, r * c:(r + 1) * c].contiguous() for r in range(cp)]
 
 
-__all__ = ["ring_source", "next_rank", "prev_rank", "DistExchange", "ring_forward",
+__all__ = ["ring_source", "next_rank", "prev_rank", "DistExchange", "HostExchange", "ring_forward",
            "ring_backward", "emulate_ring_forward", "emulate_ring_backward", "LibrarySteps",
            "rank_chunks"]

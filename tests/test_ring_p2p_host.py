@@ -126,7 +126,7 @@ def _port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, layout, out):
+def _worker(rank, world, port, layout, out, exchange="dist"):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
@@ -136,7 +136,7 @@ def _worker(rank, world, port, layout, out):
         c = lay[0].shape[2] // world
         mine = [torch.from_numpy(np.ascontiguousarray(x[:, :, rank * c:(rank + 1) * c]))
                 for x in lay]
-        exch = R.DistExchange()
+        exch = R.DistExchange() if exchange == "dist" else R.HostExchange()
         o, lse, held_f = R.ring_forward(steps, exch, mine[0], mine[1], mine[2])
         dq, dk, dv, held_b = R.ring_backward(steps, exch, mine[0], mine[1], mine[2], o, lse,
                                              mine[3])
@@ -166,12 +166,14 @@ def _check_rank(world, layout, res, nat, pos):
     assert rel_err(gdv, dv[:, :, p]) < 1e-12, ("dv home", r)
 
 
-@pytest.mark.parametrize("world,layout", [(2, "zigzag"), (3, "contiguous"), (4, "zigzag")])
-def test_ring_over_gloo_ranks(world, layout):
+@pytest.mark.parametrize("world,layout,exchange", [(2, "zigzag", "dist"), (3, "contiguous", "dist"),
+                                                   (4, "zigzag", "dist"), (3, "zigzag", "host")])
+def test_ring_over_gloo_ranks(world, layout, exchange):
     ctx = mp.get_context("spawn")
     out = ctx.Queue()
     port = _port()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, layout, out)) for r in range(world)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, layout, out, exchange))
+             for r in range(world)]
     for p in procs:
         p.start()
     results = [out.get(timeout=180) for _ in range(world)]
