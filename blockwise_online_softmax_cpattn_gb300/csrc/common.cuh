@@ -80,15 +80,36 @@ struct TileWalk {
     return w < h ? s * h + w : (2 * cp - 1 - s) * h + (w - h);
   }
   __device__ __forceinline__ void next() {
-    if (++t == tpc) {
-      t = 0;
-      if (++rep == reps) {
-        rep = 0;
-        ++i;
-        s += dir;
-        if (s < 0) s += cp;
-        else if (s >= cp) s -= cp;
-      }
+    if (++t == tpc) end_pass();
+  }
+  // The next pass over this chunk's tiles, or the next chunk after the last pass.
+  __device__ __forceinline__ void end_pass() {
+    t = 0;
+    if (++rep == reps) {
+      rep = 0;
+      ++i;
+      s += dir;
+      if (s < 0) s += cp;
+      else if (s >= cp) s -= cp;
+    }
+  }
+  // The next chunk, whatever pass this is.
+  __device__ __forceinline__ void end_chunk() {
+    rep = reps - 1;
+    end_pass();
+  }
+
+  // Query-stationary walks over key tiles: move to the next key tile that the
+  // query tile at q0 sees (a key tile is hidden when its first position is past
+  // the query tile's last row).  Inside a chunk the tile positions grow with t (in
+  // the zigzag layout the late half follows the early one), so the visible key
+  // tiles of a chunk are a prefix: the first hidden tile ends the pass, and a chunk
+  // whose first tile is hidden is left at once.  The tiles visited, and their
+  // order, are those of stepping through every tile and skipping the hidden ones.
+  __device__ __forceinline__ void settle_keys(int q0) {
+    while (!done() && pos() > q0 + 127) {
+      if (t == 0) end_chunk();  // the chunk's first tile is hidden: all of it is
+      else end_pass();          // the rest of this pass is hidden
     }
   }
 };

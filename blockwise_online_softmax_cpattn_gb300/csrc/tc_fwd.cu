@@ -251,12 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.start(p.m, doc_row(it)[it.pos0] >> 7, it.pos0 >> 7, 1);
     } else {
       w.start(p.m, one_chunk ? p.kv_rank : it.rank, one_chunk ? 1 : p.m.cp, -1, 1);
-      while (!w.done() && classify(it.pos0, w.pos(), nullptr) == kEmpty) w.next();
+      w.settle_keys(it.pos0);
     }
   };
   auto walk_next = [&](Walk& w, const Item& it) {
-    if constexpr (PK) w.next();
-    else do w.next(); while (!w.done() && classify(it.pos0, w.pos(), nullptr) == kEmpty);
+    w.next();
+    if constexpr (!PK) w.settle_keys(it.pos0);
   };
 
   if (warp < 4) {
