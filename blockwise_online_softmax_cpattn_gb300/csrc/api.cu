@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "../../include/cpattn.h"
+#include "api_internal.h"
 #include "kernels.h"
 
 // Device status word (one per device that loads the library): the first error a
@@ -219,6 +220,17 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
                               const void* v, const void* o, const float* lse, const void* dO,
                               void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                               void* stream) {
+  return cpattn::ring_bwd_after_dkdv(desc, q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes,
+                                     stream, nullptr);
+}
+
+}  // extern "C"
+
+cpattn_status cpattn::ring_bwd_after_dkdv(const cpattn_desc* desc, const void* q, const void* k,
+                                          const void* v, const void* o, const float* lse,
+                                          const void* dO, void* dq, void* dk, void* dv,
+                                          void* workspace, size_t ws_bytes, void* stream,
+                                          const AfterDkdv* after) {
   Ring R;
   cpattn_status s = validate(desc, &R);
   if (s != CPATTN_OK) return s;
@@ -236,11 +248,16 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
   cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   if (tc)
-    return from_cuda(launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st));
+    return from_cuda(launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st,
+                                   nullptr, nullptr, nullptr, nullptr, after));
   e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  return from_cuda(launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st));
+  e = launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st);
+  if (e == cudaSuccess && after != nullptr && after->fn != nullptr) e = after->fn(after->ctx, st);
+  return from_cuda(e);
 }
+
+extern "C" {
 
 // ---------------------------------------------------------------------------
 // packed sequences

@@ -1,34 +1,42 @@
 // cpattn_ring_step_host: one forward + backward step of the ring over tensors that
 // live in host memory, with the host<->device transfers overlapping the compute.
 //
-// The problem splits into n independent groups: batch rows when B is even, else
-// (B = 1) K/V heads with their query heads when H_kv is even.  Group j of every
-// tensor is the j-th contiguous n-th of it, so each group is a smaller problem of
-// the same kind.  Two copy streams per device, created once, carry the transfers:
+// The problem splits into independent groups: batch rows, or K/V heads with their
+// query heads.  Group j of n of every tensor is its j-th contiguous n-th, so each
+// group is a smaller problem of the same kind.  The backward runs in nb groups (two
+// when the problem splits so), the forward in nf = 2 nb groups when it splits that
+// far (the forward's kernels lose little on a quarter of the problem, the
+// backward's dK/dV kernel would), so backward group j covers forward groups 2j and
+// 2j + 1.  Two copy streams per device, created once, carry the transfers:
 //
-//   upload stream    q, k, v of group 0, 1, ...; then dO of group 0, 1, ...
-//   caller's stream  per group: permute q, k, v to layout order, ring forward,
-//                    permute o and LSE back; then per group: permute dO, ring
-//                    backward, permute dq, dk, dv back
-//   download stream  o and LSE of a group as soon as its forward is done; dq, dk,
-//                    dv of a group as soon as its backward is done
+//   upload stream    q, k, v of forward group 2j, of 2j + 1, then dO of backward
+//                    group j; then the same for j + 1
+//   caller's stream  per backward group j: for its forward groups, permute q, k, v
+//                    to layout order, ring forward, permute o and LSE back; then
+//                    permute dO, ring backward with dk and dv permuted back between
+//                    its dK/dV and dQ kernels, permute dq back
+//   download stream  o and LSE of a forward group as soon as it is done; dk and dv
+//                    of a backward group while its dQ kernel runs; dq once its
+//                    backward is done
 //
-// so a group's uploads run while the previous group computes, and its downloads
-// while the next one does.  The caller's stream waits for the last download, so
-// the call's work is complete when that stream's work is.
+// so the first kernel waits only for the first forward group's inputs, uploads
+// run while earlier groups compute, downloads while later ones do, and only the
+// last group's dq is left to download after the last kernel.  The caller's stream
+// waits for the last download, so the call's work is complete when that stream's
+// work is.
 #include <mutex>
 
 #include "../../include/cpattn.h"
+#include "api_internal.h"
 #include "kernels.h"
 
 namespace cpattn {
 namespace {
 
-constexpr int kMaxGroups = 2;
-// events per device: start, end, and per group: inputs landed, dO landed, forward
-// outputs ready, gradients ready
-constexpr int kEventsPerGroup = 4;
-constexpr int kNumEvents = 2 + kEventsPerGroup * kMaxGroups;
+constexpr int kMaxBwdGroups = 2, kMaxFwdGroups = 2 * kMaxBwdGroups;
+// events per device: start, end; per forward group: inputs landed, outputs ready;
+// per backward group: dO landed, dk and dv ready, dq ready
+constexpr int kNumEvents = 2 + 2 * kMaxFwdGroups + 3 * kMaxBwdGroups;
 
 struct CopyStreams {
   cudaStream_t up = nullptr, down = nullptr;
@@ -68,15 +76,23 @@ struct StepLayout {
   size_t nat_lse, bwd_ws, total;
 };
 
-// Two groups when the problem splits into independent halves whose slices of every
-// tensor (q, k, the LSE) start on 16-byte boundaries; else one.
-int groups_of(const cpattn_desc* d) {
-  if (!(d->B % 2 == 0 || (d->B == 1 && d->H_kv % 2 == 0))) return 1;
+// Whether the j-th contiguous n-th of every tensor is an independent problem of the
+// same kind (n divides B, or each batch row splits into n / B groups of K/V heads)
+// whose slices of q, k and the LSE start on 16-byte boundaries.
+bool splits(const cpattn_desc* d, int n) {
+  if (n == 1) return true;
+  if (!(d->B % n == 0 || (n % d->B == 0 && d->H_kv % (n / d->B) == 0))) return false;
   const size_t elt = d->dtype == CPATTN_BF16 ? 2 : 4;
-  const size_t q = (size_t)d->B * d->H_q * d->T * d->D * elt / 2;
-  const size_t k = (size_t)d->B * d->H_kv * d->T * d->D * elt / 2;
-  const size_t l = (size_t)d->B * d->H_q * d->T * sizeof(float) / 2;
-  return q % 16 == 0 && k % 16 == 0 && l % 16 == 0 ? 2 : 1;
+  const size_t q = (size_t)d->B * d->H_q * d->T * d->D * elt / n;
+  const size_t k = (size_t)d->B * d->H_kv * d->T * d->D * elt / n;
+  const size_t l = (size_t)d->B * d->H_q * d->T * sizeof(float) / n;
+  return q % 16 == 0 && k % 16 == 0 && l % 16 == 0;
+}
+
+int bwd_groups(const cpattn_desc* d) { return splits(d, 2) ? 2 : 1; }
+int fwd_groups(const cpattn_desc* d) {
+  const int nb = bwd_groups(d);
+  return splits(d, 2 * nb) ? 2 * nb : nb;
 }
 
 cpattn_desc group_desc(const cpattn_desc* d, int n) {
@@ -85,8 +101,10 @@ cpattn_desc group_desc(const cpattn_desc* d, int n) {
     if (d->B % n == 0) {
       g.B = d->B / n;
     } else {
-      g.H_q = d->H_q / n;
-      g.H_kv = d->H_kv / n;
+      const int m = n / d->B;  // groups per batch row
+      g.B = 1;
+      g.H_q = d->H_q / m;
+      g.H_kv = d->H_kv / m;
     }
   }
   return g;
@@ -98,7 +116,7 @@ StepLayout layout_of(const cpattn_desc* d) {
   s.q = round256((size_t)d->B * d->H_q * d->T * d->D * elt);
   s.kv = round256((size_t)d->B * d->H_kv * d->T * d->D * elt);
   s.lse = round256((size_t)d->B * d->H_q * d->T * sizeof(float));
-  const cpattn_desc g = group_desc(d, groups_of(d));
+  const cpattn_desc g = group_desc(d, bwd_groups(d));
   s.bwd = round256(cpattn_ring_bwd_workspace(&g));
   size_t off = 0;
   auto take = [&](size_t b) {
@@ -123,6 +141,23 @@ StepLayout layout_of(const cpattn_desc* d) {
   s.bwd_ws = take(s.bwd);
   s.total = off;
   return s;
+}
+
+// Queued by the backward between its dK/dV and dQ kernels: dk and dv back to
+// natural order, then the event the download stream waits for.
+struct DkdvOut {
+  const cpattn_desc* gd;
+  const void* src[2];
+  void* dst[2];
+  int heads[2];
+  cudaEvent_t done;
+};
+
+cudaError_t dkdv_out(void* ctx, cudaStream_t st) {
+  DkdvOut* d = static_cast<DkdvOut*>(ctx);
+  if (cpattn_layout_batch(CPATTN_ZIGZAG_INV, d->gd, 2, d->src, d->dst, d->heads, st) != CPATTN_OK)
+    return cudaErrorLaunchFailure;
+  return cudaEventRecord(d->done, st);
 }
 
 }  // namespace
@@ -153,16 +188,19 @@ extern "C" cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const vo
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
 
-  const int n = groups_of(desc);
-  const cpattn_desc gd = group_desc(desc, n);
-  cpattn_desc gd_lse = gd;  // the LSE permuted as rows of one float32
-  gd_lse.D = 1;
-  gd_lse.dtype = CPATTN_F32;
+  const int nb = bwd_groups(desc), nf = fwd_groups(desc), r = nf / nb;
+  const cpattn_desc gb = group_desc(desc, nb), gf = group_desc(desc, nf);
+  cpattn_desc gf_lse = gf;  // the LSE permuted as rows of one float32
+  gf_lse.D = 1;
+  gf_lse.dtype = CPATTN_F32;
   char* w = static_cast<char*>(workspace);
   const size_t elt = desc->dtype == CPATTN_BF16 ? 2 : 4;
-  const size_t qb = (size_t)desc->B * desc->H_q * desc->T * desc->D * elt / n;   // per group
-  const size_t kb = (size_t)desc->B * desc->H_kv * desc->T * desc->D * elt / n;
-  const size_t lb = (size_t)desc->B * desc->H_q * desc->T * sizeof(float) / n;
+  const size_t q_all = (size_t)desc->B * desc->H_q * desc->T * desc->D * elt;
+  const size_t k_all = (size_t)desc->B * desc->H_kv * desc->T * desc->D * elt;
+  const size_t l_all = (size_t)desc->B * desc->H_q * desc->T * sizeof(float);
+  // bytes of one group's slice: backward groups (b) and forward groups (f)
+  const size_t qb = q_all / nb, kb = k_all / nb, lb = l_all / nb;
+  const size_t qf = q_all / nf, kf = k_all / nf, lf = l_all / nf;
   auto dev_at = [&](size_t section, int j, size_t per) { return w + section + j * per; };
   auto host_at = [&](const void* p, int j, size_t per) {
     return static_cast<const char*>(p) + j * per;
@@ -170,11 +208,11 @@ extern "C" cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const vo
   auto host_out = [&](void* p, int j, size_t per) { return static_cast<char*>(p) + j * per; };
   cudaEvent_t* ev = cs->ev;
   cudaEvent_t ev_start = ev[0], ev_end = ev[1];
-  auto ev_in = [&](int j) { return ev[2 + kEventsPerGroup * j]; };
-  auto ev_do = [&](int j) { return ev[3 + kEventsPerGroup * j]; };
-  auto ev_fwd = [&](int j) { return ev[4 + kEventsPerGroup * j]; };
-  auto ev_grad = [&](int j) { return ev[5 + kEventsPerGroup * j]; };
-  const int Hq = gd.H_q, Hkv = gd.H_kv;
+  auto ev_in = [&](int f) { return ev[2 + f]; };                  // forward group f
+  auto ev_fwd = [&](int f) { return ev[2 + kMaxFwdGroups + f]; };
+  auto ev_do = [&](int j) { return ev[2 + 2 * kMaxFwdGroups + j]; };  // backward group j
+  auto ev_dkdv = [&](int j) { return ev[2 + 2 * kMaxFwdGroups + kMaxBwdGroups + j]; };
+  auto ev_grad = [&](int j) { return ev[2 + 2 * kMaxFwdGroups + 2 * kMaxBwdGroups + j]; };
 
 #define CPATTN_TRY(x)                         \
   do {                                        \
@@ -190,70 +228,77 @@ extern "C" cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const vo
   CPATTN_TRY(cudaEventRecord(ev_start, st));
   CPATTN_TRY(cudaStreamWaitEvent(cs->up, ev_start, 0));
   CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_start, 0));
-  // uploads: q, k, v of every group, then dO of every group
-  for (int j = 0; j < n; ++j) {
-    CPATTN_TRY(cudaMemcpyAsync(dev_at(L.stage_q, j, qb), host_at(q, j, qb), qb,
-                               cudaMemcpyHostToDevice, cs->up));
-    CPATTN_TRY(cudaMemcpyAsync(dev_at(L.stage_k, j, kb), host_at(k, j, kb), kb,
-                               cudaMemcpyHostToDevice, cs->up));
-    CPATTN_TRY(cudaMemcpyAsync(dev_at(L.stage_v, j, kb), host_at(v, j, kb), kb,
-                               cudaMemcpyHostToDevice, cs->up));
-    CPATTN_TRY(cudaEventRecord(ev_in(j), cs->up));
-  }
-  for (int j = 0; j < n; ++j) {
+  // uploads in the order the groups use them
+  for (int j = 0; j < nb; ++j) {
+    for (int f = j * r; f < (j + 1) * r; ++f) {
+      CPATTN_TRY(cudaMemcpyAsync(dev_at(L.stage_q, f, qf), host_at(q, f, qf), qf,
+                                 cudaMemcpyHostToDevice, cs->up));
+      CPATTN_TRY(cudaMemcpyAsync(dev_at(L.stage_k, f, kf), host_at(k, f, kf), kf,
+                                 cudaMemcpyHostToDevice, cs->up));
+      CPATTN_TRY(cudaMemcpyAsync(dev_at(L.stage_v, f, kf), host_at(v, f, kf), kf,
+                                 cudaMemcpyHostToDevice, cs->up));
+      CPATTN_TRY(cudaEventRecord(ev_in(f), cs->up));
+    }
     CPATTN_TRY(cudaMemcpyAsync(dev_at(L.stage_do, j, qb), host_at(dO, j, qb), qb,
                                cudaMemcpyHostToDevice, cs->up));
     CPATTN_TRY(cudaEventRecord(ev_do(j), cs->up));
   }
-  // forward of every group; o and LSE go back to natural order and home
-  for (int j = 0; j < n; ++j) {
-    CPATTN_TRY(cudaStreamWaitEvent(st, ev_in(j), 0));
-    const void* src[3] = {dev_at(L.stage_q, j, qb), dev_at(L.stage_k, j, kb),
-                          dev_at(L.stage_v, j, kb)};
-    void* dst[3] = {dev_at(L.lay_q, j, qb), dev_at(L.lay_k, j, kb), dev_at(L.lay_v, j, kb)};
-    const int heads[3] = {Hq, Hkv, Hkv};
-    CPATTN_TRY_S(cpattn_layout_batch(CPATTN_ZIGZAG_FWD, &gd, 3, src, dst, heads, st));
-    float* lay_lse = reinterpret_cast<float*>(dev_at(L.lay_lse, j, lb));
-    CPATTN_TRY_S(cpattn_ring_fwd(&gd, dst[0], dst[1], dst[2], dev_at(L.lay_o, j, qb), lay_lse,
-                                 st));
-    // the natural-order o takes q's staging (q was permuted above, on this stream)
-    CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_INV, &gd, dev_at(L.lay_o, j, qb),
-                               dev_at(L.stage_q, j, qb), Hq, st));
-    CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_INV, &gd_lse, lay_lse, dev_at(L.nat_lse, j, lb), Hq,
-                               st));
-    CPATTN_TRY(cudaEventRecord(ev_fwd(j), st));
-    CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_fwd(j), 0));
-    CPATTN_TRY(cudaMemcpyAsync(host_out(o, j, qb), dev_at(L.stage_q, j, qb), qb,
-                               cudaMemcpyDeviceToHost, cs->down));
-    CPATTN_TRY(cudaMemcpyAsync(host_out(lse, j, lb), dev_at(L.nat_lse, j, lb), lb,
-                               cudaMemcpyDeviceToHost, cs->down));
-  }
-  // backward of every group; dq, dk, dv go back to natural order and home
-  for (int j = 0; j < n; ++j) {
+  for (int j = 0; j < nb; ++j) {
+    // forward of the group's forward groups; o and LSE go back to natural order and home
+    for (int f = j * r; f < (j + 1) * r; ++f) {
+      CPATTN_TRY(cudaStreamWaitEvent(st, ev_in(f), 0));
+      const void* src[3] = {dev_at(L.stage_q, f, qf), dev_at(L.stage_k, f, kf),
+                            dev_at(L.stage_v, f, kf)};
+      void* dst[3] = {dev_at(L.lay_q, f, qf), dev_at(L.lay_k, f, kf), dev_at(L.lay_v, f, kf)};
+      const int heads[3] = {gf.H_q, gf.H_kv, gf.H_kv};
+      CPATTN_TRY_S(cpattn_layout_batch(CPATTN_ZIGZAG_FWD, &gf, 3, src, dst, heads, st));
+      float* lay_lse = reinterpret_cast<float*>(dev_at(L.lay_lse, f, lf));
+      CPATTN_TRY_S(cpattn_ring_fwd(&gf, dst[0], dst[1], dst[2], dev_at(L.lay_o, f, qf), lay_lse,
+                                   st));
+      // the natural-order o takes q's staging (q was permuted above, on this stream)
+      CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_INV, &gf, dev_at(L.lay_o, f, qf),
+                                 dev_at(L.stage_q, f, qf), gf.H_q, st));
+      CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_INV, &gf_lse, lay_lse, dev_at(L.nat_lse, f, lf),
+                                 gf.H_q, st));
+      CPATTN_TRY(cudaEventRecord(ev_fwd(f), st));
+      CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_fwd(f), 0));
+      CPATTN_TRY(cudaMemcpyAsync(host_out(o, f, qf), dev_at(L.stage_q, f, qf), qf,
+                                 cudaMemcpyDeviceToHost, cs->down));
+      CPATTN_TRY(cudaMemcpyAsync(host_out(lse, f, lf), dev_at(L.nat_lse, f, lf), lf,
+                                 cudaMemcpyDeviceToHost, cs->down));
+    }
+    // backward (its layout-order q, k, v, o, LSE are those of its forward groups, end
+    // to end); natural-order dk and dv take the staging of k and v (read by the
+    // forward's permutes above), dq that of dO
     CPATTN_TRY(cudaStreamWaitEvent(st, ev_do(j), 0));
-    CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_FWD, &gd, dev_at(L.stage_do, j, qb),
-                               dev_at(L.lay_do, j, qb), Hq, st));
-    CPATTN_TRY_S(cpattn_ring_bwd(&gd, dev_at(L.lay_q, j, qb), dev_at(L.lay_k, j, kb),
-                                 dev_at(L.lay_v, j, kb), dev_at(L.lay_o, j, qb),
-                                 reinterpret_cast<float*>(dev_at(L.lay_lse, j, lb)),
-                                 dev_at(L.lay_do, j, qb), dev_at(L.lay_dq, j, qb),
-                                 dev_at(L.lay_dk, j, kb), dev_at(L.lay_dv, j, kb),
-                                 w + L.bwd_ws, L.bwd, st));
-    // natural-order dq, dk, dv take the staging of dO, k and v
-    const void* src[3] = {dev_at(L.lay_dq, j, qb), dev_at(L.lay_dk, j, kb),
-                          dev_at(L.lay_dv, j, kb)};
-    void* dst[3] = {dev_at(L.stage_do, j, qb), dev_at(L.stage_k, j, kb),
-                    dev_at(L.stage_v, j, kb)};
-    const int heads[3] = {Hq, Hkv, Hkv};
-    CPATTN_TRY_S(cpattn_layout_batch(CPATTN_ZIGZAG_INV, &gd, 3, src, dst, heads, st));
+    CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_FWD, &gb, dev_at(L.stage_do, j, qb),
+                               dev_at(L.lay_do, j, qb), gb.H_q, st));
+    DkdvOut out;
+    out.gd = &gb;
+    out.src[0] = dev_at(L.lay_dk, j, kb);
+    out.src[1] = dev_at(L.lay_dv, j, kb);
+    out.dst[0] = dev_at(L.stage_k, j, kb);
+    out.dst[1] = dev_at(L.stage_v, j, kb);
+    out.heads[0] = out.heads[1] = gb.H_kv;
+    out.done = ev_dkdv(j);
+    const AfterDkdv after{dkdv_out, &out};
+    CPATTN_TRY_S(ring_bwd_after_dkdv(&gb, dev_at(L.lay_q, j, qb), dev_at(L.lay_k, j, kb),
+                                     dev_at(L.lay_v, j, kb), dev_at(L.lay_o, j, qb),
+                                     reinterpret_cast<float*>(dev_at(L.lay_lse, j, lb)),
+                                     dev_at(L.lay_do, j, qb), dev_at(L.lay_dq, j, qb),
+                                     dev_at(L.lay_dk, j, kb), dev_at(L.lay_dv, j, kb),
+                                     w + L.bwd_ws, L.bwd, st, &after));
+    CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_dkdv(j), 0));
+    CPATTN_TRY(cudaMemcpyAsync(host_out(dk, j, kb), out.dst[0], kb, cudaMemcpyDeviceToHost,
+                               cs->down));
+    CPATTN_TRY(cudaMemcpyAsync(host_out(dv, j, kb), out.dst[1], kb, cudaMemcpyDeviceToHost,
+                               cs->down));
+    CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_INV, &gb, dev_at(L.lay_dq, j, qb),
+                               dev_at(L.stage_do, j, qb), gb.H_q, st));
     CPATTN_TRY(cudaEventRecord(ev_grad(j), st));
     CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_grad(j), 0));
-    CPATTN_TRY(cudaMemcpyAsync(host_out(dq, j, qb), dst[0], qb, cudaMemcpyDeviceToHost,
-                               cs->down));
-    CPATTN_TRY(cudaMemcpyAsync(host_out(dk, j, kb), dst[1], kb, cudaMemcpyDeviceToHost,
-                               cs->down));
-    CPATTN_TRY(cudaMemcpyAsync(host_out(dv, j, kb), dst[2], kb, cudaMemcpyDeviceToHost,
-                               cs->down));
+    CPATTN_TRY(cudaMemcpyAsync(host_out(dq, j, qb), dev_at(L.stage_do, j, qb), qb,
+                               cudaMemcpyDeviceToHost, cs->down));
   }
   // the caller's stream completes with the last download
   CPATTN_TRY(cudaEventRecord(ev_end, cs->down));

@@ -90,13 +90,21 @@ bool tc_supported(const Ring& R);
 cudaError_t launch_tc_fwd(const Ring& R, int q_rank, int kv_rank, const void* q, const void* k,
                           const void* v, void* o, float* lse, int* status, cudaStream_t st,
                           const int* doc_lo = nullptr, const int* ord_q = nullptr);
+// Work a caller queues on the backward's stream between the dK/dV and the dQ
+// kernel (dk and dv are final there): fn(ctx, st).
+struct AfterDkdv {
+  cudaError_t (*fn)(void* ctx, cudaStream_t st);
+  void* ctx;
+};
 // doc_lo / doc_hi (packed sequences): first and last position of each position's
-// document, [B][T] int32 each; nullptr for plain causal.
+// document, [B][T] int32 each; nullptr for plain causal.  after (optional): see
+// AfterDkdv.
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st,
                           const int* doc_lo = nullptr, const int* doc_hi = nullptr,
-                          const int* ord_q = nullptr, const int* ord_k = nullptr);
+                          const int* ord_q = nullptr, const int* ord_k = nullptr,
+                          const AfterDkdv* after = nullptr);
 // All-gather mode backward of rank q_rank (see launch_simt_allgather_bwd); lse2 /
 // delta are the pre-pass statistics of the rank's rows.
 cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,

@@ -1098,7 +1098,7 @@ static cudaError_t prep(K kern, int smem) {
 template <int D>
 static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, const void* k,
                            const void* v, const void* dO, void* dq, void* dk, void* dv,
-                           cudaStream_t st) {
+                           cudaStream_t st, const AfterDkdv* after = nullptr) {
   const bool ag = base.ag_rank >= 0;
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t qrows = (uint64_t)R.B * R.Hq * R.T, krows = (uint64_t)R.B * R.Hkv * R.T;
@@ -1127,6 +1127,8 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   e = cudaGetLastError();
   timing_end(st);
   if (e != cudaSuccess) return e;
+  if (after != nullptr && after->fn != nullptr && (e = after->fn(after->ctx, st)) != cudaSuccess)
+    return e;
   Params pq = base;
   pq.out0 = dq;
   pq.out1 = nullptr;
@@ -1180,14 +1182,15 @@ static tcbwd::Params bwd_params(const Ring& R, const float* lse2, const float* d
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st, const int* doc_lo,
-                          const int* doc_hi, const int* ord_q, const int* ord_k) {
+                          const int* doc_hi, const int* ord_q, const int* ord_k,
+                          const AfterDkdv* after) {
   tcbwd::Params p = bwd_params(R, lse2, delta, status);
   p.doc_lo = doc_lo;
   p.doc_hi = doc_hi;
   p.ord_q = ord_q;
   p.ord_k = ord_k;
-  if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st);
-  return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st);
+  if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st, after);
+  return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st, after);
 }
 
 cudaError_t launch_tc_partial_bwd(const Ring& R, int q_rank, int kv_rank, const void* q,

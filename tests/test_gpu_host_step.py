@@ -2,8 +2,11 @@
 memory, transfers overlapping the compute) gives what the device-resident path
 gives (cpattn_layout to layout order, cpattn_ring_fwd, cpattn_ring_bwd, cpattn_layout
 back to natural order), bit for bit: its halves are independent problems run by the
-same kernels with the same per-tile arithmetic.  Pinned and pageable host buffers,
-a head split (B = 1), a batch split (B even) and an unsplit float32 problem."""
+same kernels with the same per-tile arithmetic.  Pinned and pageable host buffers;
+splits by K/V heads (B = 1: halves, and a forward in quarters), by batch rows (B 4:
+halves, forward quarters), by batch rows for the backward and heads within a row
+for the forward (B 2); an unsplit float32 problem and a split one (whose dk and dv
+come back after both backward kernels)."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +19,10 @@ pytestmark = pytest.mark.gpu
 CASES = [
     W.Workload("hs_tc_B1_H8x2_T2048_cp4_zz", 1, 8, 2, 2048, 128, 4, "zigzag", "bf16"),
     W.Workload("hs_tc_B2_H4x4_T1024_cp2_contig_D64", 2, 4, 4, 1024, 64, 2, "contiguous", "bf16"),
+    W.Workload("hs_tc_B1_H8x4_T1024_cp2_zz", 1, 8, 4, 1024, 128, 2, "zigzag", "bf16"),
+    W.Workload("hs_tc_B4_H2x1_T512_cp2_zz_D64", 4, 2, 1, 512, 64, 2, "zigzag", "bf16"),
     W.Workload("hs_simt_B3_H2x1_T96_cp3_zz_f32", 3, 2, 1, 96, 20, 3, "zigzag", "f32"),
+    W.Workload("hs_simt_B2_H4x2_T64_cp2_zz_f32", 2, 4, 2, 64, 16, 2, "zigzag", "f32"),
 ]
 
 
