@@ -92,15 +92,19 @@ struct Params {
 
 template <int D>
 struct Smem {
-  // one Q tile; K and V in rings of their own (K is last read by S, V by PV); the
-  // (m, l) exchange of the two column halves of each row
-  static constexpr int kKStages = D == 128 ? 3 : 4;
+  // one Q tile; K and V in rings of their own (K is last read by S, V by PV); at
+  // D = 128 a 4 KB staging area per softmax warp for the bf16 output (a third K
+  // stage in its place measured no faster); the (m, l) exchange of the two column
+  // halves of each row
+  static constexpr int kKStages = D == 128 ? 2 : 4;
   static constexpr int kVStages = D == 128 ? 3 : 4;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kTileBytes;
   static constexpr int kV = kK + kKStages * kTileBytes;
-  static constexpr int kXch = kV + kVStages * kTileBytes;
+  static constexpr int kOst = kV + kVStages * kTileBytes;
+  static constexpr int kOstBytes = D == 128 ? 8 * 32 * 128 : 0;
+  static constexpr int kXch = kOst + kOstBytes;
   static constexpr int kBar = kXch + 2 * kTile * 8;
   // barriers: q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
   // s_full[2], p_full[2 buffers][2 halves], pv_done[2], o_free, xch_full, xch_free,
@@ -579,6 +583,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t bh = (int64_t)it.b * p.Hq + it.h;
       const int64_t orow = local ? bh * p.m.c + (it.slot0 - p.q_rank * p.m.c) + row
                                  : bh * p.T + it.slot0 + row;
+      if constexpr (D == 128 && !OUT_F32) {
+        // This thread's 64 output columns [64 half, 64 half + 64) of its row, as bf16:
+        // one 128-byte line in eight 16-byte chunks.  Stored from registers, every
+        // store instruction of the warp would touch 32 lines (one per row); staged
+        // through shared memory, each writes four whole lines.
+        uint32_t wd[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o0[32], o1[32];
+          if (cnt > 0) {
+            tmem_ld32(tmem + lane_off + 256 + half * 64 + c * 32, o0);
+            tmem_ld32(tmem + lane_off + 256 + D + half * 64 + c * 32, o1);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o0[j] = o1[j] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            wd[c * 16 + j] = pack_bf16(a0 * __uint_as_float(o0[2 * j]) + a1 * __uint_as_float(o1[2 * j]),
+                                       a0 * __uint_as_float(o0[2 * j + 1]) +
+                                           a1 * __uint_as_float(o1[2 * j + 1]));
+        }
+        // through this warp's staging area: line i (row 32 quad + i) at 128 i, its
+        // 16-byte chunk a at slot a ^ (i & 7), so that eight lanes writing chunk a of
+        // eight lines, and eight lanes reading the eight chunks of one line, meet
+        // eight different bank groups
+        uint4* st4 = reinterpret_cast<uint4*>(smem + L::kOst + (warp - 4) * 4096);
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+          st4[lane * 8 + (a ^ (lane & 7))] = make_uint4(wd[4 * a], wd[4 * a + 1], wd[4 * a + 2],
+                                                        wd[4 * a + 3]);
+        __syncwarp();
+        // store j: lanes 8 u .. 8 u + 7 write the eight chunks of line 4 j + u
+        const int64_t tile_row0 = orow - row;
+        const int ch = lane & 7;
+        if (in_bounds(tile_row0, kTile, o_rows, p.status)) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int li = 4 * j + (lane >> 3);
+            const uint4 val = st4[li * 8 + (ch ^ (li & 7))];
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                      (tile_row0 + quad * 32 + li) * D + half * 64 + ch * 8) = val;
+          }
+        }
+        // the next item's writes into this area come after these reads
+        __syncwarp();
+      } else {
       // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
       // (the TMEM loads are warp-collective: only the global stores are guarded)
       const bool store = in_bounds(orow, 1, o_rows, p.status);
@@ -613,7 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pack_bf16(v[8 * j + 6], v[8 * j + 7]));
         }
       }
-      if (half == 0 && store) p.lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * kLn2 : -INFINITY;
+      }
+      if (half == 0 && in_bounds(orow, 1, o_rows, p.status))
+        p.lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * kLn2 : -INFINITY;
       // O has been read: the next item's first PV may overwrite it
       tc_fence_before();
       mbar_arrive(o_free);
