@@ -567,7 +567,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t orow = step ? ((int64_t)b * p.Hkv + g) * p.m.c + (kslot0 - p.kv_chunk * p.m.c) + row
                               : ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
     const bool store = in_bounds(orow, 1, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status);
-    if (ok && AG) {
+    if (ok && AG && D == 128 && (cnt > 0 || !p.accumulate)) {
+      // all-gather: float32 share of this rank's queries, added to the sum so far.
+      // This thread's 64 columns of its row are two 128-byte lines of each of dK
+      // and dV; the warp stages its 64 lines of each through shared memory (the Q and
+      // dO stages, idle once the walk is done; chunk a of line i at slot a ^ (i & 7))
+      // so that each load and store of the read-modify-write covers whole lines.
+      tc_fence_after();
+      float4* st4 = reinterpret_cast<float4*>(smem + L::kQ + (warp - 4) * 16384);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times the scale)
+        const float mul = which ? p.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v32[32];
+          if (cnt > 0) {
+            tmem_ld32(tmem + lane_off + 256 + which * D + half * 64 + c * 32, v32);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v32[j] = 0u;
+          }
+          const int li = lane * 2 + c;
+#pragma unroll
+          for (int a = 0; a < 8; ++a)
+            st4[which * 512 + li * 8 + (a ^ (li & 7))] =
+                make_float4(__uint_as_float(v32[4 * a]) * mul, __uint_as_float(v32[4 * a + 1]) * mul,
+                            __uint_as_float(v32[4 * a + 2]) * mul,
+                            __uint_as_float(v32[4 * a + 3]) * mul);
+        }
+      }
+      __syncwarp();
+      const int64_t orow0 = orow - row;  // the tile's first row
+      const int ch = lane & 7;
+      if (in_bounds(orow0, kTile, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status)) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          float* out = static_cast<float*>(which ? p.out0 : p.out1);
+          float4 y[16];
+          if (p.accumulate) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int li = 4 * j + (lane >> 3);
+              y[j] = *reinterpret_cast<const float4*>(out + (orow0 + quad * 32 + (li >> 1)) * D +
+                                                      half * 64 + (li & 1) * 32 + ch * 4);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int li = 4 * j + (lane >> 3);  // line li: row 32 quad + li / 2, half li & 1
+            float4 x = st4[which * 512 + li * 8 + (ch ^ (li & 7))];
+            if (p.accumulate) {
+              x.x += y[j].x;
+              x.y += y[j].y;
+              x.z += y[j].z;
+              x.w += y[j].w;
+            }
+            *reinterpret_cast<float4*>(out + (orow0 + quad * 32 + (li >> 1)) * D + half * 64 +
+                                       (li & 1) * 32 + ch * 4) = x;
+          }
+        }
+      }
+    } else if (ok && AG) {
       // all-gather: float32 share of this rank's queries, added to the sum so far
       tc_fence_after();
       float* dkf = static_cast<float*>(p.out0) + orow * D + half * (D / 2);
@@ -601,6 +665,52 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               dst[j] = x;
             }
+          }
+        }
+      }
+    } else if (ok && !AG && D == 128) {
+      // bf16 dK and dV: this thread's 64 columns of its row are one 128-byte line of
+      // each.  The warp's lines go through shared memory (the Q stages, idle once the
+      // walk is done: chunk a of line i at slot a ^ (i & 7)) so that each store writes
+      // whole lines instead of touching 32 of them.
+      tc_fence_after();
+      uint4* st4 = reinterpret_cast<uint4*>(smem + L::kQ + (warp - 4) * 8192);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times the scale)
+        const float mul = which ? p.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v32[32];
+          if (cnt > 0) {
+            tmem_ld32(tmem + lane_off + 256 + which * D + half * 64 + c * 32, v32);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v32[j] = 0u;
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const int ca = c * 4 + a;  // 16-byte chunk of the line
+            st4[which * 256 + lane * 8 + (ca ^ (lane & 7))] = make_uint4(
+                pack_bf16(__uint_as_float(v32[8 * a]) * mul, __uint_as_float(v32[8 * a + 1]) * mul),
+                pack_bf16(__uint_as_float(v32[8 * a + 2]) * mul, __uint_as_float(v32[8 * a + 3]) * mul),
+                pack_bf16(__uint_as_float(v32[8 * a + 4]) * mul, __uint_as_float(v32[8 * a + 5]) * mul),
+                pack_bf16(__uint_as_float(v32[8 * a + 6]) * mul, __uint_as_float(v32[8 * a + 7]) * mul));
+          }
+        }
+      }
+      __syncwarp();
+      const int64_t orow0 = orow - row;  // the tile's first row
+      const int ch = lane & 7;
+      if (in_bounds(orow0, kTile, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status)) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(which ? p.out0 : p.out1);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int li = 4 * j + (lane >> 3);
+            *reinterpret_cast<uint4*>(out + (orow0 + quad * 32 + li) * D + half * 64 + ch * 8) =
+                st4[which * 256 + li * 8 + (ch ^ (li & 7))];
           }
         }
       }
