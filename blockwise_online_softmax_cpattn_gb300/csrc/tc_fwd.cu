@@ -183,7 +183,8 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t par) {
 template <int D, bool OUT_F32, bool PK>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const Params p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const Params p) {
   using L = Smem<D>;
   constexpr int KS = L::kKStages, VS = L::kVStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -610,26 +611,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 16-byte chunk a at slot a ^ (i & 7), so that eight lanes writing chunk a of
         // eight lines, and eight lanes reading the eight chunks of one line, meet
         // eight different bank groups
+        // The area is laid out as a 32 x 64 box of the output in the tensor map's
+        // 128-byte swizzle (it starts on a 1024-byte boundary), so one TMA store
+        // writes it out while the warp goes on to the next item; the area is
+        // written again only once that store has read it.
+        const uint32_t ost = sbase + L::kOst + (warp - 4) * 4096;
         uint4* st4 = reinterpret_cast<uint4*>(smem + L::kOst + (warp - 4) * 4096);
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
         for (int a = 0; a < 8; ++a)
           st4[lane * 8 + (a ^ (lane & 7))] = make_uint4(wd[4 * a], wd[4 * a + 1], wd[4 * a + 2],
                                                         wd[4 * a + 3]);
+        fence_proxy_async_smem();
         __syncwarp();
-        // store j: lanes 8 u .. 8 u + 7 write the eight chunks of line 4 j + u
         const int64_t tile_row0 = orow - row;
-        const int ch = lane & 7;
-        if (in_bounds(tile_row0, kTile, o_rows, p.status)) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int li = 4 * j + (lane >> 3);
-            const uint4 val = st4[li * 8 + (ch ^ (li & 7))];
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                      (tile_row0 + quad * 32 + li) * D + half * 64 + ch * 8) = val;
-          }
+        if (lane == 0 && in_bounds(tile_row0, kTile, o_rows, p.status)) {
+          tma_store_2d(&tm_o, half * 64, (int)(tile_row0 + quad * 32), ost);
+          bulk_commit_group();
         }
-        // the next item's writes into this area come after these reads
-        __syncwarp();
       } else {
       // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
       // (the TMEM loads are warp-collective: only the global stores are guarded)
@@ -674,6 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // every output store of this CTA is complete before it ends
+  if constexpr (D == 128 && !OUT_F32)
+    if (warp >= 4 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -696,11 +699,19 @@ bool tc_supported(const Ring& R) {
 template <int D, bool F32, bool PK = false>
 static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, const void* q,
                            const void* k, const void* v, cudaStream_t st) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (encode_tmap_2d_bf16(&tq, q, D, (uint64_t)R.B * R.Hq * R.T, 64, tcfwd::kTile) != CUDA_SUCCESS ||
       encode_tmap_2d_bf16(&tk, k, D, (uint64_t)R.B * R.Hkv * R.T, 64, tcfwd::kTile) != CUDA_SUCCESS ||
       encode_tmap_2d_bf16(&tv, v, D, (uint64_t)R.B * R.Hkv * R.T, 64, tcfwd::kTile) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // the bf16 output as 32-row, 64-column boxes (one softmax warp's rows and half); the
+  // float32 outputs of a ring step are stored by the threads themselves
+  to = tq;
+  if (!F32 && D == 128) {
+    const uint64_t o_rows = (uint64_t)R.B * R.Hq * (p.q_rank >= 0 ? R.T / R.cp : R.T);
+    if (encode_tmap_2d_bf16(&to, p.o, D, o_rows, 64, 32) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   constexpr int kSmem = tcfwd::Smem<D>::kBytes;
   auto kern = tcfwd::fwd_kernel<D, F32, PK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -712,7 +723,7 @@ static cudaError_t run_fwd(const Ring& R, const tcfwd::Params& p, int items, con
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
   const int grid = items < sms ? items : sms;
-  kern<<<grid, tcfwd::kThreads, kSmem, st>>>(tq, tk, tv, p);
+  kern<<<grid, tcfwd::kThreads, kSmem, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
