@@ -72,6 +72,19 @@ CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                            uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 // ---------------------------------------------------------------------------
 // kernel timing
 // ---------------------------------------------------------------------------

@@ -139,5 +139,8 @@ void timing_end(cudaStream_t st);
 // Tensor-map encoder (driver entry point fetched through the runtime).
 CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                              uint32_t box_inner, uint32_t box_rows);
+// The same for a float32 [rows][inner] tensor.
+CUresult encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                             uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace cpattn

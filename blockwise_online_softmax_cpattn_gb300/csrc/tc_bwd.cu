@@ -161,6 +161,7 @@ template <int D, bool AG, bool PK>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                 const Params p) {
   using L = DkdvSmem<D>;
   constexpr int QS = L::kQStages, DS = L::kDOStages;
@@ -568,12 +569,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                               : ((int64_t)b * p.Hkv + g) * p.T + kslot0 + row;
     const bool store = in_bounds(orow, 1, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status);
     if (ok && AG && D == 128 && (cnt > 0 || !p.accumulate)) {
-      // all-gather: float32 share of this rank's queries, added to the sum so far.
-      // This thread's 64 columns of its row are two 128-byte lines of each of dK
-      // and dV; the warp stages its 64 lines of each through shared memory (the Q and
-      // dO stages, idle once the walk is done; chunk a of line i at slot a ^ (i & 7))
-      // so that each load and store of the read-modify-write covers whole lines.
+      // all-gather / ring step: float32 share of this rank's queries.  This thread's
+      // 64 columns of its row are two 128-byte lines of each of dK and dV.  The warp
+      // stages them in shared memory (the Q and dO stages, idle once the walk is
+      // done) as four 32-row x 32-column boxes in the tensor maps' 128-byte swizzle
+      // (chunk a of row i at slot a ^ (i & 7)), and one TMA operation per box adds
+      // them into the sums (or stores them, for the first share) in L2, with no load
+      // on the SM.  Each element receives one addition per launch.
       tc_fence_after();
+      const uint32_t stage = sbase + L::kQ + (warp - 4) * 16384;
       float4* st4 = reinterpret_cast<float4*>(smem + L::kQ + (warp - 4) * 16384);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times the scale)
@@ -588,48 +592,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v32[j] = 0u;
           }
-          const int li = lane * 2 + c;
 #pragma unroll
           for (int a = 0; a < 8; ++a)
-            st4[which * 512 + li * 8 + (a ^ (li & 7))] =
+            st4[which * 512 + c * 256 + lane * 8 + (a ^ (lane & 7))] =
                 make_float4(__uint_as_float(v32[4 * a]) * mul, __uint_as_float(v32[4 * a + 1]) * mul,
                             __uint_as_float(v32[4 * a + 2]) * mul,
                             __uint_as_float(v32[4 * a + 3]) * mul);
         }
       }
+      fence_proxy_async_smem();
       __syncwarp();
       const int64_t orow0 = orow - row;  // the tile's first row
-      const int ch = lane & 7;
-      if (in_bounds(orow0, kTile, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status)) {
+      if (lane == 0 &&
+          in_bounds(orow0, kTile, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status)) {
+        const int y = (int)(orow0 + quad * 32);
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          float* out = static_cast<float*>(which ? p.out0 : p.out1);
-          float4 y[16];
-          if (p.accumulate) {
+        for (int which = 0; which < 2; ++which)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int li = 4 * j + (lane >> 3);
-              y[j] = *reinterpret_cast<const float4*>(out + (orow0 + quad * 32 + (li >> 1)) * D +
-                                                      half * 64 + (li & 1) * 32 + ch * 4);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < 2; ++c) {
+            const CUtensorMap* map = which ? &tm_dk : &tm_dv;
+            const uint32_t box = stage + which * 8192 + c * 4096;
+            if (p.accumulate) tma_reduce_add_2d(map, half * 64 + c * 32, y, box);
+            else tma_store_2d(map, half * 64 + c * 32, y, box);
           }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int li = 4 * j + (lane >> 3);  // line li: row 32 quad + li / 2, half li & 1
-            float4 x = st4[which * 512 + li * 8 + (ch ^ (li & 7))];
-            if (p.accumulate) {
-              x.x += y[j].x;
-              x.y += y[j].y;
-              x.z += y[j].z;
-              x.w += y[j].w;
-            }
-            *reinterpret_cast<float4*>(out + (orow0 + quad * 32 + (li >> 1)) * D + half * 64 +
-                                       (li & 1) * 32 + ch * 4) = x;
-          }
-        }
+        bulk_commit_group();
+        bulk_wait_all();  // the CTA's shared memory is released when it ends
       }
     } else if (ok && AG) {
       // all-gather: float32 share of this rank's queries, added to the sum so far
@@ -671,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (ok && !AG && D == 128) {
       // bf16 dK and dV: this thread's 64 columns of its row are one 128-byte line of
       // each.  The warp's lines go through shared memory (the Q stages, idle once the
-      // walk is done: chunk a of line i at slot a ^ (i & 7)) so that each store writes
-      // whole lines instead of touching 32 of them.
+      // walk is done: chunk a of line i at slot a ^ (i & 7)) so that they leave as
+      // whole boxes instead of stores that touch 32 lines each.
       tc_fence_after();
       uint4* st4 = reinterpret_cast<uint4*>(smem + L::kQ + (warp - 4) * 8192);
 #pragma unroll
@@ -699,20 +686,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      fence_proxy_async_smem();
       __syncwarp();
+      // the two areas are 32 x 64 boxes of dV and dK in the tensor maps' 128-byte
+      // swizzle: one TMA store each
       const int64_t orow0 = orow - row;  // the tile's first row
-      const int ch = lane & 7;
-      if (in_bounds(orow0, kTile, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status)) {
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(which ? p.out0 : p.out1);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int li = 4 * j + (lane >> 3);
-            *reinterpret_cast<uint4*>(out + (orow0 + quad * 32 + li) * D + half * 64 + ch * 8) =
-                st4[which * 256 + li * 8 + (ch ^ (li & 7))];
-          }
-        }
+      if (lane == 0 &&
+          in_bounds(orow0, kTile, step ? (int64_t)p.B * p.Hkv * p.m.c : kv_rows, p.status)) {
+        const uint32_t stage = sbase + L::kQ + (warp - 4) * 8192;
+        tma_store_2d(&tm_dv, half * 64, (int)(orow0 + quad * 32), stage);
+        tma_store_2d(&tm_dk, half * 64, (int)(orow0 + quad * 32), stage + 4096);
+        bulk_commit_group();
+        bulk_wait_all();  // the CTA's shared memory is released when it ends
       }
     } else if (ok) {
       tc_fence_after();
@@ -1218,6 +1203,18 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
       encode_tmap_2d_bf16(&tk, k, D, krows, 64, kTile) != CUDA_SUCCESS ||
       encode_tmap_2d_bf16(&tv, v, D, krows, 64, kTile) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // dK / dV as boxes of 32 rows x 64 bf16 columns (ring) or 32 x 32 float32 columns
+  // (the all-gather sums and a ring step's parts), for the epilogue's TMA operations
+  CUtensorMap tdk = tq, tdv = tq;
+  if (D == 128) {
+    const bool step_mode = ag && base.kv_chunk >= 0;
+    const uint64_t orows = (uint64_t)R.B * R.Hkv * (step_mode ? R.T / R.cp : R.T);
+    const CUresult r1 = ag ? encode_tmap_2d_f32(&tdk, dk, D, orows, 32, 32)
+                           : encode_tmap_2d_bf16(&tdk, dk, D, orows, 64, 32);
+    const CUresult r2 = ag ? encode_tmap_2d_f32(&tdv, dv, D, orows, 32, 32)
+                           : encode_tmap_2d_bf16(&tdv, dv, D, orows, 64, 32);
+    if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   Params pk = base;
   pk.out0 = dk;
   pk.out1 = dv;
@@ -1233,7 +1230,7 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
                : packed ? "tc_packed_dkdv"
                         : "tc_bwd_dkdv",
                st);
-  kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pk);
+  kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, pk);
   e = cudaGetLastError();
   timing_end(st);
   if (e != cudaSuccess) return e;
