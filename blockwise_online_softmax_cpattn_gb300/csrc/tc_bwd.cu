@@ -129,6 +129,23 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
   }
 }
 
+// The same with two 32-byte stores (dst 32-byte aligned).
+__device__ __forceinline__ void store_row32_bf16_v8(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                                    float mul) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      w[j] = pack_bf16(__uint_as_float(v[16 * h + 2 * j]) * mul,
+                       __uint_as_float(v[16 * h + 2 * j + 1]) * mul);
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * h),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                 "r"(w[7])
+                 : "memory");
+  }
+}
+
 // ===========================================================================
 // dK / dV
 // ===========================================================================
@@ -1147,7 +1164,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 32; ++jj) v32[jj] = 0u;
         }
         if (!row_ok) continue;
-        if (p.kv_chunk >= 0) {
+        if (p.kv_chunk >= 0 && (reinterpret_cast<uintptr_t>(p.out0) & 31) == 0) {
+          // one ring step: the float32 contribution, overwritten or added; 32-byte
+          // loads and stores, every old value loaded before any store
+          float* dst = static_cast<float*>(p.out0) + dq_off + c * 32;
+          float y[32];
+          if (p.accumulate) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              asm volatile("ld.global.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                           : "=f"(y[8 * j]), "=f"(y[8 * j + 1]), "=f"(y[8 * j + 2]), "=f"(y[8 * j + 3]),
+                             "=f"(y[8 * j + 4]), "=f"(y[8 * j + 5]), "=f"(y[8 * j + 6]), "=f"(y[8 * j + 7])
+                           : "l"(dst + 8 * j));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) y[j] = 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              x[e] = __uint_as_float(v32[8 * j + e]) * p.scale;
+              if (p.accumulate) x[e] += y[8 * j + e];
+            }
+            asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * j),
+                         "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+                         "f"(x[7])
+                         : "memory");
+          }
+        } else if (p.kv_chunk >= 0) {
           // one ring step: the float32 contribution, overwritten or added
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + dq_off + c * 32);
 #pragma unroll
@@ -1165,6 +1211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             dst[j] = x;
           }
+        } else if ((reinterpret_cast<uintptr_t>(p.out0) & 31) == 0) {
+          // 32-byte stores: half as many store instructions, each touching 32 rows
+          store_row32_bf16_v8(static_cast<__nv_bfloat16*>(p.out0) + dq_off + c * 32, v32, p.scale);
         } else {
           store_row32_bf16(static_cast<__nv_bfloat16*>(p.out0) + dq_off + c * 32, v32, p.scale);
         }
