@@ -650,7 +650,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           v[j] = a0 * __uint_as_float(o0[j]) + a1 * __uint_as_float(o1[j]);
-        if (store && OUT_F32) {
+        if (store && OUT_F32 && (reinterpret_cast<uintptr_t>(p.o) & 31) == 0) {
+          // 32-byte stores: half as many store instructions, each touching 32 rows
+          float* dst = static_cast<float*>(p.o) + orow * D + col;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * j),
+                         "f"(v[8 * j]), "f"(v[8 * j + 1]), "f"(v[8 * j + 2]), "f"(v[8 * j + 3]),
+                         "f"(v[8 * j + 4]), "f"(v[8 * j + 5]), "f"(v[8 * j + 6]), "f"(v[8 * j + 7])
+                         : "memory");
+        } else if (store && OUT_F32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + col);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
