@@ -23,6 +23,11 @@ __global__ void __launch_bounds__(256) merge_kernel(int64_t rows, int D,
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
        row += warps) {
+    float4 xa, xb;
+    if (VEC4 && D == 128) {  // the row's operands in flight before its weights are known
+      xa = reinterpret_cast<const float4*>(oa + row * 128)[lane];
+      xb = reinterpret_cast<const float4*>(ob + row * 128)[lane];
+    }
     const float a = la[row], b = lb[row];
     const float m = fmaxf(a, b);
     float wa = 0.f, wb = 0.f, lse = -INFINITY;
@@ -34,7 +39,14 @@ __global__ void __launch_bounds__(256) merge_kernel(int64_t rows, int D,
       lse = m + logf(s);
     }
     const int64_t base = row * (int64_t)D;
-    if (VEC4) {
+    if (VEC4 && D == 128) {
+      float4 z;
+      z.x = wa * xa.x + wb * xb.x;
+      z.y = wa * xa.y + wb * xb.y;
+      z.z = wa * xa.z + wb * xb.z;
+      z.w = wa * xa.w + wb * xb.w;
+      reinterpret_cast<float4*>(oo + base)[lane] = z;
+    } else if (VEC4) {
       const float4* pa = reinterpret_cast<const float4*>(oa + base);
       const float4* pb = reinterpret_cast<const float4*>(ob + base);
       float4* po = reinterpret_cast<float4*>(oo + base);
