@@ -234,7 +234,7 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
                               void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                               void* stream) {
   return cpattn::ring_bwd_after_dkdv(desc, q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes,
-                                     stream, nullptr);
+                                     stream, nullptr, nullptr);
 }
 
 }  // extern "C"
@@ -243,7 +243,7 @@ cpattn_status cpattn::ring_bwd_after_dkdv(const cpattn_desc* desc, const void* q
                                           const void* v, const void* o, const float* lse,
                                           const void* dO, void* dq, void* dk, void* dv,
                                           void* workspace, size_t ws_bytes, void* stream,
-                                          const AfterDkdv* after) {
+                                          const AfterDkdv* after, const AfterDqPart* dq_parts) {
   Ring R;
   cpattn_status s = validate(desc, &R);
   if (s != CPATTN_OK) return s;
@@ -262,11 +262,14 @@ cpattn_status cpattn::ring_bwd_after_dkdv(const cpattn_desc* desc, const void* q
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   if (tc)
     return from_cuda(launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st,
-                                   nullptr, nullptr, nullptr, nullptr, after));
+                                   nullptr, nullptr, nullptr, nullptr, after, dq_parts));
   e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   e = launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st);
   if (e == cudaSuccess && after != nullptr && after->fn != nullptr) e = after->fn(after->ctx, st);
+  if (dq_parts != nullptr && dq_parts->fn != nullptr)
+    for (int j = 0; j < dq_parts->parts && e == cudaSuccess; ++j)
+      e = dq_parts->fn(dq_parts->ctx, st, j);
   return from_cuda(e);
 }
 

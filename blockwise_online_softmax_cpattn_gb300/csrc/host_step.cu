@@ -17,7 +17,8 @@
 //                    its dK/dV and dQ kernels, permute dq back
 //   download stream  o and LSE of a forward group as soon as it is done; dk and dv
 //                    of a backward group while its dQ kernel runs; dq once its
-//                    backward is done
+//                    backward is done (the last group's in two parts, the first
+//                    while the second part's dQ kernel runs)
 //
 // so the first kernel waits only for the first forward group's inputs, uploads
 // run while earlier groups compute, downloads while later ones do, and only the
@@ -36,7 +37,9 @@ namespace {
 constexpr int kMaxBwdGroups = 2, kMaxFwdGroups = 2 * kMaxBwdGroups;
 // events per device: start, end; per forward group: inputs landed, outputs ready;
 // per backward group: dO landed, dk and dv ready, dq ready
-constexpr int kNumEvents = 2 + 2 * kMaxFwdGroups + 3 * kMaxBwdGroups;
+// plus the two parts of the last backward group's dq
+constexpr int kDqParts = 2;
+constexpr int kNumEvents = 2 + 2 * kMaxFwdGroups + 3 * kMaxBwdGroups + kDqParts;
 
 struct CopyStreams {
   cudaStream_t up = nullptr, down = nullptr;
@@ -160,6 +163,24 @@ cudaError_t dkdv_out(void* ctx, cudaStream_t st) {
   return cudaEventRecord(d->done, st);
 }
 
+// Queued by the backward after each part of its dQ kernel: that part's dq back to
+// natural order, then the event the download stream waits for.
+struct DqOut {
+  cpattn_desc gp;  // one part
+  const char* src;
+  char* dst;
+  size_t bytes;  // of one part
+  cudaEvent_t done[kDqParts];
+};
+
+cudaError_t dq_out(void* ctx, cudaStream_t st, int part) {
+  DqOut* d = static_cast<DqOut*>(ctx);
+  if (cpattn_layout(CPATTN_ZIGZAG_INV, &d->gp, d->src + part * d->bytes, d->dst + part * d->bytes,
+                    d->gp.H_q, st) != CPATTN_OK)
+    return cudaErrorLaunchFailure;
+  return cudaEventRecord(d->done[part], st);
+}
+
 }  // namespace
 }  // namespace cpattn
 
@@ -213,6 +234,7 @@ extern "C" cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const vo
   auto ev_do = [&](int j) { return ev[2 + 2 * kMaxFwdGroups + j]; };  // backward group j
   auto ev_dkdv = [&](int j) { return ev[2 + 2 * kMaxFwdGroups + kMaxBwdGroups + j]; };
   auto ev_grad = [&](int j) { return ev[2 + 2 * kMaxFwdGroups + 2 * kMaxBwdGroups + j]; };
+  auto ev_dq = [&](int part) { return ev[2 + 2 * kMaxFwdGroups + 3 * kMaxBwdGroups + part]; };
 
 #define CPATTN_TRY(x)                         \
   do {                                        \
@@ -282,23 +304,42 @@ extern "C" cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const vo
     out.heads[0] = out.heads[1] = gb.H_kv;
     out.done = ev_dkdv(j);
     const AfterDkdv after{dkdv_out, &out};
+    // the last group's dq is the one download left after the last kernel: its dQ
+    // kernel runs in two parts, and the first part goes home while the second computes
+    const bool parts = j == nb - 1 && splits(&gb, kDqParts);
+    DqOut dqo;
+    dqo.gp = group_desc(&gb, kDqParts);
+    dqo.src = dev_at(L.lay_dq, j, qb);
+    dqo.dst = dev_at(L.stage_do, j, qb);
+    dqo.bytes = qb / kDqParts;
+    for (int part = 0; part < kDqParts; ++part) dqo.done[part] = ev_dq(part);
+    const AfterDqPart after_dq{dq_out, &dqo, kDqParts};
     CPATTN_TRY_S(ring_bwd_after_dkdv(&gb, dev_at(L.lay_q, j, qb), dev_at(L.lay_k, j, kb),
                                      dev_at(L.lay_v, j, kb), dev_at(L.lay_o, j, qb),
                                      reinterpret_cast<float*>(dev_at(L.lay_lse, j, lb)),
                                      dev_at(L.lay_do, j, qb), dev_at(L.lay_dq, j, qb),
                                      dev_at(L.lay_dk, j, kb), dev_at(L.lay_dv, j, kb),
-                                     w + L.bwd_ws, L.bwd, st, &after));
+                                     w + L.bwd_ws, L.bwd, st, &after, parts ? &after_dq : nullptr));
     CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_dkdv(j), 0));
     CPATTN_TRY(cudaMemcpyAsync(host_out(dk, j, kb), out.dst[0], kb, cudaMemcpyDeviceToHost,
                                cs->down));
     CPATTN_TRY(cudaMemcpyAsync(host_out(dv, j, kb), out.dst[1], kb, cudaMemcpyDeviceToHost,
                                cs->down));
-    CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_INV, &gb, dev_at(L.lay_dq, j, qb),
-                               dev_at(L.stage_do, j, qb), gb.H_q, st));
-    CPATTN_TRY(cudaEventRecord(ev_grad(j), st));
-    CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_grad(j), 0));
-    CPATTN_TRY(cudaMemcpyAsync(host_out(dq, j, qb), dev_at(L.stage_do, j, qb), qb,
-                               cudaMemcpyDeviceToHost, cs->down));
+    if (parts) {
+      for (int part = 0; part < kDqParts; ++part) {
+        CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_dq(part), 0));
+        CPATTN_TRY(cudaMemcpyAsync(host_out(dq, j, qb) + part * dqo.bytes,
+                                   dqo.dst + part * dqo.bytes, dqo.bytes, cudaMemcpyDeviceToHost,
+                                   cs->down));
+      }
+    } else {
+      CPATTN_TRY_S(cpattn_layout(CPATTN_ZIGZAG_INV, &gb, dev_at(L.lay_dq, j, qb),
+                                 dev_at(L.stage_do, j, qb), gb.H_q, st));
+      CPATTN_TRY(cudaEventRecord(ev_grad(j), st));
+      CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_grad(j), 0));
+      CPATTN_TRY(cudaMemcpyAsync(host_out(dq, j, qb), dev_at(L.stage_do, j, qb), qb,
+                                 cudaMemcpyDeviceToHost, cs->down));
+    }
   }
   // the caller's stream completes with the last download
   CPATTN_TRY(cudaEventRecord(ev_end, cs->down));

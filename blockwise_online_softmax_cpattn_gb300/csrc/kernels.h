@@ -96,15 +96,25 @@ struct AfterDkdv {
   cudaError_t (*fn)(void* ctx, cudaStream_t st);
   void* ctx;
 };
+// The dQ kernel run as `parts` launches, part j over the j-th contiguous parts-th of
+// every tensor (an independent problem of the same kind), with fn(ctx, st, j)
+// queued after launch j, so another stream can take part j's dq while the next
+// part computes.  Plain ring problems only; where the problem does not split so,
+// one launch is followed by fn for every part in order.
+struct AfterDqPart {
+  cudaError_t (*fn)(void* ctx, cudaStream_t st, int part);
+  void* ctx;
+  int parts;
+};
 // doc_lo / doc_hi (packed sequences): first and last position of each position's
 // document, [B][T] int32 each; nullptr for plain causal.  after (optional): see
-// AfterDkdv.
+// AfterDkdv; dq_parts (optional): see AfterDqPart.
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st,
                           const int* doc_lo = nullptr, const int* doc_hi = nullptr,
                           const int* ord_q = nullptr, const int* ord_k = nullptr,
-                          const AfterDkdv* after = nullptr);
+                          const AfterDkdv* after = nullptr, const AfterDqPart* dq_parts = nullptr);
 // All-gather mode backward of rank q_rank (see launch_simt_allgather_bwd); lse2 /
 // delta are the pre-pass statistics of the rank's rows.
 cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,

@@ -1242,7 +1242,8 @@ static cudaError_t prep(K kern, int smem) {
 template <int D>
 static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, const void* k,
                            const void* v, const void* dO, void* dq, void* dk, void* dv,
-                           cudaStream_t st, const AfterDkdv* after = nullptr) {
+                           cudaStream_t st, const AfterDkdv* after = nullptr,
+                           const AfterDqPart* dq_parts = nullptr) {
   const bool ag = base.ag_rank >= 0;
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t qrows = (uint64_t)R.B * R.Hq * R.T, krows = (uint64_t)R.B * R.Hkv * R.T;
@@ -1297,6 +1298,43 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
+  // dQ in parts (plain ring only): part j is the j-th contiguous np-th of every tensor,
+  // batch rows when np divides B, else K/V heads (with their query heads) of each row
+  const int np = dq_parts != nullptr && dq_parts->fn != nullptr ? dq_parts->parts : 1;
+  const bool split = np > 1 && !ag && !packed &&
+                     (R.B % np == 0 || (np % R.B == 0 && R.Hkv % (np / R.B) == 0));
+  if (split) {
+    const int m = R.B % np == 0 ? 1 : np / R.B;  // parts per batch row
+    const int Bp = R.B % np == 0 ? R.B / np : 1, Hqp = R.Hq / m, Hkvp = R.Hkv / m;
+    const uint64_t qr = (uint64_t)Bp * Hqp * R.T, kr = (uint64_t)Bp * Hkvp * R.T;
+    for (int j = 0; j < np; ++j) {
+      const char* qj = static_cast<const char*>(q) + j * qr * D * 2;
+      const char* kj = static_cast<const char*>(k) + j * kr * D * 2;
+      const char* vj = static_cast<const char*>(v) + j * kr * D * 2;
+      const char* dj = static_cast<const char*>(dO) + j * qr * D * 2;
+      CUtensorMap pqm, pkm, pvm, pdm;
+      if (encode_tmap_2d_bf16(&pqm, qj, D, qr, 64, kTile) != CUDA_SUCCESS ||
+          encode_tmap_2d_bf16(&pdm, dj, D, qr, 64, kTile) != CUDA_SUCCESS ||
+          encode_tmap_2d_bf16(&pkm, kj, D, kr, 64, kTile) != CUDA_SUCCESS ||
+          encode_tmap_2d_bf16(&pvm, vj, D, kr, 64, kTile) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+      Params pj = pq;
+      pj.B = Bp;
+      pj.Hq = Hqp;
+      pj.Hkv = Hkvp;
+      pj.lse2 = base.lse2 + j * qr;
+      pj.delta = base.delta + j * qr;
+      pj.out0 = static_cast<char*>(dq) + j * qr * D * 2;
+      const int items = (int)(qr / kTile);
+      timing_begin("tc_bwd_dq", st);
+      kdq<<<items < sms ? items : sms, kThreads, DqSmem<D>::kBytes, st>>>(pqm, pkm, pvm, pdm, pj);
+      e = cudaGetLastError();
+      timing_end(st);
+      if (e != cudaSuccess) return e;
+      if ((e = dq_parts->fn(dq_parts->ctx, st, j)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   timing_begin(step     ? "tc_partial_dq"
                : ag     ? "tc_allgather_dq"
                : packed ? "tc_packed_dq"
@@ -1305,6 +1343,8 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   kdq<<<q_items < sms ? q_items : sms, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
   e = cudaGetLastError();
   timing_end(st);
+  if (e == cudaSuccess && np > 1)
+    for (int j = 0; j < np && e == cudaSuccess; ++j) e = dq_parts->fn(dq_parts->ctx, st, j);
   return e;
 }
 
@@ -1339,14 +1379,14 @@ cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const voi
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st, const int* doc_lo,
                           const int* doc_hi, const int* ord_q, const int* ord_k,
-                          const AfterDkdv* after) {
+                          const AfterDkdv* after, const AfterDqPart* dq_parts) {
   tcbwd::Params p = bwd_params(R, lse2, delta, status);
   p.doc_lo = doc_lo;
   p.doc_hi = doc_hi;
   p.ord_q = ord_q;
   p.ord_k = ord_k;
-  if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st, after);
-  return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st, after);
+  if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st, after, dq_parts);
+  return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st, after, dq_parts);
 }
 
 cudaError_t launch_tc_partial_bwd(const Ring& R, int q_rank, int kv_rank, const void* q,
