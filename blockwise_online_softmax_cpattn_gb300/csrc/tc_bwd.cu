@@ -1185,8 +1185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              x[e] = __uint_as_float(v32[8 * j + e]) * p.scale;
-              if (p.accumulate) x[e] += y[8 * j + e];
+              // a multiply and an add, each rounded (no fused multiply-add), as below
+              x[e] = __fmul_rn(__uint_as_float(v32[8 * j + e]), p.scale);
+              if (p.accumulate) x[e] = __fadd_rn(x[e], y[8 * j + e]);
             }
             asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * j),
                          "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
@@ -1198,16 +1199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out0) + dq_off + c * 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            float4 x = make_float4(__uint_as_float(v32[4 * j]) * p.scale,
-                                   __uint_as_float(v32[4 * j + 1]) * p.scale,
-                                   __uint_as_float(v32[4 * j + 2]) * p.scale,
-                                   __uint_as_float(v32[4 * j + 3]) * p.scale);
+            float4 x = make_float4(__fmul_rn(__uint_as_float(v32[4 * j]), p.scale),
+                                   __fmul_rn(__uint_as_float(v32[4 * j + 1]), p.scale),
+                                   __fmul_rn(__uint_as_float(v32[4 * j + 2]), p.scale),
+                                   __fmul_rn(__uint_as_float(v32[4 * j + 3]), p.scale));
             if (p.accumulate) {
               const float4 y = dst[j];
-              x.x += y.x;
-              x.y += y.y;
-              x.z += y.z;
-              x.w += y.w;
+              x.x = __fadd_rn(x.x, y.x);
+              x.y = __fadd_rn(x.y, y.y);
+              x.z = __fadd_rn(x.z, y.z);
+              x.w = __fadd_rn(x.w, y.w);
             }
             dst[j] = x;
           }
