@@ -587,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (D == 128 && !OUT_F32) {
         // This thread's 64 output columns [64 half, 64 half + 64) of its row, as bf16:
         // one 128-byte line in eight 16-byte chunks.  Stored from registers, every
-        // store instruction of the warp would touch 32 lines (one per row); staged
-        // through shared memory, each writes four whole lines.
+        // store instruction of the warp would touch 32 lines (one per row); instead
+        // the warp's 32 lines go to shared memory and leave as one TMA store.
         uint32_t wd[32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -607,14 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        a0 * __uint_as_float(o0[2 * j + 1]) +
                                            a1 * __uint_as_float(o1[2 * j + 1]));
         }
-        // through this warp's staging area: line i (row 32 quad + i) at 128 i, its
-        // 16-byte chunk a at slot a ^ (i & 7), so that eight lanes writing chunk a of
-        // eight lines, and eight lanes reading the eight chunks of one line, meet
-        // eight different bank groups
-        // The area is laid out as a 32 x 64 box of the output in the tensor map's
-        // 128-byte swizzle (it starts on a 1024-byte boundary), so one TMA store
-        // writes it out while the warp goes on to the next item; the area is
-        // written again only once that store has read it.
+        // This warp's staging area holds line i (row 32 quad + i) at 128 i, its chunk
+        // a at slot a ^ (i & 7): the tensor map's 128-byte swizzle of a 32 x 64 box
+        // (the area starts on a 1024-byte boundary), and eight lanes writing chunk a
+        // of eight lines meet eight different bank groups.  One TMA store writes the
+        // box out while the warp goes on to the next item; the area is written again
+        // only once that store has read it.
         const uint32_t ost = sbase + L::kOst + (warp - 4) * 4096;
         uint4* st4 = reinterpret_cast<uint4*>(smem + L::kOst + (warp - 4) * 4096);
         if (lane == 0) bulk_wait_read_all();
@@ -631,49 +629,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit_group();
         }
       } else {
-      // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
-      // (the TMEM loads are warp-collective: only the global stores are guarded)
-      const bool store = in_bounds(orow, 1, o_rows, p.status);
+        // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
+        // (the TMEM loads are warp-collective: only the global stores are guarded)
+        const bool store = in_bounds(orow, 1, o_rows, p.status);
 #pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = half * (D / 2) + c * 32;
-        uint32_t o0[32], o1[32];
-        if (cnt > 0) {
-          tmem_ld32(tmem + lane_off + 256 + col, o0);
-          tmem_ld32(tmem + lane_off + 256 + D + col, o1);
-          tmem_wait_ld();
-        } else {
+        for (int c = 0; c < D / 64; ++c) {
+          const int col = half * (D / 2) + c * 32;
+          uint32_t o0[32], o1[32];
+          if (cnt > 0) {
+            tmem_ld32(tmem + lane_off + 256 + col, o0);
+            tmem_ld32(tmem + lane_off + 256 + D + col, o1);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o0[j] = o1[j] = 0u;
+            for (int j = 0; j < 32; ++j) o0[j] = o1[j] = 0u;
+          }
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = a0 * __uint_as_float(o0[j]) + a1 * __uint_as_float(o1[j]);
+          if (store && OUT_F32 && (reinterpret_cast<uintptr_t>(p.o) & 31) == 0) {
+            // 32-byte stores: half as many store instructions, each touching 32 rows
+            float* dst = static_cast<float*>(p.o) + orow * D + col;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * j),
+                           "f"(v[8 * j]), "f"(v[8 * j + 1]), "f"(v[8 * j + 2]), "f"(v[8 * j + 3]),
+                           "f"(v[8 * j + 4]), "f"(v[8 * j + 5]), "f"(v[8 * j + 6]), "f"(v[8 * j + 7])
+                           : "memory");
+          } else if (store && OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + col);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else if (store) {
+            uint4* dst =
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                                  pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                                  pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+          }
         }
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          v[j] = a0 * __uint_as_float(o0[j]) + a1 * __uint_as_float(o1[j]);
-        if (store && OUT_F32 && (reinterpret_cast<uintptr_t>(p.o) & 31) == 0) {
-          // 32-byte stores: half as many store instructions, each touching 32 rows
-          float* dst = static_cast<float*>(p.o) + orow * D + col;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 8 * j),
-                         "f"(v[8 * j]), "f"(v[8 * j + 1]), "f"(v[8 * j + 2]), "f"(v[8 * j + 3]),
-                         "f"(v[8 * j + 4]), "f"(v[8 * j + 5]), "f"(v[8 * j + 6]), "f"(v[8 * j + 7])
-                         : "memory");
-        } else if (store && OUT_F32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + col);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        } else if (store) {
-          uint4* dst =
-              reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                                pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                                pack_bf16(v[8 * j + 6], v[8 * j + 7]));
-        }
-      }
       }
       if (half == 0 && in_bounds(orow, 1, o_rows, p.status))
         p.lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * kLn2 : -INFINITY;
