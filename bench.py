@@ -202,6 +202,9 @@ def kernel_flops_or_bytes(name, w, pairs=None):
         return "tensor", 8.0 * w.D * pairs
     if name in ("tc_bwd_dq", "simt_bwd_dq", "tc_packed_dq"):        # the dQ product only
         return "tensor", 2.0 * w.D * pairs
+    # the dK/dV kernel and the dQ kernel that overlaps its end, timed as one unit
+    if name in ("tc_bwd_dkdv_dq", "tc_packed_dkdv_dq"):
+        return "tensor", 10.0 * w.D * pairs
     # all-gather mode: one launch covers one rank's rows (1/cp of the pairs on average)
     # one ring step (rank, chunk): 1 / cp^2 of the pairs on average
     if name == "tc_partial_fwd":
@@ -240,6 +243,8 @@ KERNEL_SOURCES = {
     "tc_bwd_dkdv": ("tc_bwd.cu", "common.cuh", "kernels.h"),
     "tc_bwd_dq": ("tc_bwd.cu", "common.cuh", "kernels.h"),
 }
+# units timed as one span: the sum of their kernels' traffic
+KERNEL_UNITS = {"tc_bwd_dkdv_dq": ("tc_bwd_dkdv", "tc_bwd_dq")}
 
 
 def source_digest(files=None):
@@ -259,7 +264,11 @@ def source_digest(files=None):
 
 def traffic_for(kernel, workload):
     """dram bytes per launch from the committed ncu summary, if the sources of the
-    kernel's translation unit are unchanged since the capture."""
+    kernel's translation unit are unchanged since the capture (for a unit of several
+    kernels, the sum over them, if every one is current)."""
+    if kernel in KERNEL_UNITS:
+        parts = [traffic_for(k, workload) for k in KERNEL_UNITS[kernel]]
+        return None if any(x is None for x in parts) else sum(parts)
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None

@@ -218,15 +218,17 @@ cpattn_status cpattn_ring_fwd(const cpattn_desc* desc, const void* q, const void
 }
 
 // Workspace: Delta (float32 per query row), then the LSE in base 2 (float32 per
-// query row), each section 256-byte aligned.
+// query row), then the dQ kernel's item counter (kClaimBytes), each section
+// 256-byte aligned.
 static size_t ws_section(const cpattn_desc* desc) {
   const size_t rows = (size_t)desc->B * desc->H_q * desc->T;
   return (rows * sizeof(float) + 255) / 256 * 256;
 }
+static constexpr size_t kClaimBytes = 256;
 
 size_t cpattn_ring_bwd_workspace(const cpattn_desc* desc) {
   if (validate(desc, nullptr) != CPATTN_OK) return 0;
-  return 2 * ws_section(desc);
+  return 2 * ws_section(desc) + kClaimBytes;
 }
 
 cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void* k,
@@ -256,13 +258,14 @@ cpattn_status cpattn::ring_bwd_after_dkdv(const cpattn_desc* desc, const void* q
   cudaGetLastError();
   float* delta = static_cast<float*>(workspace);
   float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_section(desc));
+  int* claim = reinterpret_cast<int*>(static_cast<char*>(workspace) + 2 * ws_section(desc));
   const int64_t rows = (int64_t)R.B * R.Hq * R.T;
   const bool tc = R.bf16 && tc_supported(R);
   cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   if (tc)
     return from_cuda(launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st,
-                                   nullptr, nullptr, nullptr, nullptr, after, dq_parts));
+                                   nullptr, nullptr, nullptr, nullptr, after, dq_parts, claim));
   e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   e = launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st);
@@ -359,6 +362,7 @@ cpattn_status cpattn_ring_bwd_packed(const cpattn_desc* desc, const int32_t* sta
   char* stats = static_cast<char*>(workspace) + packed_stats_offset(desc);
   float* delta = reinterpret_cast<float*>(stats);
   float* lse2 = reinterpret_cast<float*>(stats + ws_section(desc));
+  int* claim = reinterpret_cast<int*>(stats + 2 * ws_section(desc));
   const bool tc = R.bf16 && tc_supported(R);
   PackedTables t;
   if (packed_tables(desc, R, starts, n_docs, workspace, tc, st, &t) != cudaSuccess)
@@ -371,7 +375,7 @@ cpattn_status cpattn_ring_bwd_packed(const cpattn_desc* desc, const int32_t* sta
   if (tc)
     return from_cuda(
         launch_tc_bwd(R, q, k, v, lse2, delta, dO, dq, dk, dv, status_ptr(), st, lo, hi, t.ord_q,
-                      t.ord_k));
+                      t.ord_k, nullptr, nullptr, claim));
   e = launch_simt_bwd_dq(R, q, k, v, lse, delta, dO, dq, st, lo);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   return from_cuda(launch_simt_bwd_dkdv(R, q, k, v, lse, delta, dO, dk, dv, st, hi));

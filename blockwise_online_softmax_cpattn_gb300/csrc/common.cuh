@@ -166,6 +166,15 @@ struct StageRing {
 // The k-th work item of a persistent CTA, or -1: resident CTAs walk a
 // heaviest-first item list in a snake (rounds of gridDim.x items, every other
 // round reversed), which evens out the per-CTA totals.
+// Programmatic dependent launch: let the grid launched after this one as its
+// programmatic dependent start once every CTA here has executed this (or exited) ...
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and, in that dependent, wait until the grids it depends on have completed and
+// their memory operations are visible (returns at once in a grid launched normally).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ int item_of(int k, int n_items) {
   const int G = gridDim.x;
   const int w = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);

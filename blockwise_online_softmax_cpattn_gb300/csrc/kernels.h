@@ -108,13 +108,17 @@ struct AfterDqPart {
 };
 // doc_lo / doc_hi (packed sequences): first and last position of each position's
 // document, [B][T] int32 each; nullptr for plain causal.  after (optional): see
-// AfterDkdv; dq_parts (optional): see AfterDqPart.
+// AfterDkdv; dq_parts (optional): see AfterDqPart.  dq_claim (optional): one int of
+// device memory that the dQ kernel's CTAs claim their items from; given (and with
+// neither after nor dq_parts), the dQ kernel is launched on st as a programmatic
+// dependent of the dK/dV kernel and overlaps its last CTAs.
 cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const void* v,
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st,
                           const int* doc_lo = nullptr, const int* doc_hi = nullptr,
                           const int* ord_q = nullptr, const int* ord_k = nullptr,
-                          const AfterDkdv* after = nullptr, const AfterDqPart* dq_parts = nullptr);
+                          const AfterDkdv* after = nullptr, const AfterDqPart* dq_parts = nullptr,
+                          int* dq_claim = nullptr);
 // All-gather mode backward of rank q_rank (see launch_simt_allgather_bwd); lse2 /
 // delta are the pre-pass statistics of the rank's rows.
 cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,

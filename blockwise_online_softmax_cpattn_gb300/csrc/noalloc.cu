@@ -21,8 +21,9 @@
 #include "kernels.h"
 
 // Scratch size: the float32 per-query-row statistics of the backward for up to
-// 2,097,152 query rows (B * H_q * T), two 8 MiB sections.
-static constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+// 2,097,152 query rows (B * H_q * T), two 8 MiB sections, and the 256 bytes of the
+// dQ kernel's item counter.
+static constexpr size_t kNoAllocScratchBytes = (size_t(16) << 20) + 256;
 
 static __device__ __align__(256) float g_bwd_scratch[kNoAllocScratchBytes / sizeof(float)];
 

@@ -79,6 +79,9 @@ struct Params {
   // test hook: kFaultDkdv / kFaultDq make that kernel's producer withhold its first
   // query-side load, so the bounded waits on it run out (50 ms under any hook value)
   int debug_fault;
+  // dQ kernel: an item counter, zero at launch, from which the CTAs claim their
+  // items in the heaviest-first order (nullptr: each CTA takes a fixed share)
+  int* claim;
 };
 
 // Query tiles of rank r at positions >= kpos0 (chunk bounds and kpos0 lie on the
@@ -182,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Params p) {
   using L = DkdvSmem<D>;
   constexpr int QS = L::kQStages, DS = L::kDOStages;
+  // a dQ kernel launched as this grid's programmatic dependent may start once every
+  // CTA of this grid has started (it reads nothing that this kernel writes)
+  griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the layout has no alignment slack
     if (threadIdx.x == 0) latch_status(p.status, kStatusLaunch);
@@ -767,10 +773,13 @@ struct DqSmem {
   // qdo_full, qdo_empty (released by the S and the dP issuer), k_full[KS], k_empty[KS],
   // v_full[VS], v_empty[VS], s_full, s_free, dp_full[2], ds_full[2] (one per dP
   // buffer), dq_done[2], dq_free, final_q (dQ issuer), final_s (S issuer), final_p
-  // (dP issuer)
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 12;
+  // (dP issuer), item_full[IS], item_empty[IS]
+  static constexpr int kItemSlots = 4;  // claimed items passed from the producer to the other roles
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 12 + 2 * kItemSlots;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16 + 1024;
+  // TMEM address, abort flag, then the item slots
+  static constexpr int kItems = kMisc + 16;
+  static constexpr int kBytes = kItems + 4 * kItemSlots + 1024;
 };
 
 // One work item of the dQ kernel: a 128-row query tile of one (batch, head), the
@@ -812,6 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t final_q = s_full + 72;
   const uint32_t final_s = s_full + 80;
   const uint32_t final_p = s_full + 88;
+  constexpr int IS = L::kItemSlots;
+  auto item_full = [&](int s) { return s_full + 96 + 8 * s; };
+  auto item_empty = [&](int s) { return s_full + 96 + 8 * (IS + s); };
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItems);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -825,7 +838,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < L::kNumBars; ++i) {
       const uint32_t b = bars + 8 * i;
       const bool compute_arrivals = b == s_free || b == ds_full(0) || b == ds_full(1) || b == dq_free;
-      mbar_init(b, compute_arrivals ? 256 : b == qdo_empty ? 2 : 1);
+      // an item slot is released by one lane of each of the 11 warps other than the producer's
+      const bool slot_release = b >= item_empty(0) && b < item_empty(IS);
+      mbar_init(b, compute_arrivals ? 256 : b == qdo_empty ? 2 : slot_release ? 11 : 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -900,6 +915,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     w.next();
     if constexpr (!PK) w.settle_keys(it.qpos0);
   };
+  // The k-th item of this CTA.  Fixed shares (no counter): item_of's order.  With the
+  // counter, the producer claims the next item (heaviest first over the whole grid,
+  // so CTAs that start late, or run slow, simply take fewer) and passes it to the
+  // other warps through a ring of shared-memory slots; -1 ends every role's loop.
+  const bool claimed = p.claim != nullptr;
+  auto claim_item = [&](int k, bool& ok) -> int {  // producer thread
+    if (!claimed) return item_of(k, n_items);
+    int w = atomicAdd(p.claim, 1);
+    if (w >= n_items) w = -1;
+    const int s = k % IS;
+    if (k >= IS && !(ok = mbar_wait(item_empty(s), ((k / IS) - 1) & 1, abort, p.status, tmo)))
+      return -1;
+    item_slot[s] = w;
+    mbar_arrive(item_full(s));
+    return w;
+  };
+  auto take_item = [&](int k, bool& ok) -> int {  // whole warps
+    if (!claimed) return item_of(k, n_items);
+    const int s = k % IS;
+    if (!(ok = warp_wait(item_full(s), (k / IS) & 1, abort, p.status, tmo))) return -1;
+    const int w = item_slot[s];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(item_empty(s));
+    return w;
+  };
 
   if (warp < 4) {
   regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2, 3)
@@ -914,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q_last = -1;
       bool ok = true;
       int w;
-      for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+      for (int k = 0; ok && (w = claim_item(k, ok)) >= 0; ++k) {
         const DqItem it = decode(w);
         // Q and dO of this item once the S and dP issuers are done with the last one's
         if (k > 0 && !(ok = mbar_wait(qdo_empty, (k - 1) & 1, abort, p.status, tmo))) break;
@@ -977,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;  // tiles so far over all items
       bool ok = true;
       int w;
-      for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+      for (int k = 0; ok && (w = take_item(k, ok)) >= 0; ++k) {
         const DqItem it = decode(w);
         if (!(ok = warp_wait(qdo_full, k & 1, abort, p.status, tmo))) break;
         Walk wk;
@@ -1037,7 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;
       bool ok = true;
       int w;
-      for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+      for (int k = 0; ok && (w = take_item(k, ok)) >= 0; ++k) {
         const DqItem it = decode(w);
         int t = 0;  // tile of this item
         Walk wk;
@@ -1081,7 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;
     bool ok = true;
     int w;
-    for (int k = 0; ok && (w = item_of(k, n_items)) >= 0; ++k) {
+    for (int k = 0; ok && (w = take_item(k, ok)) >= 0; ++k) {
       const DqItem it = decode(w);
       const int* lo_row = doc_row(it);
       const int lo_q = PK ? lo_row[it.qpos0 + row] : 0;  // packed: first key of the document
@@ -1231,6 +1271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // launched as the dK/dV kernel's programmatic dependent: finish only after that
+  // grid has completed (a no-op for any other launch)
+  griddep_wait();
 }
 
 template <typename K>
@@ -1239,6 +1282,7 @@ static cudaError_t prep(K kern, int smem) {
   if (e != cudaSuccess) return e;
   return check_register_split(kern, kThreads);
 }
+
 
 template <int D>
 static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, const void* k,
@@ -1269,6 +1313,7 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   Params pk = base;
   pk.out0 = dk;
   pk.out1 = dv;
+  pk.claim = nullptr;
   const bool packed = base.doc_lo != nullptr;  // ring mode only (checked by the caller)
   auto kdkdv = ag ? dkdv_kernel<D, true, false>
                   : (packed ? dkdv_kernel<D, false, true> : dkdv_kernel<D, false, false>);
@@ -1276,17 +1321,6 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   if (e != cudaSuccess) return e;
   const bool step = ag && base.kv_chunk >= 0;  // one ring step: the chunk's K/V tiles only
   const int kv_items = R.B * R.Hkv * ((step ? R.T / R.cp : R.T) / kTile);
-  timing_begin(step     ? "tc_partial_dkdv"
-               : ag     ? "tc_allgather_dkdv"
-               : packed ? "tc_packed_dkdv"
-                        : "tc_bwd_dkdv",
-               st);
-  kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, pk);
-  e = cudaGetLastError();
-  timing_end(st);
-  if (e != cudaSuccess) return e;
-  if (after != nullptr && after->fn != nullptr && (e = after->fn(after->ctx, st)) != cudaSuccess)
-    return e;
   Params pq = base;
   pq.out0 = dq;
   pq.out1 = nullptr;
@@ -1299,11 +1333,56 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
+  const int q_grid = q_items < sms ? q_items : sms;
   // dQ in parts (plain ring only): part j is the j-th contiguous np-th of every tensor,
   // batch rows when np divides B, else K/V heads (with their query heads) of each row
   const int np = dq_parts != nullptr && dq_parts->fn != nullptr ? dq_parts->parts : 1;
   const bool split = np > 1 && !ag && !packed &&
                      (R.B % np == 0 || (np % R.B == 0 && R.Hkv % (np / R.B) == 0));
+
+  // The dK/dV and dQ kernels read the same inputs and write disjoint outputs, so they
+  // may overlap.  The dK/dV kernel's CTAs differ in work by up to 64 times (a key
+  // tile is seen by the query tiles at or after it), and its last ones leave SMs
+  // idle while they finish.  With an item counter (ring problems, nothing queued
+  // between the two kernels) the dQ kernel is launched as a programmatic dependent
+  // of the dK/dV kernel, whose CTAs release it as they start: once the last dK/dV
+  // CTA is resident the persistent dQ CTAs take the SMs that the dK/dV kernel frees,
+  // claiming their items from the counter, and each waits for the dK/dV grid to
+  // complete before it exits, so the stream's next work sees both kernels' results.
+  if (base.claim != nullptr && !ag && after == nullptr && np == 1) {
+    if ((e = cudaMemsetAsync(base.claim, 0, sizeof(int), st)) != cudaSuccess) return e;
+    timing_begin(packed ? "tc_packed_dkdv_dq" : "tc_bwd_dkdv_dq", st);
+    kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, pk);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)q_grid);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = DqSmem<D>::kBytes;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, kdq, tq, tk, tv, tdo, pq);
+    }
+    timing_end(st);
+    return e;
+  }
+  pq.claim = nullptr;
+
+  timing_begin(step     ? "tc_partial_dkdv"
+               : ag     ? "tc_allgather_dkdv"
+               : packed ? "tc_packed_dkdv"
+                        : "tc_bwd_dkdv",
+               st);
+  kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, pk);
+  e = cudaGetLastError();
+  timing_end(st);
+  if (e != cudaSuccess) return e;
+  if (after != nullptr && after->fn != nullptr && (e = after->fn(after->ctx, st)) != cudaSuccess)
+    return e;
   if (split) {
     const int m = R.B % np == 0 ? 1 : np / R.B;  // parts per batch row
     const int Bp = R.B % np == 0 ? R.B / np : 1, Hqp = R.Hq / m, Hkvp = R.Hkv / m;
@@ -1341,7 +1420,7 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
                : packed ? "tc_packed_dq"
                         : "tc_bwd_dq",
                st);
-  kdq<<<q_items < sms ? q_items : sms, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
+  kdq<<<q_grid, kThreads, DqSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, pq);
   e = cudaGetLastError();
   timing_end(st);
   if (e == cudaSuccess && np > 1)
@@ -1373,6 +1452,7 @@ static tcbwd::Params bwd_params(const Ring& R, const float* lse2, const float* d
   p.ord_q = nullptr;
   p.ord_k = nullptr;
   p.debug_fault = R.debug_fault;
+  p.claim = nullptr;
   return p;
 }
 
@@ -1380,12 +1460,13 @@ cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const voi
                           const float* lse2, const float* delta, const void* dO, void* dq,
                           void* dk, void* dv, int* status, cudaStream_t st, const int* doc_lo,
                           const int* doc_hi, const int* ord_q, const int* ord_k,
-                          const AfterDkdv* after, const AfterDqPart* dq_parts) {
+                          const AfterDkdv* after, const AfterDqPart* dq_parts, int* dq_claim) {
   tcbwd::Params p = bwd_params(R, lse2, delta, status);
   p.doc_lo = doc_lo;
   p.doc_hi = doc_hi;
   p.ord_q = ord_q;
   p.ord_k = ord_k;
+  p.claim = dq_claim;
   if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq, dk, dv, st, after, dq_parts);
   return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq, dk, dv, st, after, dq_parts);
 }

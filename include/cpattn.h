@@ -193,7 +193,8 @@ cpattn_status cpattn_merge(int64_t rows, int D, const float* o_a, const float* l
 cpattn_status cpattn_ring_fwd(const cpattn_desc* desc, const void* q, const void* k,
                               const void* v, void* o, float* lse, void* stream);
 
-/* Bytes of device workspace cpattn_ring_bwd needs (float32 row statistics). */
+/* Bytes of device workspace cpattn_ring_bwd needs (float32 row statistics and a
+ * 256-byte work counter). */
 size_t cpattn_ring_bwd_workspace(const cpattn_desc* desc);
 
 /*
@@ -204,6 +205,10 @@ size_t cpattn_ring_bwd_workspace(const cpattn_desc* desc);
  * slice of dk/dv is what its owner receives.  `workspace` is device scratch of at
  * least cpattn_ring_bwd_workspace(desc) bytes (ws_bytes smaller ->
  * CPATTN_ERR_INVALID_ARG); its contents on entry do not matter.
+ * On the tensor-core path the dQ kernel is launched as a programmatic dependent
+ * of the dK/dV kernel on `stream` (it starts on the SMs that the dK/dV kernel's
+ * last CTAs leave idle), and completes only after the dK/dV kernel has: work
+ * queued on `stream` afterwards sees every result.
  */
 cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void* k,
                               const void* v, const void* o, const float* lse,
@@ -218,10 +223,10 @@ cpattn_status cpattn_ring_bwd(const cpattn_desc* desc, const void* q, const void
  * while a step runs, cannot provide the workspace cpattn_ring_bwd asks for.
  * This call computes exactly what cpattn_ring_bwd computes (same arguments
  * minus the workspace) and uses instead a scratch array compiled into the
- * library: 16 MiB of device memory that every GPU loading the library holds
- * until the process exits.  It allocates nothing, on the device or through any
- * allocating library routine.
- *   Limit: cpattn_ring_bwd_workspace(desc) <= 16 MiB, i.e. B * H_q * T <=
+ * library: 16 MiB and 256 bytes of device memory that every GPU loading the
+ * library holds until the process exits.  It allocates nothing, on the device or
+ * through any allocating library routine.
+ *   Limit: cpattn_ring_bwd_workspace(desc) <= 16 MiB + 256 bytes, i.e. B * H_q * T <=
  *   2,097,152 query rows; larger problems return CPATTN_ERR_UNSUPPORTED before
  *   anything is enqueued.
  *   Set-up: the first call on a device looks up the scratch's device address
@@ -284,7 +289,7 @@ cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const void* q, cons
  *               (but finite, in-bounds) results.
  *   workspace : at least cpattn_packed_workspace(desc) bytes (the documents of
  *               every position, the 128-token tiles in order of decreasing work,
- *               and for the backward the row statistics)
+ *               and for the backward the row statistics and a work counter)
  * Errors: n_docs < 1, null or misaligned starts, workspace too small ->
  * CPATTN_ERR_INVALID_ARG; desc->a2a != 1 -> CPATTN_ERR_UNSUPPORTED; others as
  * cpattn_ring_fwd / cpattn_ring_bwd.

@@ -170,3 +170,27 @@ def test_traffic_is_keyed_to_the_kernels_own_sources(tmp_path, monkeypatch):
     assert bench.traffic_for("tc_ring_fwd", "wl") == 123.0
     (csrc / "common.cuh").write_text("#pragma once\nconstexpr int k = 1;\n")
     assert bench.traffic_for("tc_ring_fwd", "wl") is None
+
+
+def test_traffic_of_a_unit_is_the_sum_over_its_kernels(tmp_path, monkeypatch):
+    """The backward's dK/dV and dQ kernels, timed as one unit when the dQ kernel
+    overlaps the end of the dK/dV kernel, report the sum of their captured DRAM
+    bytes, and nothing once either capture is missing or stale."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    csrc = tmp_path / "blockwise_online_softmax_cpattn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    for f, text in (("tc_bwd.cu", "int bwd() { return 1; }\n"), ("common.cuh", "#pragma once\n"),
+                    ("kernels.h", "#pragma once\n")):
+        (csrc / f).write_text(text)
+    digest = bench.source_digest(bench.KERNEL_SOURCES["tc_bwd_dkdv"])
+    path = tmp_path / "profiles" / "ncu_traffic.txt"
+    path.write_text(f"tc_bwd_dkdv wl 100 {digest}\ntc_bwd_dq wl 23 {digest}\n")
+    assert bench.traffic_for("tc_bwd_dkdv_dq", "wl") == 123.0
+    path.write_text(f"tc_bwd_dkdv wl 100 {digest}\n")
+    assert bench.traffic_for("tc_bwd_dkdv_dq", "wl") is None
+    assert bench.kernel_flops_or_bytes("tc_bwd_dkdv_dq", W.LLAMA) == \
+        ("tensor", 10.0 * W.LLAMA.D * W.LLAMA.attended_pairs)
