@@ -13,12 +13,13 @@
 //                    group j; then the same for j + 1
 //   caller's stream  per backward group j: for its forward groups, permute q, k, v
 //                    to layout order, ring forward, permute o and LSE back; then
-//                    permute dO, ring backward with dk and dv permuted back between
-//                    its dK/dV and dQ kernels, permute dq back
+//                    permute dO, ring backward (its dQ kernel overlapping the end of
+//                    its dK/dV kernel), permute dk, dv and dq back; in the last group
+//                    dk and dv are permuted back between the two kernels instead
 //   download stream  o and LSE of a forward group as soon as it is done; dk and dv
-//                    of a backward group while its dQ kernel runs; dq once its
-//                    backward is done (the last group's in two parts, the first
-//                    while the second part's dQ kernel runs)
+//                    of a backward group once permuted (the last group's while its
+//                    dQ kernel runs); dq once its backward is done (the last group's
+//                    in two parts, the first while the second part's dQ kernel runs)
 //
 // so the first kernel waits only for the first forward group's inputs, uploads
 // run while earlier groups compute, downloads while later ones do, and only the
@@ -314,12 +315,19 @@ extern "C" cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const vo
     dqo.bytes = qb / kDqParts;
     for (int part = 0; part < kDqParts; ++part) dqo.done[part] = ev_dq(part);
     const AfterDqPart after_dq{dq_out, &dqo, kDqParts};
+    // Before the last group, nothing waits for dk and dv: the group's dQ kernel may then
+    // overlap the end of its dK/dV kernel (nothing queued between them), and dk, dv go
+    // back to natural order after both.  The last group's dk and dv go home while its
+    // dQ kernel runs.
+    const bool last = j == nb - 1;
     CPATTN_TRY_S(ring_bwd_after_dkdv(&gb, dev_at(L.lay_q, j, qb), dev_at(L.lay_k, j, kb),
                                      dev_at(L.lay_v, j, kb), dev_at(L.lay_o, j, qb),
                                      reinterpret_cast<float*>(dev_at(L.lay_lse, j, lb)),
                                      dev_at(L.lay_do, j, qb), dev_at(L.lay_dq, j, qb),
                                      dev_at(L.lay_dk, j, kb), dev_at(L.lay_dv, j, kb),
-                                     w + L.bwd_ws, L.bwd, st, &after, parts ? &after_dq : nullptr));
+                                     w + L.bwd_ws, L.bwd, st, last ? &after : nullptr,
+                                     parts ? &after_dq : nullptr));
+    if (!last) CPATTN_TRY(dkdv_out(&out, st));
     CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_dkdv(j), 0));
     CPATTN_TRY(cudaMemcpyAsync(host_out(dk, j, kb), out.dst[0], kb, cudaMemcpyDeviceToHost,
                                cs->down));
