@@ -219,6 +219,8 @@ def kernel_flops_or_bytes(name, w, pairs=None):
         return "tensor", 8.0 * w.D * pairs / w.cp
     if name == "tc_allgather_dq":
         return "tensor", 2.0 * w.D * pairs / w.cp
+    if name == "tc_allgather_dkdv_dq":
+        return "tensor", 10.0 * w.D * pairs / w.cp
     if name == "bwd_prepass":
         return "hbm", 2.0 * rows_q * w.D * elt + 12.0 * rows_q
     if name in ("layout_zigzag_batch", "layout_a2a_batch"):

@@ -410,7 +410,7 @@ static size_t ag_section(const Ring& R) {
 size_t cpattn_allgather_bwd_workspace(const cpattn_desc* desc) {
   Ring R;
   if (validate(desc, &R) != CPATTN_OK) return 0;
-  return 2 * ag_section(R);
+  return 2 * ag_section(R) + kClaimBytes;  // Delta, LSE in base 2, the dQ item counter
 }
 
 cpattn_status cpattn_allgather_bwd(const cpattn_desc* desc, int q_rank, const void* q,
@@ -432,13 +432,14 @@ cpattn_status cpattn_allgather_bwd(const cpattn_desc* desc, int q_rank, const vo
   cudaGetLastError();
   float* delta = static_cast<float*>(workspace);
   float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ag_section(R));
+  int* claim = reinterpret_cast<int*>(static_cast<char*>(workspace) + 2 * ag_section(R));
   const int64_t rows = (int64_t)R.B * R.Hq * (R.T / R.cp);
   const bool tc = R.bf16 && tc_supported(R);
   cudaError_t e = launch_delta(rows, R.D, R.bf16, o, dO, lse, delta, tc ? lse2 : nullptr, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   if (tc)
     return from_cuda(launch_tc_allgather_bwd(R, q_rank, q, k, v, lse2, delta, dO, dq, dk_sum,
-                                             dv_sum, accumulate, status_ptr(), st));
+                                             dv_sum, accumulate, status_ptr(), st, claim));
   return from_cuda(launch_simt_allgather_bwd(R, q_rank, q, k, v, lse, delta, dO, dq, dk_sum,
                                              dv_sum, accumulate, st));
 }

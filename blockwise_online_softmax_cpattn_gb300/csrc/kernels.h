@@ -120,11 +120,13 @@ cudaError_t launch_tc_bwd(const Ring& R, const void* q, const void* k, const voi
                           const AfterDkdv* after = nullptr, const AfterDqPart* dq_parts = nullptr,
                           int* dq_claim = nullptr);
 // All-gather mode backward of rank q_rank (see launch_simt_allgather_bwd); lse2 /
-// delta are the pre-pass statistics of the rank's rows.
+// delta are the pre-pass statistics of the rank's rows; dq_claim (optional) as for
+// launch_tc_bwd.
 cudaError_t launch_tc_allgather_bwd(const Ring& R, int q_rank, const void* q, const void* k,
                                     const void* v, const float* lse2, const float* delta,
                                     const void* dO, void* dq, float* dk_sum, float* dv_sum,
-                                    int accumulate, int* status, cudaStream_t st);
+                                    int accumulate, int* status, cudaStream_t st,
+                                    int* dq_claim = nullptr);
 
 // One ring step of the backward (see launch_simt_partial_bwd); lse2 / delta are the
 // pre-pass statistics of the rank's rows.

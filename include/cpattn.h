@@ -119,7 +119,8 @@ cpattn_status cpattn_partial_fwd(const cpattn_desc* desc, int q_rank, int kv_ran
                                  float* o_part, float* lse_part, void* stream);
 
 /* Bytes of device workspace that holds one rank's row statistics for
- * cpattn_partial_bwd (float32, two values per query row of the rank). */
+ * cpattn_partial_bwd (float32, two values per query row of the rank; the size of
+ * cpattn_allgather_bwd's workspace, whose last 256 bytes this call leaves unused). */
 size_t cpattn_partial_bwd_workspace(const cpattn_desc* desc);
 
 /*
@@ -322,7 +323,8 @@ cpattn_status cpattn_allgather_fwd(const cpattn_desc* desc, int q_rank, const vo
                                    void* stream);
 
 /* Bytes of device workspace cpattn_allgather_bwd needs (float32 row statistics of
- * one rank's rows). */
+ * one rank's rows and a 256-byte work counter; on the tensor-core path the call's
+ * dQ kernel overlaps the end of its dK/dV kernel, as in cpattn_ring_bwd). */
 size_t cpattn_allgather_bwd_workspace(const cpattn_desc* desc);
 
 /*
