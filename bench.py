@@ -213,6 +213,8 @@ def kernel_flops_or_bytes(name, w, pairs=None):
         return "tensor", 8.0 * w.D * pairs / w.cp ** 2
     if name == "tc_partial_dq":
         return "tensor", 2.0 * w.D * pairs / w.cp ** 2
+    if name == "tc_partial_dkdv_dq":
+        return "tensor", 10.0 * w.D * pairs / w.cp ** 2
     if name == "tc_allgather_fwd":
         return "tensor", 4.0 * w.D * pairs / w.cp
     if name == "tc_allgather_dkdv":

@@ -478,7 +478,7 @@ cpattn_status cpattn_partial_bwd_stats(const cpattn_desc* desc, const void* o, c
 cpattn_status cpattn_partial_bwd(const cpattn_desc* desc, int q_rank, int kv_rank,
                                  const void* q, const void* k, const void* v, const void* dO,
                                  float* dq_part, float* dk_part, float* dv_part, int accumulate,
-                                 const void* workspace, size_t ws_bytes, void* stream) {
+                                 void* workspace, size_t ws_bytes, void* stream) {
   Ring R;
   cpattn_status s = validate(desc, &R);
   if (s != CPATTN_OK) return s;
@@ -494,9 +494,10 @@ cpattn_status cpattn_partial_bwd(const cpattn_desc* desc, int q_rank, int kv_ran
   const float* delta = static_cast<const float*>(workspace);
   const float* sec1 =
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + ag_section(R));
+  int* claim = reinterpret_cast<int*>(static_cast<char*>(workspace) + 2 * ag_section(R));
   if (R.bf16 && tc_supported(R))
     return from_cuda(launch_tc_partial_bwd(R, q_rank, kv_rank, q, k, v, sec1, delta, dO, dq_part,
-                                           dk_part, dv_part, accumulate, status_ptr(), st));
+                                           dk_part, dv_part, accumulate, status_ptr(), st, claim));
   return from_cuda(launch_simt_partial_bwd(R, q_rank, kv_rank, q, k, v, sec1, delta, dO, dq_part,
                                            dk_part, dv_part, accumulate, st));
 }

@@ -134,7 +134,7 @@ cudaError_t launch_tc_partial_bwd(const Ring& R, int q_rank, int kv_rank, const 
                                   const void* k, const void* v, const float* lse2,
                                   const float* delta, const void* dO, float* dq_part,
                                   float* dk_part, float* dv_part, int accumulate, int* status,
-                                  cudaStream_t st);
+                                  cudaStream_t st, int* dq_claim = nullptr);
 
 // The register split of the tensor-core kernels (3 warpgroups: one control, two
 // math) must fit in what a launch of `kern` allocates; a split that does not fit

@@ -1343,15 +1343,19 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   // The dK/dV and dQ kernels read the same inputs and write disjoint outputs, so they
   // may overlap.  The dK/dV kernel's CTAs differ in work by up to 64 times (a key
   // tile is seen by the query tiles at or after it), and its last ones leave SMs
-  // idle while they finish.  With an item counter (ring and all-gather problems,
-  // nothing queued between the two kernels) the dQ kernel is launched as a programmatic dependent
+  // idle while they finish.  With an item counter (nothing queued between the two
+  // kernels) the dQ kernel is launched as a programmatic dependent
   // of the dK/dV kernel, whose CTAs release it as they start: once the last dK/dV
   // CTA is resident the persistent dQ CTAs take the SMs that the dK/dV kernel frees,
   // claiming their items from the counter, and each waits for the dK/dV grid to
   // complete before it exits, so the stream's next work sees both kernels' results.
-  if (base.claim != nullptr && !step && after == nullptr && np == 1) {
+  if (base.claim != nullptr && after == nullptr && np == 1) {
     if ((e = cudaMemsetAsync(base.claim, 0, sizeof(int), st)) != cudaSuccess) return e;
-    timing_begin(ag ? "tc_allgather_dkdv_dq" : packed ? "tc_packed_dkdv_dq" : "tc_bwd_dkdv_dq", st);
+    timing_begin(step     ? "tc_partial_dkdv_dq"
+                 : ag     ? "tc_allgather_dkdv_dq"
+                 : packed ? "tc_packed_dkdv_dq"
+                          : "tc_bwd_dkdv_dq",
+                 st);
     kdkdv<<<kv_items, kThreads, DkdvSmem<D>::kBytes, st>>>(tq, tk, tv, tdo, tdk, tdv, pk);
     e = cudaGetLastError();
     if (e == cudaSuccess) {
@@ -1475,11 +1479,12 @@ cudaError_t launch_tc_partial_bwd(const Ring& R, int q_rank, int kv_rank, const 
                                   const void* k, const void* v, const float* lse2,
                                   const float* delta, const void* dO, float* dq_part,
                                   float* dk_part, float* dv_part, int accumulate, int* status,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, int* dq_claim) {
   tcbwd::Params p = bwd_params(R, lse2, delta, status);
   p.ag_rank = q_rank;
   p.kv_chunk = kv_rank;
   p.accumulate = accumulate ? 1 : 0;
+  p.claim = dq_claim;
   if (R.D == 128) return tcbwd::run_bwd<128>(R, p, q, k, v, dO, dq_part, dk_part, dv_part, st);
   return tcbwd::run_bwd<64>(R, p, q, k, v, dO, dq_part, dk_part, dv_part, st);
 }

@@ -119,8 +119,8 @@ cpattn_status cpattn_partial_fwd(const cpattn_desc* desc, int q_rank, int kv_ran
                                  float* o_part, float* lse_part, void* stream);
 
 /* Bytes of device workspace that holds one rank's row statistics for
- * cpattn_partial_bwd (float32, two values per query row of the rank; the size of
- * cpattn_allgather_bwd's workspace, whose last 256 bytes this call leaves unused). */
+ * cpattn_partial_bwd (float32, two values per query row of the rank) and its
+ * 256-byte work counter: the size of cpattn_allgather_bwd's workspace. */
 size_t cpattn_partial_bwd_workspace(const cpattn_desc* desc);
 
 /*
@@ -150,7 +150,10 @@ cpattn_status cpattn_partial_bwd_stats(const cpattn_desc* desc, const void* o, c
  *                 query slots and kv_rank's key slots are read)
  *   dO          : rank q_rank's rows of the upstream gradient, [B', H_q', c, D]
  *   workspace   : the rank's statistics, as cpattn_partial_bwd_stats left them for
- *                 the same rank's o, lse and dO (read only)
+ *                 the same rank's o, lse and dO (read only), and after them a
+ *                 256-byte work counter that the call writes: the step's dQ kernel
+ *                 overlaps the end of its dK/dV kernel, as in cpattn_ring_bwd.
+ *                 Calls that share a workspace must be ordered (one stream).
  *   dq_part     : [B', H_q', c, D] float32, the step's dQ contribution to the
  *                 rank's rows
  *   dk_part, dv_part : [B', H_kv', c, D] float32, the step's dK / dV contribution
@@ -169,7 +172,7 @@ cpattn_status cpattn_partial_bwd_stats(const cpattn_desc* desc, const void* o, c
 cpattn_status cpattn_partial_bwd(const cpattn_desc* desc, int q_rank, int kv_rank,
                                  const void* q, const void* k, const void* v, const void* dO,
                                  float* dq_part, float* dk_part, float* dv_part, int accumulate,
-                                 const void* workspace, size_t ws_bytes, void* stream);
+                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Online-softmax merge of two partial results over disjoint key sets (tutorial,

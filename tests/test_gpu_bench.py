@@ -95,8 +95,10 @@ def test_bench_p2p_ring_emulated_gpt2():
     assert out["unit"] == "TFLOP/s" and out["value"] > 0 and out["n_gpus"] == 1
     assert out["config"]["mode"] == "p2p" and out["config"]["graph"] is True
     names = set(out["kernels"])
-    assert {"tc_partial_fwd", "merge", "tc_partial_dkdv", "tc_partial_dq"} <= names
-    # cp^2 forward steps per training step, over the min(steps, 5) steps of the
-    # per-kernel timing pass
+    # each step's dQ kernel overlaps the end of its dK/dV kernel: timed as one unit
+    assert {"tc_partial_fwd", "merge", "tc_partial_dkdv_dq"} <= names
+    # cp^2 forward and backward steps per training step, over the min(steps, 5) steps
+    # of the per-kernel timing pass
     assert out["kernels"]["tc_partial_fwd"]["launches"] == min(STEPS, 5) * 4 * 4
+    assert out["kernels"]["tc_partial_dkdv_dq"]["launches"] == min(STEPS, 5) * 4 * 4
     assert out["roofline"]["frac"] < 2.0
