@@ -3,7 +3,8 @@
 // The pull request "Feat: Context Parallel" #181 (mode "p2p") computes the ring
 // backward by recomputing the probabilities from the saved statistics and
 // sending each K/V chunk's gradient around the ring back to its owner.  On one
-// GPU the same sums are formed by two kernels, neither of which needs atomics:
+// GPU the same sums are formed by two kernels, neither of which adds its results
+// with atomics (each output tile is summed by one CTA, in a fixed order):
 //
 //  dkdv_kernel  one CTA per 128-row K/V tile (K/V stationary in shared memory).
 //               It walks the query tiles that can see it, in the order the
