@@ -194,3 +194,12 @@ def test_traffic_of_a_unit_is_the_sum_over_its_kernels(tmp_path, monkeypatch):
     assert bench.traffic_for("tc_bwd_dkdv_dq", "wl") is None
     assert bench.kernel_flops_or_bytes("tc_bwd_dkdv_dq", W.LLAMA) == \
         ("tensor", 10.0 * W.LLAMA.D * W.LLAMA.attended_pairs)
+
+
+def test_launch_count_counts_both_kernels_of_an_overlapped_pair():
+    """The dK/dV + dQ pair is one timing entry but two kernel launches."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.kernels_in("tc_bwd_dkdv_dq") == 2
+    assert bench.kernels_in("tc_partial_dkdv_dq") == 2
+    assert bench.kernels_in("tc_ring_fwd") == 1 and bench.kernels_in("tc_bwd_dkdv") == 1
