@@ -1284,7 +1284,6 @@ static cudaError_t prep(K kern, int smem) {
   return check_register_split(kern, kThreads);
 }
 
-
 template <int D>
 static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, const void* k,
                            const void* v, const void* dO, void* dq, void* dk, void* dv,
@@ -1345,9 +1344,9 @@ static cudaError_t run_bwd(const Ring& R, const Params& base, const void* q, con
   // may overlap.  The dK/dV kernel's CTAs differ in work by up to 64 times (a key
   // tile is seen by the query tiles at or after it), and its last ones leave SMs
   // idle while they finish.  With an item counter (nothing queued between the two
-  // kernels) the dQ kernel is launched as a programmatic dependent
-  // of the dK/dV kernel, whose CTAs release it as they start: once the last dK/dV
-  // CTA is resident the persistent dQ CTAs take the SMs that the dK/dV kernel frees,
+  // kernels) the dQ kernel is launched as a programmatic dependent of the dK/dV
+  // kernel, whose CTAs release it as they start: once the last dK/dV CTA is
+  // resident, the persistent dQ CTAs take the SMs that the dK/dV kernel frees,
   // claiming their items from the counter, and each waits for the dK/dV grid to
   // complete before it exits, so the stream's next work sees both kernels' results.
   if (base.claim != nullptr && after == nullptr && np == 1) {
