@@ -16,7 +16,9 @@
 //                    permute dO, ring backward (its dQ kernel overlapping the end of
 //                    its dK/dV kernel), permute dk, dv and dq back; in the last group
 //                    dk and dv are permuted back between the two kernels instead
-//   download stream  o and LSE of a forward group as soon as it is done; dk and dv
+//   download stream  (once every upload is done: the two directions share the host
+//                    link, and only the first uploads are on the compute's path)
+//                    o and LSE of a forward group as soon as it is done; dk and dv
 //                    of a backward group once permuted (the last group's while its
 //                    dQ kernel runs); dq once its backward is done (the last group's
 //                    in two parts, the first while the second part's dQ kernel runs)
@@ -266,6 +268,9 @@ extern "C" cpattn_status cpattn_ring_step_host(const cpattn_desc* desc, const vo
                                cudaMemcpyHostToDevice, cs->up));
     CPATTN_TRY(cudaEventRecord(ev_do(j), cs->up));
   }
+  // downloads start once every upload is done: the two directions share the host
+  // link, and the first uploads are on the compute's critical path
+  CPATTN_TRY(cudaStreamWaitEvent(cs->down, ev_do(nb - 1), 0));
   for (int j = 0; j < nb; ++j) {
     // forward of the group's forward groups; o and LSE go back to natural order and home
     for (int f = j * r; f < (j + 1) * r; ++f) {
