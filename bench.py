@@ -529,9 +529,10 @@ def run_cpattn(args, rank, world):
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "transfers": ("one cpattn_ring_step_host call per step on pinned host buffers: the "
-                         "library splits the problem into independent halves and overlaps one "
-                         "half's uploads and downloads with the other's compute on its own "
-                         "copy streams, all inside each step's events"
+                         "library runs the problem as independent groups (forward quarters, "
+                         "backward halves) and overlaps their uploads and downloads with "
+                         "other groups' compute on its own copy streams, all inside each "
+                         "step's events"
                          if host_step else
                          "pinned host buffers (the ranks' token shards for the a2a layout); dO "
                          "upload overlaps the forward and o download overlaps the backward on "
