@@ -112,6 +112,33 @@ struct TileWalk {
       else end_pass();          // the rest of this pass is hidden
     }
   }
+
+  // Key-stationary walks over query tiles (a K/V tile at k0 is seen by the query
+  // tiles at or after its position): inside a pass the visible query tiles are a
+  // suffix, so at the start of each pass jump to its first visible tile, or past the
+  // chunk when none of its tiles is visible.  The tiles visited, and their order, are
+  // those of stepping through every tile and skipping the hidden ones.
+  __device__ __forceinline__ void settle_queries(int k0) {
+    while (!done() && t == 0) {
+      int f;  // first tile of the pass at or after k0 (tpc: none)
+      if (!zz) {
+        const int p0 = s * c;
+        f = k0 <= p0 ? 0 : k0 < p0 + c ? (k0 - p0) >> 7 : tpc;
+      } else {
+        const int e0 = s * h, l0 = (2 * cp - 1 - s) * h, th = h >> 7;
+        f = k0 <= e0 ? 0
+            : k0 < e0 + h ? (k0 - e0) >> 7
+            : k0 <= l0 ? th
+            : k0 < l0 + h ? th + ((k0 - l0) >> 7)
+            : tpc;
+      }
+      if (f < tpc) {
+        t = f;
+        return;
+      }
+      end_chunk();
+    }
+  }
 };
 
 // Walk over the 128-token tiles of a range of NATURAL positions, tiles

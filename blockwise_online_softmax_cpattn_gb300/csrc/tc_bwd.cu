@@ -175,7 +175,9 @@ struct DkdvSmem {
   // s_issued, dp_issued
   static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  // TMEM address, abort flag, then the first query position of each Q stage's tile
+  static constexpr int kQPos = kMisc + 8;
+  static constexpr int kBytes = kQPos + 4 * kQStages + 4;
 };
 
 template <int D, bool AG, bool PK>
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t dp_issued = s_full + 64;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  volatile int* stage_qpos = reinterpret_cast<volatile int*>(smem + L::kQPos);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t tmo = p.debug_fault ? kDebugTimeoutNs : kTimeoutNs;
   // row extents of the tensors (for the bounds checks of a CPATTN_DEBUG build): q,
@@ -263,28 +266,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int s_own = kslot0 / p.m.c;
   // query tiles in the order the chunk's gradient travels the ring back to its
   // owner: ranks s, s+1, ..., s-1; every query head of the group per rank; tiles
-  // that cannot see this K/V tile are skipped by every role alike
+  // that cannot see this K/V tile are skipped (by the producer's walk, which the
+  // other roles follow)
   // packed sequences only in the PK instantiation, so the plain path keeps its code
   const int* lo_row = PK ? p.doc_lo + (int64_t)b * p.T : nullptr;
   // packed: the query tiles from this one up to the tile holding the end of its last
   // key's document, in natural order (every head of the group in turn)
   using Walk = std::conditional_t<PK, NatWalk, TileWalk>;
   const int pk_last = PK ? p.doc_hi[(int64_t)b * p.T + kpos0 + kTile - 1] >> 7 : 0;
+  // Only the producer walks; it jumps over the hidden query tiles (see
+  // TileWalk::settle_queries) and writes each tile's first query position next to its
+  // Q stage.  The other roles count: every query tile at or after this K/V tile's
+  // position sees it, once per query head of the group.
   auto walk_start = [&](Walk& w) {
     if constexpr (PK) {
       w.start(p.m, kpos0 >> 7, pk_last, p.n_rep);
     } else {
       if (AG) w.start(p.m, p.ag_rank, 1, +1, p.n_rep);  // all-gather: one rank's queries
       else w.start(p.m, s_own, p.m.cp, +1, p.n_rep);
-      // hidden tiles are stepped over one at a time here: jumping over them (as the
-      // query-stationary kernels do) measured 3 % slower on this kernel
-      while (!w.done() && classify(w.pos(), kpos0, nullptr) == kEmpty) w.next();
+      w.settle_queries(kpos0);
     }
   };
   auto walk_next = [&](Walk& w) {
-    if constexpr (PK) w.next();
-    else do w.next(); while (!w.done() && classify(w.pos(), kpos0, nullptr) == kEmpty);
+    w.next();
+    if constexpr (!PK) w.settle_queries(kpos0);
   };
+  const int n_tiles =
+      PK ? p.n_rep * (pk_last - (kpos0 >> 7) + 1)
+         : p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0) : (p.T - kpos0) >> 7);
 
   if (warp < 4) {
   regs_ctl();  // warpgroup 0: TMA producer (warp 0) and MMA issuers (warps 1, 2, 3)
@@ -311,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rows of dO and of the statistics (the rank's own rows in all-gather mode)
         const int srow = AG ? qbh * p.m.c + (wk.slot() - p.ag_rank * p.m.c) : qrow;
         if (!mbar_wait(q_empty(qr.stage), qr.par ^ 1, abort, p.status, tmo)) break;
+        stage_qpos[qr.stage] = wk.pos();  // published by the arrival below
         // fault hook: the first Q tile never arrives, so the waits on it run out
         if (!(p.debug_fault == kFaultDkdv && first)) {
           mbar_expect_tx(q_full(qr.stage), L::kTB + 512);
@@ -358,8 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd0 = sdesc_sw128(sbase + L::kQ, 16, 1024);
       StageRing<QS> qr;
       int cnt = 0;
-      Walk wk;
-      for (walk_start(wk); !wk.done() && ok; walk_next(wk)) {
+      for (int t = 0; t < n_tiles && ok; ++t) {
         // The tensor pipe runs MMAs in the order they are queued.  The gradient warp
         // queues ... dV(t-1), dK(t-1), dP^T(t) back to back; S^T(t+1) goes in behind
         // dP^T(t), where it runs while the compute warps turn dP^T(t) into P^T(t).
@@ -407,12 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dod_k0 = sdesc_sw128(sbase + L::kDO, 16, 1024);
       const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQ, kTile * 128, 1024);
       const uint64_t dod_mn0 = sdesc_sw128(sbase + L::kDO, kTile * 128, 1024);
-      // every query tile at or after this K/V tile's position sees it, once per
-      // query head of the group (the walk of the other roles skips the rest)
-      // packed: the natural range the walk covers, once per head of the group
-      const int n_tiles =
-          PK ? p.n_rep * (pk_last - (kpos0 >> 7) + 1)
-             : p.n_rep * (AG ? rank_tiles_from(p.m, p.ag_rank, kpos0) : (p.T - kpos0) >> 7);
       bool ok = warp_wait(kv_full, 0, abort, p.status, tmo);
       tc_fence_after();
       StageRing<QS> qr;   // Q stage of tile t
@@ -497,11 +500,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     StageRing<DS> dr;
     int cnt = 0;
     bool ok = true;
+    // packed: the query tiles form one natural range (nothing hidden), walked here
     Walk wk;
-    for (walk_start(wk); !wk.done(); walk_next(wk)) {
-      const int qpos0 = wk.pos();
-      const int cls = classify(qpos0, kpos0, lo_row);
+    if constexpr (PK) walk_start(wk);
+    for (int t = 0; t < n_tiles; ++t) {
+      int qpos0;
+      if constexpr (PK) {
+        qpos0 = wk.pos();
+        walk_next(wk);
+      }
       if (!(ok = warp_wait(q_full(qr.stage), qr.par, abort, p.status, tmo))) break;  // -LSE log2e landed
+      if constexpr (!PK) qpos0 = stage_qpos[qr.stage];
+      const int cls = classify(qpos0, kpos0, lo_row);
       const float* lse_t = lse_s + qr.stage * 128 + half * 64;
       const float* del_t = del_s + dr.stage * 128 + half * 64;
       // this half's 64 per-query LSE values, fetched while S^T is still being computed

@@ -1,9 +1,10 @@
 """Host test of the tile walk the tensor-core kernels share (csrc/common.cuh,
 TileWalk): the jumps of the query-stationary walks (forward, dQ) over the key
-tiles the causal mask hides visit exactly the tiles, in exactly the order, that
-stepping through every tile and skipping the hidden ones one by one visits.  Both
-layouts, several cp, chunk sizes, passes, first chunks and directions, every
-query tile.
+tiles the causal mask hides, and of the key-stationary walk (the dK/dV kernel's
+producer) over the query tiles that cannot see its key tile, visit exactly the
+tiles, in exactly the order, that stepping through every tile and skipping the
+hidden ones one by one visits.  Both layouts, several cp, chunk sizes, passes,
+first chunks and directions, every anchor tile.
 
 The struct is compiled from the header itself with the host compiler (its device
 qualifiers defined away), so the test checks the code the kernels use."""
@@ -46,6 +47,27 @@ static std::vector<int> jumped(const SeqMap& m, int first, int n, int dir, int r
   }
   return out;
 }
+// key-stationary: a query tile at qpos is hidden from the key tile at k0 when k0 is
+// past qpos + 127
+static std::vector<int> plain_q(const SeqMap& m, int first, int n, int dir, int reps, int k0) {
+  std::vector<int> out;
+  TileWalk w;
+  for (w.start(m, first, n, dir, reps); !w.done(); w.next())
+    if (!(k0 > w.pos() + 127)) out.push_back(w.i * 1000000 + w.rep * 10000 + w.slot() / 128);
+  return out;
+}
+static std::vector<int> jumped_q(const SeqMap& m, int first, int n, int dir, int reps, int k0) {
+  std::vector<int> out;
+  TileWalk w;
+  w.start(m, first, n, dir, reps);
+  w.settle_queries(k0);
+  while (!w.done()) {
+    out.push_back(w.i * 1000000 + w.rep * 10000 + w.slot() / 128);
+    w.next();
+    w.settle_queries(k0);
+  }
+  return out;
+}
 int main() {
   long cases = 0, bad = 0;
   const int cps[] = {1, 2, 3, 4, 5, 8};
@@ -64,6 +86,11 @@ int main() {
                       ++bad < 5)
                     std::printf("mismatch zz=%d cp=%d c=%d reps=%d first=%d n=%d dir=%d q0=%d\n",
                                 zz, cp, c, reps, first, n, dir, q0);
+                  ++cases;  // the same anchor as a key tile of the key-stationary walk
+                  if (plain_q(m, first, n, dir, reps, q0) != jumped_q(m, first, n, dir, reps, q0) &&
+                      ++bad < 5)
+                    std::printf("mismatch (queries) zz=%d cp=%d c=%d reps=%d first=%d n=%d "
+                                "dir=%d k0=%d\n", zz, cp, c, reps, first, n, dir, q0);
                 }
       }
   std::printf("cases %ld mismatches %ld\n", cases, bad);
