@@ -7,7 +7,8 @@
 // with atomics (each output tile is summed by one CTA, in a fixed order):
 //
 //  dkdv_kernel  one CTA per 128-row K/V tile (K/V stationary in shared memory).
-//               It walks the query tiles that can see it, in the order the
+//               Its producer walks the query tiles that can see it (the other
+//               roles count them), in the order the
 //               chunk's gradient travels the ring (ranks s, s+1, ..., s-1), for
 //               every query head of its group, so the grouped-query sum over the
 //               n_rep heads (the reverse of RepeatKVHeads) happens in the TMEM
@@ -17,10 +18,13 @@
 //                 dS^T = P^T (dP^T - Delta)
 //                 dV += P^T dO, dK += dS^T Q          (TS MMAs, P^T/dS^T in TMEM)
 //               TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
-//  dq_kernel    one CTA per 128-row query tile (Q, dO stationary), walking the
-//               K/V tiles in ring order like the forward:
+//  dq_kernel    persistent CTAs over 128-row query tiles (Q, dO stationary),
+//               walking the K/V tiles in ring order like the forward:
 //                 S = Q K^T, dP = dO V^T, dS = P (dP - Delta), dQ += dS K.
 //               TMEM: S [0,128), dP double-buffered [128,384), dQ [384, 384+D).
+//               Launched after the dK/dV kernel; when nothing is queued between
+//               them, as its programmatic dependent, so it overlaps that kernel's
+//               last CTAs, its CTAs claiming their query tiles from a counter.
 //
 // Delta = rowsum(dO * O) comes from the pre-pass kernel (merge.cu).  Compute
 // warps: 8, warp w handles TMEM lane quadrant w%4 and column half (w-4)/4.
