@@ -94,3 +94,36 @@ def test_allgather_equals_ring():
         assert torch.allclose(lse, lse_ring[:, :, sl], atol=1e-4, rtol=0)
         assert (o.float() - o_ring[:, :, sl].float()).abs().max().item() <= 1e-2
     cp.check(cp.cpattn_check())
+
+
+def test_allgather_backward_is_deterministic():
+    """Each rank's dQ kernel overlaps the end of its dK/dV kernel and its CTAs claim
+    their query tiles from a counter, so which CTA computes a tile changes from run
+    to run; each tile is still computed the same way, and the K/V sums get one float32
+    addition per element per rank in rank order.  Two runs give identical bits."""
+    cp = cp_mod()
+    w = CASES[0]
+    _, lay = ring_inputs(w)
+    ql, kl, vl, dol = lay
+    desc = desc_of(w)
+    c = w.T // w.cp
+    ws = torch.empty(cp.cpattn_allgather_bwd_workspace(desc), dtype=torch.uint8, device=dev())
+
+    def run():
+        dk_sum = torch.empty(w.B, w.H_kv, w.T, w.D, dtype=torch.float32, device=dev())
+        dv_sum = torch.empty_like(dk_sum)
+        dqs = []
+        for r in range(w.cp):
+            o = torch.empty(w.B, w.H_q, c, w.D, dtype=ql.dtype, device=dev())
+            lse = torch.empty(w.B, w.H_q, c, dtype=torch.float32, device=dev())
+            cp.check(cp.cpattn_allgather_fwd(desc, r, ql, kl, vl, o, lse))
+            dq = torch.empty_like(o)
+            do_r = dol[:, :, r * c:(r + 1) * c].contiguous()
+            cp.check(cp.cpattn_allgather_bwd(desc, r, ql, kl, vl, o, lse, do_r, dq, dk_sum,
+                                             dv_sum, r > 0, ws))
+            dqs.append(dq)
+        cp.check(cp.cpattn_check())
+        return dqs + [dk_sum, dv_sum]
+
+    for a, b in zip(run(), run()):
+        assert torch.equal(a, b)
