@@ -191,3 +191,25 @@ def test_host_step_arguments_are_checked(cp):
     assert cp.cpattn_ring_step_host(d, *h, FAKE + 16, need, 0) == 1          # 256-byte alignment
     assert cp.cpattn_ring_step_host(d, *h[:8], 0, FAKE, need, 0) == 1        # null dv
     assert cp.cpattn_ring_step_host(_desc(cp, H_q=3), *h, FAKE, need, 0) == 1
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_header_compiles_on_its_own(tmp_path, lang, std):
+    """include/cpattn.h is a plain C header (no CUDA or torch types in the
+    signatures): it compiles alone, warning-free, as C99 and as C++17."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text('#include "cpattn.h"\n'
+                   'int main(void) {\n'
+                   '  cpattn_status (*f)(void*) = cpattn_check;\n'
+                   '  (void)f;\n'
+                   '  return 0;\n'
+                   '}\n')
+    r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), "-c", str(src),
+                        "-o", str(tmp_path / "use.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
